@@ -1,0 +1,153 @@
+"""Oracle: per-head budgets (Max-Min shifting) and work schedules (LPT, naive).
+
+Test infrastructure only (see the package docstring).  Integer arithmetic in
+Python ints, written step by step as the pages describe it.
+
+Budget unit (a reading; the pages speak of a "token budget"): k_h is the number
+of KV blocks kept per query-block row, capped at the row's causal block count
+i+1, with the two mandatory blocks (sink block 0 and the diagonal block i)
+counted inside it.
+"""
+from __future__ import annotations
+
+import heapq
+
+import numpy as np
+
+
+def causal_blocks(nb: int) -> int:
+    """Number of (i, j) block pairs with j <= i in an nb x nb causal grid."""
+    return nb * (nb + 1) // 2
+
+
+def kept_blocks(k: int, nb: int) -> int:
+    """Blocks kept over all rows when every row i keeps min(k, i+1) blocks."""
+    return int(np.minimum(k, np.arange(1, nb + 1)).sum())
+
+
+def density(k: int, nb: int) -> float:
+    """Fraction of causal blocks kept by a per-row budget of k blocks."""
+    return kept_blocks(k, nb) / causal_blocks(nb)
+
+
+def density_table(nb: int) -> np.ndarray:
+    """density(k, nb) for k = 1..nb (entry k-1)."""
+    rows = np.arange(1, nb + 1)
+    kept = np.minimum(rows[:, None], rows[None, :]).sum(axis=1)   # k along axis 0
+    return kept / causal_blocks(nb)
+
+
+def budget_for_density(target: float, nb: int) -> int:
+    """The k in [1, nb] whose density is nearest the target; ties -> smaller k.
+
+    This is how "X% of causal blocks" becomes an integer per-row budget (a
+    reading: the pages give budgets only as fractions).
+    """
+    err = np.abs(density_table(nb) - target)
+    return int(np.argmin(err)) + 1          # argmin takes the first (smaller k)
+
+
+def maxmin_shift(k_uniform: int, demand: list[int], k_min: int, nb: int) -> list[int]:
+    """Max-Min budget shifting (S-HPLB, "Strategia Max-Min (Budget Shifting)";
+    Chinese summary 2.1 "最大-最小预算迁移策略").
+
+    Every head starts at the uniform budget.  Budget then moves, one block at a
+    time, from the head with the most budget to spare relative to its demand
+    (a high-sparsity head) to the head that is shortest of its demand (a
+    low-sparsity head); the total never changes.  Reading of the stopping
+    rule: the donor is argmax_h (k_h - d_h) over heads above k_min, the
+    receiver argmin_h (k_h - d_h) over heads below nb, ties to the lowest h;
+    stop once the donor's surplus exceeds the receiver's by at most one.  The
+    result maximises min_h (k_h - d_h) with surpluses levelled to within one.
+    """
+    H = len(demand)
+    k = [k_uniform] * H
+    while True:
+        surplus = [k[h] - demand[h] for h in range(H)]
+        donor = -1
+        for h in range(H):
+            if k[h] > k_min and (donor < 0 or surplus[h] > surplus[donor]):
+                donor = h
+        receiver = -1
+        for h in range(H):
+            if k[h] < nb and (receiver < 0 or surplus[h] < surplus[receiver]):
+                receiver = h
+        if donor < 0 or receiver < 0:
+            break
+        if surplus[donor] - surplus[receiver] <= 1:
+            break
+        k[donor] -= 1
+        k[receiver] += 1
+    return k
+
+
+def item_costs(budgets: list[int], nb: int) -> list[int]:
+    """Cost of work item (h, i), id h*nb+i: the blocks it attends, min(k_h, i+1).
+
+    Reading: the pages balance by the per-head budget; on one GPU the work unit
+    is a (head, query-block) item whose budget in blocks is capped by
+    causality.
+    """
+    costs = []
+    for h in range(len(budgets)):
+        for i in range(nb):
+            costs.append(min(budgets[h], i + 1))
+    return costs
+
+
+def lpt_assign(order: list[int], costs: list[int], workers: int):
+    """Greedy longest-first assignment (S-HPLB "Algoritmo Greedy"; Chinese
+    summary 2.2 "贪心启发式算法"): walk the items in the given order and give
+    each to the currently least-loaded worker (ties: lowest worker id)."""
+    heap = [(0, w) for w in range(workers)]
+    lists = [[] for _ in range(workers)]
+    loads = [0] * workers
+    for item in order:
+        load, w = heapq.heappop(heap)
+        lists[w].append(item)
+        loads[w] = load + costs[item]
+        heapq.heappush(heap, (loads[w], w))
+    return lists, loads
+
+
+def schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int = 1):
+    """Work lists of (head, query-block) items for ``workers`` persistent workers.
+
+    policy:
+      "lpt"         items sorted by cost, descending (ties: lower item id), then
+                    greedy least-loaded assignment -- the pages' heuristic.
+      "lpt_grouped" the same greedy, but items are walked KV group by KV group
+                    (g = h // group ascending; within a group cost descending,
+                    ties lower id).  All workers then finish each group at
+                    nearly the same time.
+      "head_order"  the naive baseline of the Chinese summary ("电脑 1 拿头
+                    1-4"): items in id order cut into W contiguous chunks of
+                    equal count; chunk w is [w*N//W, (w+1)*N//W).
+    Returns (wptr, items, loads): CSR offsets [W+1], item ids in each worker's
+    processing order, and per-worker total cost.
+    """
+    costs = item_costs(budgets, nb)
+    n = len(costs)
+    if policy == "head_order":
+        lists = []
+        for w in range(workers):
+            lists.append(list(range(w * n // workers, (w + 1) * n // workers)))
+        loads = [sum(costs[x] for x in lst) for lst in lists]
+    elif policy == "lpt":
+        order = sorted(range(n), key=lambda x: (-costs[x], x))
+        lists, loads = lpt_assign(order, costs, workers)
+    elif policy == "lpt_grouped":
+        order = sorted(range(n), key=lambda x: ((x // nb) // group, -costs[x], x))
+        lists, loads = lpt_assign(order, costs, workers)
+    else:
+        raise ValueError(policy)
+    wptr = [0]
+    items = []
+    for lst in lists:
+        items.extend(lst)
+        wptr.append(len(items))
+    return wptr, items, loads
+
+
+def makespan(loads: list[int]) -> int:
+    return max(loads) if loads else 0
