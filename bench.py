@@ -1,0 +1,452 @@
+"""Benchmark: one block-sparse attention prefill layer (score -> select ->
+forward) of the 128K-token Llama-3.1-8B-shaped workload on one GB300, through
+the C ABI.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the hot path over the layer: pooled block scoring,
+per-head top-k selection and block-sparse attention on the persistent LPT
+schedule.  Budgets and the schedule are the offline plan (built once from the
+stored calibration profile, as the pages' offline profiling prescribes; its
+host time is reported separately and is inside the end-to-end number).
+Inputs (Q 1.07 GB, K and V 0.27 GB each) are larger than L2, so no flush is
+needed between steps.  With N > 1 (torchrun) every rank runs an independent
+replica (the path has no exchange step), timing is the max over ranks and
+value is the sum of the replicas' work over that time.
+
+--impl reference times the fp64 oracle on the host cores on a bounded sample
+of the same workload (a few heads of scoring and selection plus a sample of
+attention items per step), scaled to the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "block-sparse attn ms/layer + TFLOP/s at 128K prefill; % of roofline (1 GB300)"
+UNIT = "TFLOP/s"
+WORKLOAD = 3
+DECODE_WORKLOAD = 5
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _profile(number):
+    with open(os.path.join(ROOT, "workloads", "demands.json")) as f:
+        return json.load(f)[str(number)]
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _attention_flops(total_blocks: int, B: int, d: int) -> float:
+    # QK^T and PV over full B x B tiles of every selected block
+    return 4.0 * B * B * d * total_blocks
+
+
+def _score_flops(w) -> float:
+    return 2.0 * w.num_q_heads * (w.nb * (w.nb + 1) / 2) * w.head_dim
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import head_heterogeneous_block_gb300 as sa
+    from head_heterogeneous_block_gb300.layer import DecodeStep, PrefillLayer
+    from workloads import generate, workload
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = workload(WORKLOAD)
+    prof = _profile(WORKLOAD)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    shape = sa.Shape.prefill(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim)
+
+    t0 = time.perf_counter()
+    layer = PrefillLayer(shape, prof["k_uniform"], demand=prof["demand"], k_min=prof["k_min"],
+                         num_workers=sms, schedule=args.schedule, device=dev)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    x = generate.prefill_inputs(w)
+    host = {n: torch.from_numpy(x[n].view(np.int16)).view(torch.bfloat16).pin_memory()
+            for n in "qkv"}
+    del x
+    t = {n: host[n].to(dev, non_blocking=True) for n in "qkv"}
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    flops = _attention_flops(layer.total_blocks, w.block, w.head_dim) + _score_flops(w)
+    attn_flops = _attention_flops(layer.total_blocks, w.block, w.head_dim)
+
+    def step():
+        layer(t["q"], t["k"], t["v"], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(layer.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(layer.dev_status.item())}")
+
+    # ---- timed region: K steps; the forward kernel is bracketed by its own
+    # events on the launching stream to measure its average duration.
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for k in range(args.steps):
+        layer.score(t["q"], t["k"], stream=stream)
+        layer.select(stream=stream)
+        ev[k][0].record(stream)
+        layer.attend(t["q"], t["k"], t["v"], stream=stream)
+        ev[k][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(stop)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_step = total_ms / args.steps
+    value = flops * ws * args.steps / (total_ms * 1e-3) / 1e12
+    status = int(layer.dev_status.item())
+
+    # ---- schedules: forward alone under each plan (same inputs, same idx)
+    sched = {}
+    for pol in ("lpt_grouped", "lpt", "head_order"):
+        p = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=prof["demand"],
+                                k_min=prof["k_min"], num_workers=sms, schedule=pol)
+        p.upload()
+        for _ in range(2):
+            sa.sparse_attn_forward(shape, p, t["q"], t["k"], t["v"], layer.idx, layer.cnt,
+                                   layer.kmax, layer.out, None, layer.dev_status, stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        a.record(stream)
+        for _ in range(reps):
+            sa.sparse_attn_forward(shape, p, t["q"], t["k"], t["v"], layer.idx, layer.cnt,
+                                   layer.kmax, layer.out, None, layer.dev_status, stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        inf = p.info()
+        sched[pol] = {"forward_ms": round(a.elapsed_time(b) / reps, 4),
+                      "makespan_blocks": inf["makespan"],
+                      "mean_load_blocks": round(inf["total_blocks"] / sms, 1)}
+        p.close()
+
+    # ---- end to end through the public API with host buffers
+    out_host = torch.empty((w.num_q_heads, w.seq_len, w.head_dim), dtype=torch.bfloat16,
+                           pin_memory=True)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in "qkv")
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(2, min(args.steps, 5))
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    for _ in range(e2e_steps):
+        plan_e2e = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=prof["demand"],
+                                       k_min=prof["k_min"], num_workers=sms,
+                                       schedule=args.schedule)
+        plan_e2e.close()
+        dq = host["q"].to(dev, non_blocking=True)
+        dk = host["k"].to(dev, non_blocking=True)
+        dv = host["v"].to(dev, non_blocking=True)
+        o = layer(dq, dk, dv, stream=stream)
+        out_host.copy_(o, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t1) / e2e_steps
+    e2e_value = flops / e2e_s / 1e12
+
+    # ---- decode step (workload 5), reported beside the prefill line
+    decode = None
+    if not args.no_decode:
+        decode = bench_decode(dev, stream)
+
+    peaks = _peaks()
+    achieved = attn_flops / (fwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, per-head query scales; calibrated budgets)",
+        "config": {"workload": w.name, "seq_len": w.seq_len, "block": w.block,
+                   "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "mean_density": round(
+                       layer.total_blocks / (w.num_q_heads * w.nb * (w.nb + 1) / 2), 5),
+                   "selected_blocks": layer.total_blocks, "schedule": args.schedule,
+                   "workers": sms, "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas{ws}"},
+        "ms_per_layer": round(ms_step, 4),
+        "forward_ms": round(fwd_ms, 4),
+        "plan_host_ms": round(plan_ms, 3),
+        "roofline": {"bound": "tensor", "kernel": "prefill_attention_kernel<128,128>",
+                     "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "peak_source": peaks["source"] + " bf16 burst", "traffic": None,
+                     "algorithmic_flops_per_launch": attn_flops},
+        "schedules": sched,
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if decode is not None:
+        line["decode"] = decode
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, sample_seconds=12.0)
+    if ws > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_decode(dev, stream):
+    import numpy as np
+    import torch
+
+    import head_heterogeneous_block_gb300 as sa
+    from head_heterogeneous_block_gb300.layer import DecodeStep
+    from workloads import generate, workload
+
+    w = workload(DECODE_WORKLOAD)
+    x = generate.decode_inputs(w)
+    t = {n: torch.from_numpy(x[n].view(np.int16)).view(torch.bfloat16).to(dev) for n in "qkv"}
+    kinds = generate.head_kinds(w)
+    shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                            w.batch)
+    step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
+                      device=dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step.build_cache(t["k"], stream=stream)
+    for _ in range(3):
+        step(t["q"], t["k"], t["v"], stream=stream)
+    # flush L2 between decode steps (the cache is 2 GB but one step touches
+    # ~0.5 GB, which would otherwise partly stay in L2)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    times, fwd = [], []
+    for _ in range(10):
+        flush.zero_()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        sa.sparse_attn_score(shape, t["q"], step.kbar, step.scores, None, 0, stream=stream)
+        sa.sparse_attn_select(shape, step.plan, step.scores, step.idx, step.cnt, step.kmax,
+                              stream=stream)
+        e1.record(stream)
+        sa.sparse_attn_forward(shape, step.plan, t["q"], t["k"], t["v"], step.idx, step.cnt,
+                               step.kmax, step.out, None, step.dev_status, stream=stream)
+        e2.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e2))
+        fwd.append(e1.elapsed_time(e2))
+    a.record(stream)
+    step.build_cache(t["k"], stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    # touched bytes: union of selected blocks per (sequence, kv head), K and V
+    idx = step.idx.view(w.batch, w.num_q_heads, step.kmax).cpu().numpy()
+    cnt = step.cnt.view(w.batch, w.num_q_heads).cpu().numpy()
+    G = w.group
+    blocks = 0
+    for bb in range(w.batch):
+        for g in range(w.num_kv_heads):
+            u = set()
+            for h in range(g * G, (g + 1) * G):
+                u.update(idx[bb, h, :cnt[bb, h]].tolist())
+            blocks += len(u)
+    kv_bytes = blocks * w.block * w.head_dim * 2 * 2
+    kbar_bytes = w.batch * w.num_kv_heads * w.nb * w.head_dim * 4
+    q_o = 2 * w.batch * w.num_q_heads * w.head_dim * 2
+    fwd_ms = statistics.median(fwd)
+    peaks = _peaks()
+    return {"workload": w.name, "ms_per_step": round(statistics.median(times), 4),
+            "forward_ms": round(fwd_ms, 4),
+            "forward_gbs": round((kv_bytes + q_o) / (fwd_ms * 1e-3) / 1e9, 1),
+            "forward_frac_hbm": round((kv_bytes + q_o) / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "touched_kv_bytes": kv_bytes, "kbar_bytes": kbar_bytes,
+            "kcache_pool_ms": round(a.elapsed_time(b), 4), "l2": "flushed between steps"}
+
+
+def cpu_baseline(args, sample_seconds: float):
+    """The oracle, as it stands, on the host cores over a bounded sample."""
+    s = reference_sample(max(1, int(sample_seconds // 4)))
+    return {"value": s["value"], "unit": UNIT, "cores": s["cores"], "kind": "oracle",
+            "sample": s["sample"]}
+
+
+def reference_sample(steps: int):
+    """Time the fp64 oracle on a sample of the headline workload and express it
+    in the bench's unit (algorithmic TFLOP/s of the work actually done)."""
+    import numpy as np
+
+    from oracle import attention as oa
+    from oracle import plan as op
+    from workloads import generate, workload
+
+    w = workload(WORKLOAD)
+    prof = _profile(WORKLOAD)
+    budgets = op.maxmin_shift(prof["k_uniform"], prof["demand"], prof["k_min"], w.nb)
+    heads = [0]                                  # one head: pool, score, select in full
+    x = generate.prefill_inputs(w, heads=heads, kv_heads=[0])
+    q = generate.bf16_to_f32(x["q"][0])
+    k = generate.bf16_to_f32(x["k"][0])
+    v = generate.bf16_to_f32(x["v"][0])
+    rng = np.random.default_rng(0)
+    items_per_step = 24
+    flops = 0.0
+    t0 = time.perf_counter()
+    for s in range(steps):
+        qb = oa.pool_blocks(q[None], w.block)
+        kb = oa.pool_blocks(k[None], w.block)
+        sc = oa.block_scores(qb, kb, 1)
+        rows = rng.integers(0, w.nb, items_per_step)
+        for i in rows:
+            sel = oa.select_row(sc[0, i], int(i), budgets[0])
+            oa.attend_item(q, k, v, int(i), sel, w.block)
+            flops += _attention_flops(len(sel), w.block, w.head_dim)
+        flops += 2.0 * (w.nb * (w.nb + 1) / 2) * w.head_dim
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(flops / dt / 1e12, 6), "seconds": dt, "cores": cores,
+            "sample": f"{steps} x (head 0: pool+score {w.nb}x{w.nb} blocks, "
+                      f"{items_per_step} random query blocks selected and attended) of "
+                      f"{w.name}; fp64 numpy (BLAS threads)"}
+
+
+def run_reference(args):
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    from workloads import workload
+    w = workload(WORKLOAD)
+    per = []
+    for _ in range(args.warmup):
+        reference_sample(1)
+    t0 = time.perf_counter()
+    res = [reference_sample(1) for _ in range(args.steps)]
+    total = time.perf_counter() - t0
+    value = statistics.mean(r["value"] for r in res)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16)", "impl": "reference",
+        "config": {"workload": w.name, "seq_len": w.seq_len, "block": w.block,
+                   "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                         "cores": res[0]["cores"], "sample": res[0]["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--schedule", default="lpt_grouped",
+                    choices=["lpt", "lpt_grouped", "head_order"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+// C ABI entry points that touch the device: plan upload, score, select,
+// forward and the decode key-cache pooling.  Arguments are validated on the
+// host before anything is launched; the kernels live in score.cu, select.cu,
+// prefill.cu and decode.cu.
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "kernels.h"
+#include "plan_impl.h"
+#include "sparse_attn.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool same_shape(const sa_shape* a, const sa_shape& b) {
+  return a->seq_len == b.seq_len && a->block == b.block && a->num_q_heads == b.num_q_heads &&
+         a->num_kv_heads == b.num_kv_heads && a->head_dim == b.head_dim &&
+         a->batch == b.batch && a->mode == b.mode;
+}
+
+void free_device(sa_plan* p) {
+  if (p->device >= 0) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    cudaFree(p->d_budgets);
+    cudaFree(p->d_kinds);
+    cudaFree(p->d_wptr);
+    cudaFree(p->d_items);
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+  }
+  p->d_budgets = nullptr;
+  p->d_kinds = nullptr;
+  p->d_wptr = nullptr;
+  p->d_items = nullptr;
+  p->device = -1;
+}
+
+sa_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SA_OK;
+  if (e == cudaErrorMemoryAllocation) return SA_ERR_NO_MEMORY;
+  return SA_ERR_CUDA;
+}
+
+int64_t nblocks(const sa_shape* s) { return s->seq_len / s->block; }
+
+}  // namespace
+
+extern "C" {
+
+sa_status sparse_attn_plan_upload(sa_plan* plan, sa_stream_t stream) {
+  if (!plan) return SA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  free_device(plan);
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+  const size_t nh = plan->budgets.size();
+  const size_t nw = plan->wptr.size();
+  const size_t ni = plan->items.size();
+  cudaError_t e = cudaMalloc(&plan->d_budgets, nh * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&plan->d_kinds, nh);
+  if (e == cudaSuccess) e = cudaMalloc(&plan->d_wptr, nw * sizeof(int32_t));
+  if (e == cudaSuccess && ni) e = cudaMalloc(&plan->d_items, ni * sizeof(int32_t));
+  plan->device = dev;
+  if (e != cudaSuccess) {
+    free_device(plan);
+    return cuda_status(e);
+  }
+  e = cudaMemcpyAsync(plan->d_budgets, plan->budgets.data(), nh * sizeof(int32_t),
+                      cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(plan->d_kinds, plan->kinds.data(), nh, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(plan->d_wptr, plan->wptr.data(), nw * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && ni)
+    e = cudaMemcpyAsync(plan->d_items, plan->items.data(), ni * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    free_device(plan);
+    return cuda_status(e);
+  }
+  return SA_OK;
+}
+
+void sparse_attn_plan_destroy(sa_plan* plan) {
+  if (!plan) return;
+  free_device(plan);
+  delete plan;
+}
+
+sa_status sparse_attn_score_workspace_size(const sa_shape* shp, size_t* bytes) {
+  if (!bytes) return SA_ERR_INVALID_ARG;
+  sa_status st = sa_host::check_shape(shp);
+  if (st != SA_OK) return st;
+  if (shp->mode == SA_MODE_DECODE) {
+    *bytes = 0;
+    return SA_OK;
+  }
+  const size_t n = size_t(shp->num_q_heads + shp->num_kv_heads) * size_t(nblocks(shp)) *
+                   size_t(shp->head_dim) * sizeof(float);
+  *bytes = (n + 255) & ~size_t(255);
+  return SA_OK;
+}
+
+sa_status sparse_attn_score(const sa_shape* shp, const void* q, const void* k, float* scores,
+                            void* ws, size_t ws_bytes, sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!q || !k || !scores) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(scores)) return SA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int nb = int(nblocks(shp));
+  const int d = shp->head_dim;
+  const int G = shp->num_q_heads / shp->num_kv_heads;
+  const float scale = float(1.0 / std::sqrt(double(d)));
+  if (shp->mode == SA_MODE_DECODE) {
+    return cuda_status(sa_k::launch_decode_scores(q, static_cast<const float*>(k), scores,
+                                                  shp->batch, shp->num_q_heads, G, nb, d, scale,
+                                                  st));
+  }
+  size_t need = 0;
+  sparse_attn_score_workspace_size(shp, &need);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return SA_ERR_INVALID_ARG;
+  float* qbar = static_cast<float*>(ws);
+  float* kbar = qbar + size_t(shp->num_q_heads) * nb * d;
+  cudaError_t e = sa_k::launch_pool(q, qbar, int64_t(shp->num_q_heads) * nb, shp->block, d, st);
+  if (e == cudaSuccess)
+    e = sa_k::launch_pool(k, kbar, int64_t(shp->num_kv_heads) * nb, shp->block, d, st);
+  if (e == cudaSuccess)
+    e = sa_k::launch_prefill_scores(qbar, kbar, scores, shp->num_q_heads, G, nb, d, scale, st);
+  return cuda_status(e);
+}
+
+sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const float* scores,
+                             int32_t* idx, int32_t* cnt, int32_t kmax, sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!plan || !scores || !idx || !cnt) return SA_ERR_INVALID_ARG;
+  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+  if (kmax < plan->kmax) return SA_ERR_SHAPE;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  sa_k::SelectArgs a;
+  a.scores = scores;
+  a.budgets = plan->d_budgets;
+  a.kinds = plan->d_kinds;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.kmax = kmax;
+  a.nb = plan->nb;
+  a.Hq = shp->num_q_heads;
+  a.decode = shp->mode == SA_MODE_DECODE;
+  a.rows = a.decode ? shp->batch * shp->num_q_heads : shp->num_q_heads * plan->nb;
+  a.window_blocks = plan->window_blocks;
+  return cuda_status(sa_k::launch_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const void* q,
+                              const void* k, const void* v, const int32_t* idx,
+                              const int32_t* cnt, int32_t kmax, void* o, float* lse,
+                              int32_t* dev_status, sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!q || !k || !v || !idx || !cnt || !o || !dev_status || kmax < 1) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (shp->mode == SA_MODE_DECODE) {
+    if (plan && !same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+    sa_k::DecodeArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.idx = idx;
+    a.cnt = cnt;
+    a.kmax = kmax;
+    a.Bt = shp->batch;
+    a.Hq = shp->num_q_heads;
+    a.Hkv = shp->num_kv_heads;
+    a.L = int(shp->seq_len);
+    a.B = shp->block;
+    a.d = shp->head_dim;
+    a.o = o;
+    a.lse = lse;
+    a.dev_status = dev_status;
+    return cuda_status(sa_k::launch_decode_attention(a, st));
+  }
+  if (!plan) return SA_ERR_INVALID_ARG;
+  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  sa_k::PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.kmax = kmax;
+  a.wptr = plan->d_wptr;
+  a.items = plan->d_items;
+  a.num_workers = plan->num_workers;
+  a.num_items = shp->num_q_heads * plan->nb;
+  a.S = int(shp->seq_len);
+  a.B = shp->block;
+  a.d = shp->head_dim;
+  a.Hq = shp->num_q_heads;
+  a.Hkv = shp->num_kv_heads;
+  a.o = o;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  bool encode_failed = false;
+  cudaError_t e = sa_k::launch_prefill_attention(a, st, &encode_failed);
+  if (encode_failed) return SA_ERR_CUDA;
+  return cuda_status(e);
+}
+
+sa_status sparse_attn_pool_kcache(const sa_shape* shp, const void* k, float* kbar,
+                                  sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (shp->mode != SA_MODE_DECODE) return SA_ERR_INVALID_ARG;
+  if (!k || !kbar || !aligned16(k) || !aligned16(kbar)) return SA_ERR_INVALID_ARG;
+  const int64_t rows = int64_t(shp->batch) * shp->num_kv_heads * nblocks(shp);
+  return cuda_status(sa_k::launch_pool(k, kbar, rows, shp->block, shp->head_dim,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

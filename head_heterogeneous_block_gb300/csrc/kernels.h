@@ -1,0 +1,73 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sa_k {
+
+// Mean of each block of `block` rows: x [rows*block][d] bf16 -> out [rows][d] fp32.
+cudaError_t launch_pool(const void* x, float* out, int64_t rows, int block, int d,
+                        cudaStream_t st);
+
+// Prefill block scores for j <= i (scores [Hq][nb][nb], upper part untouched).
+cudaError_t launch_prefill_scores(const float* qbar, const float* kbar, float* scores, int Hq,
+                                  int group, int nb, int d, float scale, cudaStream_t st);
+
+// Decode scores [Bt][Hq][nb] from q [Bt][Hq][d] (bf16) and kbar [Bt][Hkv][nb][d].
+cudaError_t launch_decode_scores(const void* q, const float* kbar, float* scores, int Bt,
+                                 int Hq, int group, int nb, int d, float scale,
+                                 cudaStream_t st);
+
+struct SelectArgs {
+  const float* scores;
+  const int32_t* budgets;   // [Hq] device
+  const uint8_t* kinds;     // [Hq] device
+  int32_t* idx;
+  int32_t* cnt;
+  int32_t kmax;
+  int32_t nb;
+  int32_t Hq;
+  int32_t rows;             // Hq*nb (prefill) or Bt*Hq (decode)
+  int32_t decode;           // 0 / 1
+  int32_t window_blocks;    // decode streaming heads
+};
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
+
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int32_t* idx;
+  const int32_t* cnt;
+  int32_t kmax;
+  const int32_t* wptr;      // [W+1] device
+  const int32_t* items;     // [N] device
+  int32_t num_workers;
+  int32_t num_items;
+  int32_t S, B, d, Hq, Hkv;
+  void* o;
+  float* lse;
+  int32_t* dev_status;
+};
+// Returns cudaSuccess, or an error; *encode_failed is set when a TMA
+// descriptor could not be built.
+cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t st, bool* encode_failed);
+
+struct DecodeArgs {
+  const void* q;            // [Bt][Hq][d]
+  const void* k;            // [Bt][Hkv][L][d]
+  const void* v;
+  const int32_t* idx;       // [Bt*Hq][kmax]
+  const int32_t* cnt;
+  int32_t kmax;
+  int32_t Bt, Hq, Hkv, L, B, d;
+  void* o;
+  float* lse;
+  int32_t* dev_status;
+};
+cudaError_t launch_decode_attention(const DecodeArgs& a, cudaStream_t st);
+
+}  // namespace sa_k

@@ -1,0 +1,187 @@
+// Index step: block mean-pooling and pooled block scores.
+//
+// Block granularity follows "Riepilogo Tecnico: Fluxion" ("Accoppiamento
+// Granularità-Budget") and the Index operation of Spin ("Abstracción de
+// Partición Unificada"); the block summary (the mean) is a reading.
+//
+// pool_kernel      HBM-bound: every block of B rows x d bf16 is read once with
+//                  16-byte loads, summed in fp32 and scaled by 1/B.
+// prefill_scores   S[h,i,j] = qbar[h,i] . kbar[g,j] * scale for j <= i; a
+//                  64x64 fp32 SIMT tile per CTA over the lower triangle (the
+//                  contraction is small -- d = 128 -- and selection needs fp32
+//                  accuracy, so no reduced-precision tensor path).
+// decode_scores    scores[b,h,j] = q[b,h] . kbar[b,g,j] * scale; one warp per
+//                  pooled key row serves all G query heads of the group.
+
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace {
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = __uint_as_float(w[k] << 16);
+    f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+
+// One CTA per pooled row: x rows [r*B, (r+1)*B) of width d -> out[r][0..d).
+template <int D>
+__global__ void __launch_bounds__(256) pool_kernel(const uint4* __restrict__ x,
+                                                   float* __restrict__ out, int block) {
+  constexpr int kVec = D / 8;                 // 16-byte vectors per row
+  constexpr int kGroups = 256 / kVec;         // rows handled in parallel
+  __shared__ float part[kGroups][D];
+  const int v = threadIdx.x % kVec;
+  const int g = threadIdx.x / kVec;
+  const size_t base = size_t(blockIdx.x) * block * kVec;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int r = g; r < block; r += kGroups) {
+    float f[8];
+    bf16x8_to_f32(__ldg(&x[base + size_t(r) * kVec + v]), f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] += f[k];
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) part[g][v * 8 + k] = acc[k];
+  __syncthreads();
+  const float inv = 1.f / float(block);
+  for (int c = threadIdx.x; c < D; c += 256) {
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < kGroups; ++q) s += part[q][c];
+    out[size_t(blockIdx.x) * D + c] = s * inv;
+  }
+}
+
+// 64x64 output tile per CTA, 256 threads, each 4x4 outputs; d in chunks of 32.
+constexpr int kT = 64, kKc = 32;
+
+__global__ void __launch_bounds__(256) prefill_scores_kernel(const float* __restrict__ qbar,
+                                                             const float* __restrict__ kbar,
+                                                             float* __restrict__ scores, int nb,
+                                                             int d, int group, float scale,
+                                                             int tiles) {
+  // blockIdx.x enumerates lower-triangle tile pairs (ti >= tj); blockIdx.y = head
+  int t = blockIdx.x, ti = 0;
+  while (t > ti) {
+    t -= ti + 1;
+    ++ti;
+  }
+  const int tj = t;
+  const int h = blockIdx.y;
+  const float* qh = qbar + size_t(h) * nb * d;
+  const float* kg = kbar + size_t(h / group) * nb * d;
+  __shared__ float sq[kKc][kT + 4];
+  __shared__ float sk[kKc][kT + 4];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4] = {};
+  for (int c0 = 0; c0 < d; c0 += kKc) {
+    for (int e = threadIdx.x; e < kT * kKc; e += 256) {
+      const int r = e / kKc, c = e % kKc;
+      const int qi = ti * kT + r, kj = tj * kT + r;
+      sq[c][r] = (qi < nb) ? qh[size_t(qi) * d + c0 + c] : 0.f;
+      sk[c][r] = (kj < nb) ? kg[size_t(kj) * d + c0 + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < kKc; ++c) {
+      float a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a[u] = sq[c][ty * 4 + u];
+        b[u] = sk[c][tx * 4 + u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(a[u], b[w], acc[u][w]);
+    }
+    __syncthreads();
+  }
+  (void)tiles;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int i = ti * kT + ty * 4 + u;
+    if (i >= nb) continue;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int j = tj * kT + tx * 4 + w;
+      if (j <= i) scores[(size_t(h) * nb + i) * nb + j] = acc[u][w] * scale;
+    }
+  }
+}
+
+// CTA = (64 pooled rows, kv head g, sequence b); 8 warps.  D = 128.
+constexpr int kDecRows = 64;
+constexpr int kMaxGroup = 16;
+
+__global__ void __launch_bounds__(256) decode_scores_kernel(const __nv_bfloat16* __restrict__ q,
+                                                            const float* __restrict__ kbar,
+                                                            float* __restrict__ scores, int Hq,
+                                                            int Hkv, int group, int nb,
+                                                            float scale) {
+  constexpr int D = 128;
+  __shared__ float sq[kMaxGroup][D];
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < group * D; e += 256) {
+    const int hh = e / D, c = e % D;
+    sq[hh][c] = __bfloat162float(q[(size_t(b) * Hq + g * group + hh) * D + c]);
+  }
+  __syncthreads();
+  const float4* kb = reinterpret_cast<const float4*>(kbar + (size_t(b) * Hkv + g) * nb * D);
+  for (int r = warp; r < kDecRows; r += 8) {
+    const int j = blockIdx.x * kDecRows + r;
+    if (j >= nb) break;
+    const float4 kv = __ldg(&kb[size_t(j) * (D / 4) + lane]);
+    for (int hh = 0; hh < group; ++hh) {
+      const float* qq = &sq[hh][lane * 4];
+      float s = kv.x * qq[0] + kv.y * qq[1] + kv.z * qq[2] + kv.w * qq[3];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) scores[(size_t(b) * Hq + g * group + hh) * nb + j] = s * scale;
+    }
+  }
+}
+
+}  // namespace
+
+namespace sa_k {
+
+cudaError_t launch_pool(const void* x, float* out, int64_t rows, int block, int d,
+                        cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const uint4* xv = static_cast<const uint4*>(x);
+  if (d == 128)
+    pool_kernel<128><<<unsigned(rows), 256, 0, st>>>(xv, out, block);
+  else if (d == 64)
+    pool_kernel<64><<<unsigned(rows), 256, 0, st>>>(xv, out, block);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_scores(const float* qbar, const float* kbar, float* scores, int Hq,
+                                  int group, int nb, int d, float scale, cudaStream_t st) {
+  const int tiles = (nb + kT - 1) / kT;
+  const dim3 grid(unsigned(tiles * (tiles + 1) / 2), unsigned(Hq));
+  prefill_scores_kernel<<<grid, 256, 0, st>>>(qbar, kbar, scores, nb, d, group, scale, tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_scores(const void* q, const float* kbar, float* scores, int Bt, int Hq,
+                                 int group, int nb, int d, float scale, cudaStream_t st) {
+  if (d != 128 || group > kMaxGroup) return cudaErrorInvalidValue;
+  const dim3 grid(unsigned((nb + kDecRows - 1) / kDecRows), unsigned(Hq / group), unsigned(Bt));
+  decode_scores_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(q), kbar, scores,
+                                             Hq, Hq / group, group, nb, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace sa_k

@@ -1,0 +1,90 @@
+"""Whole-layer drivers over the C ABI: buffers come from PyTorch, every step of
+the computation runs in libsparse_attn's kernels.
+
+``PrefillLayer``  Index -> Select -> Attention for one prefill layer
+                  (score, select, forward) on a plan built once per
+                  configuration (the offline profile gives the demands).
+``DecodeStep``    the same three calls for one decode step over an
+                  HBM-resident cache, with the pooled key cache built once.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (Shape, sparse_attn_forward, sparse_attn_plan, sparse_attn_pool_kcache,
+               sparse_attn_score, sparse_attn_score_workspace_size, sparse_attn_select)
+
+
+class PrefillLayer:
+    def __init__(self, shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
+                 num_workers: int | None = None, schedule="lpt_grouped", device="cuda",
+                 with_lse: bool = False):
+        dev = torch.device(device)
+        if num_workers is None:
+            num_workers = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.shape = shape
+        self.plan = sparse_attn_plan(shape, k_uniform, demand=demand, k_min=k_min,
+                                     num_workers=num_workers, schedule=schedule)
+        self.plan.upload()
+        info = self.plan.info()
+        self.kmax = info["kmax"]
+        self.total_blocks = info["total_blocks"]
+        H, nb, S, d = shape.num_q_heads, shape.nb, shape.seq_len, shape.head_dim
+        self.scores = torch.empty(H * nb * nb, dtype=torch.float32, device=dev)
+        ws = sparse_attn_score_workspace_size(shape)
+        self.ws = torch.empty(ws // 4 + 1, dtype=torch.float32, device=dev)
+        self.idx = torch.empty(H * nb * self.kmax, dtype=torch.int32, device=dev)
+        self.cnt = torch.empty(H * nb, dtype=torch.int32, device=dev)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.lse = torch.empty(H * S, dtype=torch.float32, device=dev) if with_lse else None
+        self.out = torch.empty(H, S, d, dtype=torch.bfloat16, device=dev)
+
+    def score(self, q, k, stream=None):
+        sparse_attn_score(self.shape, q, k, self.scores, self.ws, stream=stream)
+
+    def select(self, stream=None):
+        sparse_attn_select(self.shape, self.plan, self.scores, self.idx, self.cnt, self.kmax,
+                           stream=stream)
+
+    def attend(self, q, k, v, out=None, stream=None):
+        out = self.out if out is None else out
+        sparse_attn_forward(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax, out,
+                            self.lse, self.dev_status, stream=stream)
+        return out
+
+    def __call__(self, q, k, v, out=None, stream=None):
+        self.score(q, k, stream)
+        self.select(stream)
+        return self.attend(q, k, v, out, stream)
+
+
+class DecodeStep:
+    def __init__(self, shape: Shape, budget_blocks: int, head_kind, window_blocks: int,
+                 device="cuda", with_lse: bool = False):
+        dev = torch.device(device)
+        self.shape = shape
+        self.plan = sparse_attn_plan(shape, budget_blocks, head_kind=head_kind,
+                                     window_blocks=window_blocks, num_workers=1)
+        self.plan.upload()
+        self.kmax = self.plan.info()["kmax"]
+        Bt, H, Hkv, nb, d = (shape.batch, shape.num_q_heads, shape.num_kv_heads, shape.nb,
+                             shape.head_dim)
+        self.kbar = torch.empty(Bt * Hkv * nb * d, dtype=torch.float32, device=dev)
+        self.scores = torch.empty(Bt * H * nb, dtype=torch.float32, device=dev)
+        self.idx = torch.empty(Bt * H * self.kmax, dtype=torch.int32, device=dev)
+        self.cnt = torch.empty(Bt * H, dtype=torch.int32, device=dev)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.lse = torch.empty(Bt * H, dtype=torch.float32, device=dev) if with_lse else None
+        self.out = torch.empty(Bt, H, d, dtype=torch.bfloat16, device=dev)
+
+    def build_cache(self, k, stream=None):
+        sparse_attn_pool_kcache(self.shape, k, self.kbar, stream=stream)
+
+    def __call__(self, q, k, v, out=None, stream=None):
+        out = self.out if out is None else out
+        sparse_attn_score(self.shape, q, self.kbar, self.scores, None, 0, stream=stream)
+        sparse_attn_select(self.shape, self.plan, self.scores, self.idx, self.cnt, self.kmax,
+                           stream=stream)
+        sparse_attn_forward(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax, out,
+                            self.lse, self.dev_status, stream=stream)
+        return out

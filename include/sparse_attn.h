@@ -1,0 +1,247 @@
+/*
+ * sparse_attn.h -- C ABI of libsparse_attn: per-head-budget block-sparse
+ * attention on one GB300 (sm_103a).
+ *
+ * The library computes one attention layer with block-granularity top-k
+ * sparsity where every query head has its own block budget:
+ *
+ *   plan     per-head budgets by Max-Min budget shifting around a uniform
+ *            budget, and a greedy longest-first (LPT) schedule of
+ *            (head, query-block) work items over persistent workers.
+ *            Source: "S-HPLB: Efficient LLM Attention Serving via
+ *            Sparsity-Aware Head Parallelism Load Balance" -- Italian summary,
+ *            "Metodologia" A ("Strategia Max-Min (Budget Shifting)") and B
+ *            ("Algoritmo Greedy"); Chinese summary 2.1 and 2.2.
+ *   score    (Index) mean-pooled query-block x key-block scores.
+ *   select   (Select) per-row top-k_h blocks, always keeping the sink block 0
+ *            and the diagonal block.
+ *   forward  (Attention) online-softmax attention over only the selected
+ *            blocks, with grouped-query KV sharing.
+ *            The Index / Select / Attention split is the one of "Unifying
+ *            Sparse Attention with Hierarchical Memory for Scalable
+ *            Long-Context LLM Serving" (Spin), "Abstracción de Partición
+ *            Unificada"; block granularity, the sink block and the
+ *            streaming / retrieval head split are from "Riepilogo Tecnico:
+ *            Fluxion", "Intuizioni Chiave" 1 and 2.
+ *
+ * Conventions
+ *  - Every call returns sa_status; none aborts, throws or prints.
+ *  - Device pointers are caller-owned (allocated by the caller, e.g. by
+ *    PyTorch).  The library owns only the opaque sa_plan, including the
+ *    device copy of its schedule made by sparse_attn_plan_upload.
+ *  - Device calls are asynchronous on the given stream (NULL = the legacy
+ *    default stream).  Argument errors are reported before anything is
+ *    launched; errors the device detects (corrupt block indices, timeouts
+ *    of bounded waits) are OR-ed into a caller-supplied int32 status word
+ *    (SA_DEV_* bits) which the caller reads after synchronising.
+ *  - Layouts (row-major, contiguous, bfloat16 unless stated):
+ *      prefill  Q [Hq][S][d], K and V [Hkv][S][d], O [Hq][S][d];
+ *      decode   q [Bt][Hq][d], K and V [Bt][Hkv][L][d], o [Bt][Hq][d].
+ *    Query head h reads KV head h / (Hq/Hkv).  A block is B consecutive
+ *    tokens; nb = S / B (or L / B).
+ *  - Supported: bf16, d in {64, 128}; prefill B in {64, 128} with
+ *    B*d*2 bytes per block as a TMA box; decode B = 32; S % B == 0.
+ *    Other shapes return SA_ERR_UNSUPPORTED.
+ */
+#ifndef SPARSE_ATTN_H
+#define SPARSE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same type as cudaStream_t). */
+typedef struct CUstream_st* sa_stream_t;
+
+typedef enum sa_status {
+  SA_OK = 0,
+  SA_ERR_INVALID_ARG = 1,    /* null pointer, bad enum, out-of-range scalar */
+  SA_ERR_SHAPE = 2,          /* inconsistent sizes (S % B, Hq % Hkv, kmax) */
+  SA_ERR_UNSUPPORTED = 3,    /* valid but not implemented (d, B, mode)     */
+  SA_ERR_CUDA = 4,           /* a CUDA runtime / driver call failed        */
+  SA_ERR_DEVICE_CHECK = 5,   /* reserved: device status word reported bits */
+  SA_ERR_DEVICE_TIMEOUT = 6, /* reserved: a bounded device wait gave up    */
+  SA_ERR_NO_MEMORY = 7,      /* host or device allocation failed           */
+  SA_ERR_NOT_UPLOADED = 8    /* plan used on the device before upload      */
+} sa_status;
+
+enum { SA_MODE_PREFILL = 0, SA_MODE_DECODE = 1 };
+
+/* Work schedules of (head, query-block) items over persistent workers. */
+enum {
+  SA_SCHED_LPT = 0,          /* cost-descending greedy, least-loaded worker  */
+  SA_SCHED_LPT_GROUPED = 1,  /* the same greedy, walked KV group by KV group */
+  SA_SCHED_HEAD_ORDER = 2    /* naive: items in head order, equal chunks     */
+};
+
+enum { SA_HEAD_RETRIEVAL = 0, SA_HEAD_STREAMING = 1 };
+
+/* Bits of the device status word. */
+enum {
+  SA_DEV_BAD_INDEX = 1,      /* a block index outside [0, i] was clamped     */
+  SA_DEV_BAD_COUNT = 2,      /* a block count outside [1, min(kmax,i+1)]     */
+  SA_DEV_TIMEOUT = 4,        /* a bounded wait gave up; outputs are invalid  */
+  SA_DEV_BAD_ITEM = 8        /* a schedule entry outside the item range      */
+};
+
+typedef struct sa_shape {
+  int64_t seq_len;       /* S (prefill) or cache length L (decode)          */
+  int32_t block;         /* B, tokens per block                             */
+  int32_t num_q_heads;   /* Hq                                              */
+  int32_t num_kv_heads;  /* Hkv (divides Hq)                                */
+  int32_t head_dim;      /* d                                               */
+  int32_t batch;         /* decode: sequences Bt; prefill: must be 1        */
+  int32_t mode;          /* SA_MODE_PREFILL or SA_MODE_DECODE               */
+} sa_shape;
+
+typedef struct sa_plan_params {
+  const int32_t* demand;    /* [Hq] per-head block demand d_h from offline
+                               calibration, or NULL: all budgets = k_uniform.
+                               Prefill only (must be NULL for decode).      */
+  int32_t k_uniform;        /* uniform starting budget, blocks per row;
+                               k_min <= k_uniform <= max(nb, k_min)          */
+  int32_t k_min;            /* smallest budget a head may be shifted to; >= 2
+                               (the sink and diagonal blocks)               */
+  const uint8_t* head_kind; /* decode: [Hq] SA_HEAD_*; NULL = all retrieval.
+                               Must be NULL for prefill.                    */
+  int32_t window_blocks;    /* decode: recent blocks a streaming head keeps
+                               besides block 0 (>= 1 when any streaming)    */
+  int32_t num_workers;      /* prefill: persistent workers W >= 1; one CTA
+                               runs one worker                              */
+  int32_t schedule;         /* SA_SCHED_*                                   */
+} sa_plan_params;
+
+typedef struct sa_plan sa_plan;
+
+/* Text for a status code (static storage; never NULL). */
+const char* sa_status_string(sa_status status);
+
+/*
+ * sparse_attn_plan -- host only, no CUDA call.
+ * Budgets: start every head at k_uniform; while the head with the largest
+ * surplus k_h - d_h among heads above k_min exceeds the head with the
+ * smallest surplus among heads below nb by more than one, move one block
+ * from the first to the second (ties: lowest head).  The total is conserved.
+ * Schedule (prefill): item (h, i) has id h*nb+i and cost min(k_h, i+1)
+ * blocks; LPT walks items by cost descending (ties: lower id) and gives each
+ * to the least-loaded worker (ties: lowest worker); LPT_GROUPED walks KV
+ * group by KV group, cost descending inside a group; HEAD_ORDER gives worker
+ * w the contiguous id range [w*N/W, (w+1)*N/W).
+ * Decode: retrieval heads keep k_uniform blocks, streaming heads block 0
+ * plus the last window_blocks blocks; no schedule is built.
+ * On success *out owns a new plan (free with sparse_attn_plan_destroy).
+ * Errors: INVALID_ARG (null shp/params/out, bad enum, k_min < 2, k_uniform
+ * out of [k_min, max(nb, k_min)], W < 1, negative demand), SHAPE, UNSUPPORTED,
+ * NO_MEMORY.  *out is left untouched on error.
+ */
+sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* params,
+                           sa_plan** out);
+
+/*
+ * Sizes of a plan: workers W, items N (Hq*nb prefill, Bt*Hq decode), the
+ * idx row stride kmax it needs (max over heads of the blocks one row keeps),
+ * the total of all item costs in blocks, and the schedule's makespan (the
+ * largest worker load, in blocks).  Any output pointer may be NULL.
+ */
+sa_status sparse_attn_plan_info(const sa_plan* plan, int32_t* num_workers,
+                                int32_t* num_items, int32_t* kmax,
+                                int64_t* total_blocks, int64_t* makespan);
+
+/*
+ * Copy a plan's contents to host arrays (any may be NULL):
+ * budgets [Hq]; wptr [W+1] CSR offsets; items [N] item ids in each worker's
+ * processing order; loads [W] per-worker cost in blocks.  Decode plans have
+ * no schedule (W = 0): wptr gets {0}.
+ */
+sa_status sparse_attn_plan_get(const sa_plan* plan, int32_t* budgets,
+                               int32_t* wptr, int32_t* items, int64_t* loads);
+
+/*
+ * Copy the budgets, head kinds and schedule to the current CUDA device
+ * (device memory owned by the plan, freed by destroy).  Synchronises the
+ * stream before returning so host staging can be reused.  Required before
+ * sparse_attn_select / sparse_attn_forward.  Errors: INVALID_ARG, CUDA,
+ * NO_MEMORY.  Calling it again re-uploads.
+ */
+sa_status sparse_attn_plan_upload(sa_plan* plan, sa_stream_t stream);
+
+/* Free a plan and its device copy (NULL is a no-op). */
+void sparse_attn_plan_destroy(sa_plan* plan);
+
+/*
+ * Scratch bytes sparse_attn_score needs: prefill (Hq + Hkv) * nb * d * 4
+ * (pooled queries and keys, fp32) rounded up to 256; decode 0.
+ */
+sa_status sparse_attn_score_workspace_size(const sa_shape* shp, size_t* bytes);
+
+/*
+ * Index: pooled block scores.
+ * Prefill: qbar[h,i] and kbar[g,j] are fp32 means of the B rows of each block
+ *   (kept in ws); scores[h][i][j] = qbar[h,i] . kbar[h/G, j] / sqrt(d) for
+ *   j <= i, fp32, layout [Hq][nb][nb]; entries with j > i are not written.
+ *   q, k: bf16 Q and K.
+ * Decode: k is the pooled key cache kbar (fp32 [Bt][Hkv][nb][d], see
+ *   sparse_attn_pool_kcache); scores[b][h][j] = q[b,h] . kbar[b,h/G,j] /
+ *   sqrt(d), layout [Bt][Hq][nb]; ws may be NULL.
+ * The mean as the block summary is a reading: the pages select at block
+ * granularity but do not name the summary.
+ * Errors: INVALID_ARG (null pointers, ws_bytes too small), SHAPE,
+ * UNSUPPORTED, CUDA (launch failure).
+ */
+sa_status sparse_attn_score(const sa_shape* shp, const void* q, const void* k,
+                            float* scores, void* ws, size_t ws_bytes,
+                            sa_stream_t stream);
+
+/*
+ * Select: for prefill row (h, i) keep min(k_h, i+1) blocks: 0 and i always,
+ * then the highest-scoring of 1..i-1, ties to the lower index.  For decode
+ * retrieval heads the row is i = nb-1 with k_h = k_uniform; streaming heads
+ * get block 0 and the last window_blocks blocks.
+ * Outputs: idx [rows][kmax] int32, each row ascending and padded with -1;
+ * cnt [rows] int32; rows = Hq*nb (prefill, row h*nb+i) or Bt*Hq (decode,
+ * row b*Hq+h).  kmax must be >= the plan's kmax (sparse_attn_plan_info).
+ * Errors: INVALID_ARG, SHAPE (kmax too small, shape differs from the plan's),
+ * NOT_UPLOADED, CUDA.
+ */
+sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan,
+                             const float* scores, int32_t* idx, int32_t* cnt,
+                             int32_t kmax, sa_stream_t stream);
+
+/*
+ * Attention over the selected blocks.
+ * Prefill: o[h, t] = sum_u softmax_u(q[h,t] . k[g,u] / sqrt(d)) v[g,u] over
+ *   the keys u of the blocks idx[h*nb+i][0..cnt) with u <= t (only the
+ *   diagonal block is partly masked); online softmax in fp32, bf16 output.
+ *   Runs as a persistent kernel: one CTA per plan worker, walking that
+ *   worker's items in order (sm_103a: TMA loads, tcgen05 MMAs into TMEM).
+ * Decode: o[b,h] over the blocks of row b*Hq+h; plan may be NULL.
+ * lse (nullable): natural-log sum of exponentials per query row, fp32,
+ *   [Hq][S] (prefill) or [Bt][Hq] (decode).
+ * dev_status: device int32 the kernels OR SA_DEV_* bits into (not cleared by
+ *   the library); an out-of-range index or count is clamped and flagged, never
+ *   dereferenced.
+ * Errors: INVALID_ARG, SHAPE, UNSUPPORTED, NOT_UPLOADED, CUDA.
+ */
+sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan,
+                              const void* q, const void* k, const void* v,
+                              const int32_t* idx, const int32_t* cnt,
+                              int32_t kmax, void* o, float* lse,
+                              int32_t* dev_status, sa_stream_t stream);
+
+/*
+ * Decode: build the pooled key cache kbar[b][g][j] = mean of the B keys of
+ * block j (fp32, [Bt][Hkv][nb][d]) from K [Bt][Hkv][L][d].  Done once per
+ * cache; the retrieval heads' scores read it.
+ * Errors: INVALID_ARG, SHAPE, UNSUPPORTED, CUDA.
+ */
+sa_status sparse_attn_pool_kcache(const sa_shape* shp, const void* k,
+                                  float* kbar, sa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_ATTN_H */

@@ -1,0 +1,120 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI and
+compare it with the oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation on the GPU, fp64 oracle):
+  scores      rtol 1e-4, atol 1e-6 (fp32 dot products of 64-128 terms)
+  selection   bit-exact, except blocks whose oracle score lies within 1e-3
+              relative of the row's k-th (last kept) score
+  attention   max |O_gpu - O_ref| <= 1e-2 and sum|diff| / sum|O_ref| <= 2e-3,
+              the oracle run on the GPU's own selected blocks
+  lse         |lse_gpu - lse_ref| <= 2e-3 (natural log units)
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import attention as oa
+from workloads import generate
+
+MAX_ABS = 1e-2
+MEAN_REL = 2e-3
+SEL_REL = 1e-3
+LSE_ABS = 2e-3
+
+
+def to_dev(bits: np.ndarray, dev="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def pooled(bits: np.ndarray, B: int) -> np.ndarray:
+    """Oracle pooling one head at a time (keeps fp64 memory small)."""
+    out = np.empty((bits.shape[0], bits.shape[1] // B, bits.shape[2]))
+    for h in range(bits.shape[0]):
+        out[h] = oa.pool_blocks(generate.bf16_to_f32(bits[h])[None], B)[0]
+    return out
+
+
+def check_scores(gpu: np.ndarray, ref: np.ndarray, rows=None):
+    """gpu/ref [H, nb, nb]; only j <= i is defined."""
+    H, nb, _ = ref.shape
+    lower = np.tril(np.ones((nb, nb), dtype=bool))
+    for h in range(H):
+        g, r = gpu[h][lower], ref[h][lower]
+        np.testing.assert_allclose(g, r, rtol=1e-4, atol=1e-6)
+
+
+def check_selection_row(gpu_sel, ref_sel, scores_row, i):
+    """Threshold rule; returns the number of tolerated mismatches."""
+    g, r = set(int(x) for x in gpu_sel), set(int(x) for x in ref_sel)
+    assert len(gpu_sel) == len(ref_sel), (i, gpu_sel, ref_sel)
+    assert list(gpu_sel) == sorted(g), gpu_sel
+    assert 0 in g and i in g and all(0 <= j <= i for j in g)
+    diff = g ^ r
+    if not diff:
+        return 0
+    kept = [j for j in r if j not in (0, i)]
+    thr = min(scores_row[j] for j in kept)
+    for j in diff:
+        assert abs(scores_row[j] - thr) <= SEL_REL * abs(thr), (i, j, scores_row[j], thr)
+    return len(diff)
+
+
+def check_selection(idx, cnt, scores_ref, budgets, rows=None):
+    """idx [H, nb, kmax], cnt [H, nb] from the GPU against oracle selection on
+    the oracle's fp64 scores."""
+    H, nb = cnt.shape
+    tolerated = 0
+    rows = rows if rows is not None else [(h, i) for h in range(H) for i in range(nb)]
+    for h, i in rows:
+        assert cnt[h, i] == min(budgets[h], i + 1), (h, i, cnt[h, i])
+        ref = oa.select_row(scores_ref[h, i], i, budgets[h])
+        gsel = idx[h, i, :cnt[h, i]]
+        assert all(x == -1 for x in idx[h, i, cnt[h, i]:])
+        tolerated += check_selection_row(gsel, ref, scores_ref[h, i], i)
+    return tolerated
+
+
+def check_attention(out_gpu: np.ndarray, lse_gpu, x: dict, idx, cnt, B: int, items, group: int):
+    """out_gpu [Hq, S, d] float; x holds the bf16 bits; items: ids h*nb+i."""
+    nb = cnt.shape[1]
+    by_head = {}
+    for it in items:
+        by_head.setdefault(int(it) // nb, []).append(int(it) % nb)
+    num = den = 0.0
+    worst = 0.0
+    kv_cache = {}
+    for h, rows in sorted(by_head.items()):
+        g = h // group
+        if g not in kv_cache:
+            kv_cache.clear()
+            kv_cache[g] = (generate.bf16_to_f32(x["k"][g]), generate.bf16_to_f32(x["v"][g]))
+        k, v = kv_cache[g]
+        q = generate.bf16_to_f32(x["q"][h])
+        for i in rows:
+            blocks = [int(j) for j in idx[h, i, :cnt[h, i]]]
+            o, lse = oa.attend_item(q, k, v, i, blocks, B)
+            got = out_gpu[h, i * B:(i + 1) * B]
+            d = np.abs(got - o)
+            worst = max(worst, float(d.max()))
+            num += float(d.sum())
+            den += float(np.abs(o).sum())
+            if lse_gpu is not None:
+                lg = lse_gpu[h, i * B:(i + 1) * B]
+                assert np.abs(lg - lse).max() <= LSE_ABS, (h, i, np.abs(lg - lse).max())
+    assert worst <= MAX_ABS, f"max abs error {worst}"
+    assert num / den <= MEAN_REL, f"mean relative error {num / den}"
+    return worst, num / den
+
+
+def sample_items(budgets, nb, per_head: int, seed: int):
+    """First, last, heaviest (smallest i reaching the head's budget) and
+    random items of every head."""
+    r = np.random.default_rng(seed)
+    items = []
+    for h, k in enumerate(budgets):
+        pick = {0, nb - 1, min(nb - 1, k - 1)}
+        while len(pick) < min(per_head, nb):
+            pick.add(int(r.integers(0, nb)))
+        items += [h * nb + i for i in sorted(pick)]
+    return items

@@ -1,0 +1,208 @@
+"""The C-ABI library on the CPU: it loads, exports every declared symbol, its
+host-only planning matches the oracle bit for bit, and its argument checks
+return the documented status codes before anything touches a GPU."""
+import ctypes
+import json
+import os
+import random
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import head_heterogeneous_block_gb300 as sa
+    return sa
+
+
+def _declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(sa):
+    declared = _declared_functions()
+    assert {"sparse_attn_plan", "sparse_attn_score", "sparse_attn_select",
+            "sparse_attn_forward"} <= declared
+    out = subprocess.run(["nm", "-D", "--defined-only", sa.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    missing = declared - exported
+    assert not missing, missing
+    lib = ctypes.CDLL(sa.library_path())
+    for name in declared:
+        assert getattr(lib, name)
+
+
+def _oracle_plan(budgets_from, k_u, demand, k_min, nb, W, policy, G):
+    from oracle import plan as op
+    k = op.maxmin_shift(k_u, list(demand), k_min, nb) if demand is not None else [k_u] * budgets_from
+    wptr, items, loads = op.schedule(k, nb, W, policy, G)
+    return k, wptr, items, loads
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("policy", ["lpt", "lpt_grouped", "head_order"])
+def test_plan_matches_oracle_random(sa, seed, policy):
+    r = random.Random(seed)
+    Hkv = r.choice([1, 2, 4])
+    Hq = Hkv * r.choice([1, 2, 4])
+    B = 64
+    nb = r.randint(1, 40)
+    W = r.randint(1, 20)
+    k_min = 2
+    k_u = r.randint(k_min, max(k_min, nb)) if nb >= 2 else None
+    if k_u is None:
+        return
+    demand = [r.randint(0, nb + 3) for _ in range(Hq)] if seed % 3 else None
+    shape = sa.Shape.prefill(nb * B, B, Hq, Hkv, 64)
+    plan = sa.sparse_attn_plan(shape, k_u, demand=demand, k_min=k_min, num_workers=W,
+                               schedule=policy)
+    got = plan.get()
+    k, wptr, items, loads = _oracle_plan(Hq, k_u, demand, k_min, nb, W, policy, Hq // Hkv)
+    assert got["budgets"].tolist() == k
+    assert got["wptr"].tolist() == wptr
+    assert got["items"].tolist() == items
+    assert got["loads"].tolist() == loads
+    assert got["makespan"] == max(loads)
+    assert got["total_blocks"] == sum(loads)
+    assert got["kmax"] == max(min(x, nb) for x in k)
+
+
+@pytest.mark.parametrize("number", [1, 2, 3, 4])
+@pytest.mark.parametrize("policy", ["lpt", "lpt_grouped", "head_order"])
+def test_plan_matches_oracle_workloads(sa, number, policy):
+    from workloads import workload
+    w = workload(number)
+    prof = json.load(open(os.path.join(ROOT, "workloads", "demands.json")))[str(number)]
+    shape = sa.Shape.prefill(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim)
+    W = 152
+    plan = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=prof["demand"],
+                               k_min=prof["k_min"], num_workers=W, schedule=policy)
+    got = plan.get()
+    k, wptr, items, loads = _oracle_plan(w.num_q_heads, prof["k_uniform"], prof["demand"],
+                                         prof["k_min"], w.nb, W, policy, w.group)
+    assert got["budgets"].tolist() == k == prof["budgets_maxmin"]
+    assert got["wptr"].tolist() == wptr
+    assert np.array_equal(got["items"], np.array(items, np.int32))
+    assert got["loads"].tolist() == loads
+
+
+def test_plan_lpt_balances(sa):
+    from workloads import workload
+    w = workload(4)
+    prof = json.load(open(os.path.join(ROOT, "workloads", "demands.json")))["4"]
+    shape = sa.Shape.prefill(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim)
+    ms = {}
+    for pol in ["lpt", "lpt_grouped", "head_order"]:
+        ms[pol] = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=prof["demand"],
+                                      num_workers=152, schedule=pol).info()
+    lower = -(-ms["lpt"]["total_blocks"] // 152)
+    assert ms["lpt"]["makespan"] <= lower + 315
+    assert ms["lpt_grouped"]["makespan"] <= lower + 8 * 315
+    assert ms["head_order"]["makespan"] > 1.5 * ms["lpt"]["makespan"]
+
+
+def test_decode_plan(sa):
+    shape = sa.Shape.decode(65536, 32, 28, 4, 128, 16)
+    kinds = np.zeros(28, np.uint8)
+    kinds[[1, 5, 9]] = sa.SA_HEAD_STREAMING
+    plan = sa.sparse_attn_plan(shape, 64, head_kind=kinds, window_blocks=64, num_workers=1)
+    got = plan.get()
+    exp = np.where(kinds == 1, 65, 64)
+    assert got["budgets"].tolist() == exp.tolist()
+    assert got["kmax"] == 65 and got["num_items"] == 16 * 28 and got["num_workers"] == 0
+    assert got["total_blocks"] == 16 * int(exp.sum())
+
+
+def _raw_plan(sa, shape, params):
+    out = ctypes.c_void_p()
+    st = sa._lib.sparse_attn_plan(ctypes.byref(shape) if shape is not None else None,
+                                  ctypes.byref(params) if params is not None else None,
+                                  ctypes.byref(out))
+    if st == 0:
+        sa._lib.sparse_attn_plan_destroy(out)
+    return st
+
+
+def _params(sa, **kw):
+    p = sa._PlanParams()
+    p.k_uniform, p.k_min, p.num_workers, p.schedule = 4, 2, 8, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_plan_argument_errors(sa):
+    good = sa.Shape.prefill(1024, 64, 8, 2, 64)
+    assert _raw_plan(sa, good, _params(sa)) == 0
+    assert _raw_plan(sa, None, _params(sa)) == 1
+    assert _raw_plan(sa, good, None) == 1
+    assert _raw_plan(sa, good, _params(sa, k_min=1)) == 1
+    assert _raw_plan(sa, good, _params(sa, k_uniform=1)) == 1
+    assert _raw_plan(sa, good, _params(sa, k_uniform=17)) == 1          # > nb = 16
+    assert _raw_plan(sa, good, _params(sa, num_workers=0)) == 1
+    assert _raw_plan(sa, good, _params(sa, schedule=7)) == 1
+    assert _raw_plan(sa, sa.Shape.prefill(1000, 64, 8, 2, 64), _params(sa)) == 2   # S % B
+    assert _raw_plan(sa, sa.Shape.prefill(1024, 64, 6, 4, 64), _params(sa)) == 2   # Hq % Hkv
+    bad = sa.Shape.prefill(1024, 64, 8, 2, 64)
+    bad.batch = 2
+    assert _raw_plan(sa, bad, _params(sa)) == 2
+    neg = (ctypes.c_int32 * 8)(1, 2, 3, -1, 5, 6, 7, 8)
+    assert _raw_plan(sa, good, _params(sa, demand=ctypes.cast(neg, ctypes.POINTER(ctypes.c_int32)))) == 1
+    kinds = (ctypes.c_uint8 * 8)(*([0] * 8))
+    kp = ctypes.cast(kinds, ctypes.POINTER(ctypes.c_uint8))
+    assert _raw_plan(sa, good, _params(sa, head_kind=kp)) == 1            # kinds on prefill
+    dec = sa.Shape.decode(2048, 32, 8, 2, 128, 2)
+    kinds[3] = 1
+    assert _raw_plan(sa, dec, _params(sa, head_kind=kp, window_blocks=0)) == 1
+    assert _raw_plan(sa, dec, _params(sa, head_kind=kp, window_blocks=4)) == 0
+    kinds[2] = 5
+    assert _raw_plan(sa, dec, _params(sa, head_kind=kp, window_blocks=4)) == 1
+    assert sa.sa_status_string(3) == "unsupported shape or mode"
+
+
+def test_device_calls_reject_bad_arguments_before_launch(sa):
+    shape = sa.Shape.prefill(4096, 64, 8, 2, 64)
+    plan = sa.sparse_attn_plan(shape, 9, num_workers=4)
+    lib, P = sa._lib, 8192   # P: any non-null, 16-byte aligned fake address
+    s = ctypes.byref(shape)
+    # null inputs
+    assert lib.sparse_attn_score(s, None, P, P, P, 1 << 30, None) == 1
+    # workspace too small
+    assert lib.sparse_attn_score(s, P, P, P, P, 16, None) == 1
+    # unsupported head dim / block
+    s96 = sa.Shape.prefill(4096, 64, 8, 2, 96)
+    assert lib.sparse_attn_score(ctypes.byref(s96), P, P, P, P, 1 << 30, None) == 3
+    s32 = sa.Shape.prefill(4096, 32, 8, 2, 64)
+    assert lib.sparse_attn_score(ctypes.byref(s32), P, P, P, P, 1 << 30, None) == 3
+    # misaligned pointer
+    assert lib.sparse_attn_score(s, P + 2, P, P, P, 1 << 30, None) == 1
+    # select: plan not uploaded, kmax too small, shape mismatch
+    assert lib.sparse_attn_select(s, plan.handle, P, P, P, 9, None) == 8
+    assert lib.sparse_attn_select(s, plan.handle, P, P, P, 8, None) == 2
+    other = sa.Shape.prefill(8192, 64, 8, 2, 64)
+    assert lib.sparse_attn_select(ctypes.byref(other), plan.handle, P, P, P, 9, None) == 2
+    # forward: not uploaded, null status word
+    assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 9, P, None, P, None) == 8
+    assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 9, P, None, None, None) == 1
+    assert lib.sparse_attn_forward(s, None, P, P, P, P, P, 9, P, None, P, None) == 1
+    # pool_kcache is decode only
+    assert lib.sparse_attn_pool_kcache(s, P, P, None) == 1
+    n = ctypes.c_size_t()
+    assert lib.sparse_attn_score_workspace_size(s, ctypes.byref(n)) == 0
+    assert n.value == (8 + 2) * 64 * 64 * 4

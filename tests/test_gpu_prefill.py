@@ -1,0 +1,185 @@
+"""GPU parity of the prefill path (score -> select -> forward) against the
+oracle, through the C ABI.  Small cases are checked element by element; the
+full-size workloads run in the bench's launch configuration (one CTA per SM,
+LPT schedule) and are checked in full for plan, scores and selection and on
+sampled items for attention."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def env():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import head_heterogeneous_block_gb300 as sa
+    return sa, torch
+
+
+def _run(sa, torch, w, x, budgets_args, schedule="lpt", workers=None, with_lse=True):
+    from head_heterogeneous_block_gb300.layer import PrefillLayer
+    from tests._parity import to_dev
+    shape = sa.Shape.prefill(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim)
+    layer = PrefillLayer(shape, schedule=schedule, num_workers=workers, with_lse=with_lse,
+                         **budgets_args)
+    t = {n: to_dev(x[n]) for n in "qkv"}
+    out = layer(t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    H, nb, S = w.num_q_heads, w.nb, w.seq_len
+    res = {
+        "status": int(layer.dev_status.item()),
+        "scores": layer.scores.view(H, nb, nb).cpu().numpy(),
+        "idx": layer.idx.view(H, nb, layer.kmax).cpu().numpy(),
+        "cnt": layer.cnt.view(H, nb).cpu().numpy(),
+        "out": out.float().cpu().numpy(),
+        "lse": layer.lse.view(H, S).cpu().numpy() if with_lse else None,
+        "budgets": layer.plan.get()["budgets"].tolist(),
+        "layer": layer, "tensors": t,
+    }
+    return res
+
+
+def _oracle_scores(w, x):
+    from oracle import attention as oa
+    from tests._parity import pooled
+    return oa.block_scores(pooled(x["q"], w.block), pooled(x["k"], w.block), w.group)
+
+
+SMALL = [
+    # (workload number, seq_len, Hq, Hkv, budget mode)
+    (1, 4096, 8, 2, "calibrated"),
+    (1, 1024, 8, 8, "uniform"),        # G = 1
+    (1, 64, 4, 1, "uniform"),          # nb = 1
+    (1, 2368, 8, 2, "uniform"),        # nb = 37: ragged score tiles
+    (2, 4096, 8, 2, "shifted"),
+    (2, 8192, 16, 4, "shifted"),
+]
+
+
+@pytest.mark.parametrize("number,S,Hq,Hkv,mode", SMALL)
+def test_prefill_small_full_parity(env, number, S, Hq, Hkv, mode):
+    sa, torch = env
+    from oracle import plan as op
+    from tests import _parity as P
+    from workloads import generate, scaled, workload
+    w = scaled(workload(number), S, Hq, Hkv)
+    x = generate.prefill_inputs(w)
+    nb = w.nb
+    if mode == "calibrated":
+        prof = json.load(open(os.path.join(ROOT, "workloads", "demands.json")))[str(number)]
+        args = {"k_uniform": prof["k_uniform"], "demand": prof["demand"]}
+    elif mode == "uniform":
+        args = {"k_uniform": max(2, min(nb, op.budget_for_density(w.target_density, nb)))}
+    else:
+        k_u = op.budget_for_density(w.target_density, nb)
+        rng = np.random.default_rng(S)
+        args = {"k_uniform": k_u, "demand": rng.integers(1, nb, Hq).tolist()}
+    r = _run(sa, torch, w, x, args, workers=16)
+    assert r["status"] == 0
+    ref_scores = _oracle_scores(w, x)
+    P.check_scores(r["scores"], ref_scores)
+    P.check_selection(r["idx"], r["cnt"], ref_scores, r["budgets"])
+    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block,
+                      range(Hq * nb), w.group)
+
+
+@pytest.mark.parametrize("budget", ["dense", "sink_diag"])
+def test_prefill_special_cases(env, budget):
+    """k >= nb is dense causal attention; k = 2 keeps only sink + diagonal."""
+    sa, torch = env
+    from tests import _parity as P
+    from workloads import generate, scaled, workload
+    w = scaled(workload(2), 4096, 4, 2)
+    x = generate.prefill_inputs(w)
+    k = w.nb if budget == "dense" else 2
+    r = _run(sa, torch, w, x, {"k_uniform": k}, workers=7)
+    assert r["status"] == 0
+    for h in range(w.num_q_heads):
+        for i in range(w.nb):
+            exp = list(range(i + 1)) if budget == "dense" else sorted({0, i})
+            assert r["idx"][h, i, :r["cnt"][h, i]].tolist() == exp
+    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block,
+                      range(w.num_q_heads * w.nb), w.group)
+    if budget == "dense":
+        # against the library's dense causal attention as well
+        t = r["tensors"]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            t["q"].float()[None], t["k"].float().repeat_interleave(w.group, 0)[None],
+            t["v"].float().repeat_interleave(w.group, 0)[None], is_causal=True)[0]
+        assert float((ref - torch.from_numpy(r["out"]).cuda()).abs().max()) < 1e-2
+
+
+def test_schedules_give_identical_outputs(env):
+    sa, torch = env
+    from workloads import generate, scaled, workload
+    w = scaled(workload(2), 8192, 8, 2)
+    x = generate.prefill_inputs(w)
+    rng = np.random.default_rng(5)
+    args = {"k_uniform": 13, "demand": rng.integers(1, w.nb, 8).tolist()}
+    outs = {}
+    for sched, W in [("lpt", 152), ("lpt_grouped", 152), ("head_order", 152), ("lpt", 1),
+                     ("head_order", 300)]:
+        r = _run(sa, torch, w, x, args, schedule=sched, workers=W)
+        assert r["status"] == 0
+        outs[(sched, W)] = r["out"]
+    ref = outs[("lpt", 152)]
+    for key, o in outs.items():
+        assert np.array_equal(o, ref), key
+
+
+def test_corrupt_indices_are_flagged_not_dereferenced(env):
+    sa, torch = env
+    from workloads import generate, scaled, workload
+    w = scaled(workload(1), 2048, 4, 2)
+    x = generate.prefill_inputs(w)
+    r = _run(sa, torch, w, x, {"k_uniform": 6}, workers=4)
+    layer, t = r["layer"], r["tensors"]
+    assert r["status"] == 0
+    idx = layer.idx.view(w.num_q_heads, w.nb, layer.kmax)
+    cnt = layer.cnt.view(w.num_q_heads, w.nb)
+    idx[1, 20, 2] = 1 << 28          # far out of range
+    idx[2, 5, 1] = -7
+    cnt[3, 9] = layer.kmax + 50      # count beyond the row stride
+    layer.dev_status.zero_()
+    layer.attend(t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    st = int(layer.dev_status.item())
+    assert st & sa.SA_DEV_BAD_INDEX and st & sa.SA_DEV_BAD_COUNT
+    assert not st & sa.SA_DEV_TIMEOUT
+    assert torch.isfinite(layer.out.float()).all()
+
+
+FULL = [2, 3, 4]
+
+
+@pytest.mark.parametrize("number", FULL)
+def test_prefill_full_size(env, number):
+    """Full-size workloads in the bench's launch configuration."""
+    sa, torch = env
+    from oracle import attention as oa
+    from tests import _parity as P
+    from workloads import generate, workload
+    w = workload(number)
+    prof = json.load(open(os.path.join(ROOT, "workloads", "demands.json")))[str(number)]
+    x = generate.prefill_inputs(w)
+    W = torch.cuda.get_device_properties(0).multi_processor_count
+    r = _run(sa, torch, w, x, {"k_uniform": prof["k_uniform"], "demand": prof["demand"]},
+             schedule="lpt_grouped", workers=W)
+    assert r["status"] == 0
+    assert r["budgets"] == prof["budgets_maxmin"]
+    ref_scores = oa.block_scores(P.pooled(x["q"], w.block), P.pooled(x["k"], w.block), w.group)
+    # scores: all rows of a sample of heads; selection: every row
+    heads = sorted({0, w.num_q_heads - 1, 5 % w.num_q_heads})
+    P.check_scores(r["scores"][heads], ref_scores[heads])
+    P.check_selection(r["idx"], r["cnt"], ref_scores, r["budgets"])
+    items = P.sample_items(r["budgets"], w.nb, 16 if number == 4 else 64, seed=number)
+    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group)
