@@ -28,6 +28,7 @@ SA_SCHED_LPT, SA_SCHED_LPT_GROUPED, SA_SCHED_HEAD_ORDER = 0, 1, 2
 SCHEDULES = {"lpt": SA_SCHED_LPT, "lpt_grouped": SA_SCHED_LPT_GROUPED,
              "head_order": SA_SCHED_HEAD_ORDER}
 SA_HEAD_RETRIEVAL, SA_HEAD_STREAMING = 0, 1
+SA_DTYPE_BF16, SA_DTYPE_F32 = 0, 1
 SA_DEV_BAD_INDEX, SA_DEV_BAD_COUNT, SA_DEV_TIMEOUT, SA_DEV_BAD_ITEM = 1, 2, 4, 8
 
 
@@ -89,7 +90,7 @@ def _load():
         "sparse_attn_score": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, SZ, P]),
         "sparse_attn_select": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, I32, P]),
         "sparse_attn_forward": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P, P, I32,
-                                               P, P, P, P]),
+                                               P, I32, P, P, P]),
         "sparse_attn_pool_kcache": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -231,11 +232,23 @@ def sparse_attn_select(shape: Shape, plan: Plan, scores, idx, cnt, kmax: int, st
                                    _ptr(cnt), kmax, _stream(stream)), "sparse_attn_select")
 
 
+def _out_dtype(o, o_dtype):
+    if o_dtype is not None:
+        return o_dtype
+    name = str(getattr(o, "dtype", ""))
+    if name.endswith("float32"):
+        return SA_DTYPE_F32
+    if name.endswith("bfloat16"):
+        return SA_DTYPE_BF16
+    raise TypeError("output must be bfloat16 or float32 (or pass o_dtype)")
+
+
 def sparse_attn_forward(shape: Shape, plan, q, k, v, idx, cnt, kmax: int, o, lse, dev_status,
-                        stream=None):
+                        stream=None, o_dtype=None):
     _check(_lib.sparse_attn_forward(ctypes.byref(shape), plan.handle if plan else None, _ptr(q),
                                     _ptr(k), _ptr(v), _ptr(idx), _ptr(cnt), kmax, _ptr(o),
-                                    _ptr(lse), _ptr(dev_status), _stream(stream)),
+                                    _out_dtype(o, o_dtype), _ptr(lse), _ptr(dev_status),
+                                    _stream(stream)),
            "sparse_attn_forward")
 
 

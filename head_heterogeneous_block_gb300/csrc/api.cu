@@ -162,11 +162,13 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const flo
 
 sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const void* q,
                               const void* k, const void* v, const int32_t* idx,
-                              const int32_t* cnt, int32_t kmax, void* o, float* lse,
+                              const int32_t* cnt, int32_t kmax, void* o, int32_t o_dtype,
+                              float* lse,
                               int32_t* dev_status, sa_stream_t stream) {
   sa_status s = sa_host::check_supported(shp);
   if (s != SA_OK) return s;
   if (!q || !k || !v || !idx || !cnt || !o || !dev_status || kmax < 1) return SA_ERR_INVALID_ARG;
+  if (o_dtype != SA_DTYPE_BF16 && o_dtype != SA_DTYPE_F32) return SA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (shp->mode == SA_MODE_DECODE) {
@@ -185,6 +187,7 @@ sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const vo
     a.B = shp->block;
     a.d = shp->head_dim;
     a.o = o;
+    a.out_f32 = o_dtype == SA_DTYPE_F32;
     a.lse = lse;
     a.dev_status = dev_status;
     return cuda_status(sa_k::launch_decode_attention(a, st));
@@ -209,6 +212,7 @@ sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const vo
   a.Hq = shp->num_q_heads;
   a.Hkv = shp->num_kv_heads;
   a.o = o;
+  a.out_f32 = o_dtype == SA_DTYPE_F32;
   a.lse = lse;
   a.dev_status = dev_status;
   bool encode_failed = false;

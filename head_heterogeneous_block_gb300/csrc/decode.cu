@@ -119,13 +119,17 @@ __global__ void __launch_bounds__(kWarps * 32) decode_attention_kernel(sa_k::Dec
       for (int e = 0; e < 4; ++e) acc[e] += so[w][lane * 4 + e] * f;
     }
     const float inv = 1.f / L;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o) + size_t(row) * kD + lane * 4;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dst) = pk;
+    if (a.out_f32) {
+      float* dst = static_cast<float*>(a.o) + size_t(row) * kD + lane * 4;
+      *reinterpret_cast<float4*>(dst) =
+          make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    } else {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o) + size_t(row) * kD + lane * 4;
+      uint2 pk;
+      pk.x = sa_dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      pk.y = sa_dev::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(dst) = pk;
+    }
     if (a.lse && lane == 0) a.lse[row] = (M + log2f(L)) * 0.6931471805599453f;
   }
 }

@@ -49,6 +49,7 @@ struct PrefillArgs {
   int32_t num_items;
   int32_t S, B, d, Hq, Hkv;
   void* o;
+  int32_t out_f32;          // 1: o is fp32, 0: bf16
   float* lse;
   int32_t* dev_status;
 };
@@ -65,6 +66,7 @@ struct DecodeArgs {
   int32_t kmax;
   int32_t Bt, Hq, Hkv, L, B, d;
   void* o;
+  int32_t out_f32;
   float* lse;
   int32_t* dev_status;
 };

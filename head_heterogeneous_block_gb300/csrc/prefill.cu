@@ -62,7 +62,9 @@ struct Bars {
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_done, o_free, drain;
+  uint64_t o_done;   // one phase per P.V (waited only before an O rescale)
+  uint64_t o_last;   // one phase per item, after its last P.V (epilogue)
+  uint64_t o_free, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -74,7 +76,8 @@ struct Params {
   const int32_t* items;
   int32_t kmax, num_items, num_workers, nb, S, B, G;
   float scale_log2;
-  __nv_bfloat16* o;
+  void* o;
+  int32_t out_f32;
   float* lse;
   int32_t* dev_status;
 };
@@ -166,6 +169,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bars->k_empty[s], 1);
     }
     mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_last, 1);
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -311,6 +315,7 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
+        mma_commit(&bars->o_last);
         ++qi;
         ++items_done;
       }
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(192, 1)
     const int row = quarter * 32 + lane;          // query row within the tile
     const uint32_t lanes = tmem + (uint32_t(quarter * 32) << 16);
     const float c = p.scale_log2;
-    uint32_t kb = 0;
+    uint32_t kb = 0, items_done = 0;
     bool ok = true;
     for (int pos = begin; pos < end && ok; ++pos) {
       const Item it = load_item(p, pos, false);
@@ -366,6 +371,9 @@ __global__ void __launch_bounds__(192, 1)
           const bool need = m_blk > m_used + 8.0f;
           if (__any_sync(0xffffffffu, need)) {
             // O still receives P V of the previous block: let it finish first.
+            // The parity wait is unambiguous: S of this block was committed
+            // after P V of block kb-2, so at least kb-1 phases are complete,
+            // and P V of this block is not issued yet.
             if (!mbar_wait(&bars->o_done, (kb - 1) & 1, abort)) {
               ok = false;
               break;
@@ -397,8 +405,9 @@ __global__ void __launch_bounds__(192, 1)
           for (int x = 0; x < 32; ++x) {
             const float p0 = ex2(fmaf(s[q * 64 + 2 * x], c, -m_used));
             const float p1 = ex2(fmaf(s[q * 64 + 2 * x + 1], c, -m_used));
-            sum += p0 + p1;
             pk[x] = pack_bf16x2(p0, p1);
+            // normalise by the same rounded weights the P.V product uses
+            sum += __uint_as_float(pk[x] << 16) + __uint_as_float(pk[x] & 0xFFFF0000u);
           }
           tmem_st32(lanes + scol + q * 32, pk);
         }
@@ -409,28 +418,38 @@ __global__ void __launch_bounds__(192, 1)
         ++kb;
       }
       if (!ok) break;
-      // ---- epilogue: O / l -> bf16
-      if (!mbar_wait(&bars->o_done, (kb - 1) & 1, abort)) {
+      // ---- epilogue: O / l.  o_last has exactly one phase per item and
+      // this warp waits on every one of them.
+      if (!mbar_wait(&bars->o_last, items_done & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool store = row < p.B;
-      __nv_bfloat16* dst =
-          p.o + (size_t(it.h) * p.S + size_t(it.i) * p.B + size_t(row)) * size_t(D);
+      const size_t orow = size_t(it.h) * p.S + size_t(it.i) * p.B + size_t(row);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t r[32];
         tmem_ld32(lanes + C::kO + q * 32, r);
         tmem_ld_wait(r);
-        uint32_t pk[16];
+        if (!store) continue;
+        if (p.out_f32) {
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + orow * D + q * 32);
 #pragma unroll
-        for (int x = 0; x < 16; ++x)
-          pk[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
-                              __uint_as_float(r[2 * x + 1]) * inv_l);
-        if (store) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + q * 32);
+          for (int x = 0; x < 8; ++x)
+            d4[x] = make_uint4(__float_as_uint(__uint_as_float(r[4 * x]) * inv_l),
+                               __float_as_uint(__uint_as_float(r[4 * x + 1]) * inv_l),
+                               __float_as_uint(__uint_as_float(r[4 * x + 2]) * inv_l),
+                               __float_as_uint(__uint_as_float(r[4 * x + 3]) * inv_l));
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            pk[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
+                                __uint_as_float(r[2 * x + 1]) * inv_l);
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D +
+                                               q * 32);
 #pragma unroll
           for (int x = 0; x < 4; ++x)
             d4[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
@@ -441,6 +460,7 @@ __global__ void __launch_bounds__(192, 1)
             (m_used + log2f(l)) * 0.6931471805599453f;
       tc_fence_before();
       mbar_arrive(&bars->o_free);
+      ++items_done;
     }
     if (!ok) raise_abort(bars, p);
   }
@@ -510,7 +530,8 @@ cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_fai
   p.B = a.B;
   p.G = a.Hq / a.Hkv;
   p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(D)));
-  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.o = a.o;
+  p.out_f32 = a.out_f32;
   p.lse = a.lse;
   p.dev_status = a.dev_status;
   auto kern = prefill_attention_kernel<D, BK>;

@@ -18,7 +18,7 @@ from . import (Shape, sparse_attn_forward, sparse_attn_plan, sparse_attn_pool_kc
 class PrefillLayer:
     def __init__(self, shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
                  num_workers: int | None = None, schedule="lpt_grouped", device="cuda",
-                 with_lse: bool = False):
+                 with_lse: bool = False, out_dtype=torch.bfloat16):
         dev = torch.device(device)
         if num_workers is None:
             num_workers = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -37,7 +37,7 @@ class PrefillLayer:
         self.cnt = torch.empty(H * nb, dtype=torch.int32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.lse = torch.empty(H * S, dtype=torch.float32, device=dev) if with_lse else None
-        self.out = torch.empty(H, S, d, dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty(H, S, d, dtype=out_dtype, device=dev)
 
     def score(self, q, k, stream=None):
         sparse_attn_score(self.shape, q, k, self.scores, self.ws, stream=stream)
@@ -60,7 +60,7 @@ class PrefillLayer:
 
 class DecodeStep:
     def __init__(self, shape: Shape, budget_blocks: int, head_kind, window_blocks: int,
-                 device="cuda", with_lse: bool = False):
+                 device="cuda", with_lse: bool = False, out_dtype=torch.bfloat16):
         dev = torch.device(device)
         self.shape = shape
         self.plan = sparse_attn_plan(shape, budget_blocks, head_kind=head_kind,
@@ -75,7 +75,7 @@ class DecodeStep:
         self.cnt = torch.empty(Bt * H, dtype=torch.int32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.lse = torch.empty(Bt * H, dtype=torch.float32, device=dev) if with_lse else None
-        self.out = torch.empty(Bt, H, d, dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty(Bt, H, d, dtype=out_dtype, device=dev)
 
     def build_cache(self, k, stream=None):
         sparse_attn_pool_kcache(self.shape, k, self.kbar, stream=stream)

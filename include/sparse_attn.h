@@ -79,6 +79,9 @@ enum {
 
 enum { SA_HEAD_RETRIEVAL = 0, SA_HEAD_STREAMING = 1 };
 
+/* Element type of the attention output. */
+enum { SA_DTYPE_BF16 = 0, SA_DTYPE_F32 = 1 };
+
 /* Bits of the device status word. */
 enum {
   SA_DEV_BAD_INDEX = 1,      /* a block index outside [0, i] was clamped     */
@@ -214,10 +217,13 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan,
  * Attention over the selected blocks.
  * Prefill: o[h, t] = sum_u softmax_u(q[h,t] . k[g,u] / sqrt(d)) v[g,u] over
  *   the keys u of the blocks idx[h*nb+i][0..cnt) with u <= t (only the
- *   diagonal block is partly masked); online softmax in fp32, bf16 output.
+ *   diagonal block is partly masked); online softmax in fp32; the bf16
+ *   probabilities fed to the P.V product also form the normaliser, so each
+ *   output row is a convex combination of value rows.
  *   Runs as a persistent kernel: one CTA per plan worker, walking that
  *   worker's items in order (sm_103a: TMA loads, tcgen05 MMAs into TMEM).
  * Decode: o[b,h] over the blocks of row b*Hq+h; plan may be NULL.
+ * o_dtype: SA_DTYPE_BF16 (round to nearest even) or SA_DTYPE_F32.
  * lse (nullable): natural-log sum of exponentials per query row, fp32,
  *   [Hq][S] (prefill) or [Bt][Hq] (decode).
  * dev_status: device int32 the kernels OR SA_DEV_* bits into (not cleared by
@@ -228,7 +234,7 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan,
 sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan,
                               const void* q, const void* k, const void* v,
                               const int32_t* idx, const int32_t* cnt,
-                              int32_t kmax, void* o, float* lse,
+                              int32_t kmax, void* o, int32_t o_dtype, float* lse,
                               int32_t* dev_status, sa_stream_t stream);
 
 /*

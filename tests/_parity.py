@@ -6,8 +6,14 @@ Tolerances (bf16 inputs, fp32 accumulation on the GPU, fp64 oracle):
   selection   bit-exact, except blocks whose oracle score lies within 1e-3
               relative of the row's k-th (last kept) score
   attention   max |O_gpu - O_ref| <= 1e-2 and sum|diff| / sum|O_ref| <= 2e-3,
-              the oracle run on the GPU's own selected blocks
-  lse         |lse_gpu - lse_ref| <= 2e-3 (natural log units)
+              the oracle run on the GPU's own selected blocks, for fp32
+              output; bf16 output is that value rounded to nearest even, so
+              each element may differ by a further half bf16 ulp of O_ref
+              (2^(e-8) for |O_ref| in [2^e, 2^(e+1)))
+  lse         |lse_gpu - lse_ref| <= 4.5e-3 (natural log units): the
+              normaliser sums the bf16-rounded weights, each within 2^-8
+              relative of the exact weight, i.e. <= ln(1 + 2^-8) = 3.9e-3 in
+              log, plus fp32 and ex2.approx error
 """
 from __future__ import annotations
 
@@ -20,7 +26,7 @@ from workloads import generate
 MAX_ABS = 1e-2
 MEAN_REL = 2e-3
 SEL_REL = 1e-3
-LSE_ABS = 2e-3
+LSE_ABS = 4.5e-3
 
 
 def to_dev(bits: np.ndarray, dev="cuda") -> torch.Tensor:
@@ -75,7 +81,14 @@ def check_selection(idx, cnt, scores_ref, budgets, rows=None):
     return tolerated
 
 
-def check_attention(out_gpu: np.ndarray, lse_gpu, x: dict, idx, cnt, B: int, items, group: int):
+def half_ulp_bf16(ref: np.ndarray) -> np.ndarray:
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (e - 8), 0.0)
+
+
+def check_attention(out_gpu: np.ndarray, lse_gpu, x: dict, idx, cnt, B: int, items, group: int,
+                    bf16_out: bool = False):
     """out_gpu [Hq, S, d] float; x holds the bf16 bits; items: ids h*nb+i."""
     nb = cnt.shape[1]
     by_head = {}
@@ -96,13 +109,14 @@ def check_attention(out_gpu: np.ndarray, lse_gpu, x: dict, idx, cnt, B: int, ite
             o, lse = oa.attend_item(q, k, v, i, blocks, B)
             got = out_gpu[h, i * B:(i + 1) * B]
             d = np.abs(got - o)
-            worst = max(worst, float(d.max()))
+            excess = d - (half_ulp_bf16(o) if bf16_out else 0.0)
+            worst = max(worst, float(excess.max()))
             num += float(d.sum())
             den += float(np.abs(o).sum())
             if lse_gpu is not None:
                 lg = lse_gpu[h, i * B:(i + 1) * B]
                 assert np.abs(lg - lse).max() <= LSE_ABS, (h, i, np.abs(lg - lse).max())
-    assert worst <= MAX_ABS, f"max abs error {worst}"
+    assert worst <= MAX_ABS, f"max abs error {worst} (beyond output rounding)"
     assert num / den <= MEAN_REL, f"mean relative error {num / den}"
     return worst, num / den
 

@@ -198,9 +198,10 @@ def test_device_calls_reject_bad_arguments_before_launch(sa):
     other = sa.Shape.prefill(8192, 64, 8, 2, 64)
     assert lib.sparse_attn_select(ctypes.byref(other), plan.handle, P, P, P, 9, None) == 2
     # forward: not uploaded, null status word
-    assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 9, P, None, P, None) == 8
-    assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 9, P, None, None, None) == 1
-    assert lib.sparse_attn_forward(s, None, P, P, P, P, P, 9, P, None, P, None) == 1
+    assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 9, P, 0, None, P, None) == 8
+    assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 9, P, 0, None, None, None) == 1
+    assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 9, P, 3, None, P, None) == 1
+    assert lib.sparse_attn_forward(s, None, P, P, P, P, P, 9, P, 1, None, P, None) == 1
     # pool_kcache is decode only
     assert lib.sparse_attn_pool_kcache(s, P, P, None) == 1
     n = ctypes.c_size_t()

@@ -25,12 +25,13 @@ def env():
     return sa, torch
 
 
-def _run(sa, torch, w, x, budgets_args, schedule="lpt", workers=None, with_lse=True):
+def _run(sa, torch, w, x, budgets_args, schedule="lpt", workers=None, with_lse=True,
+         out_dtype="float32"):
     from head_heterogeneous_block_gb300.layer import PrefillLayer
     from tests._parity import to_dev
     shape = sa.Shape.prefill(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim)
     layer = PrefillLayer(shape, schedule=schedule, num_workers=workers, with_lse=with_lse,
-                         **budgets_args)
+                         out_dtype=getattr(torch, out_dtype), **budgets_args)
     t = {n: to_dev(x[n]) for n in "qkv"}
     out = layer(t["q"], t["k"], t["v"])
     torch.cuda.synchronize()
@@ -65,8 +66,9 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("out_dtype", ["float32", "bfloat16"])
 @pytest.mark.parametrize("number,S,Hq,Hkv,mode", SMALL)
-def test_prefill_small_full_parity(env, number, S, Hq, Hkv, mode):
+def test_prefill_small_full_parity(env, number, S, Hq, Hkv, mode, out_dtype):
     sa, torch = env
     from oracle import plan as op
     from tests import _parity as P
@@ -83,13 +85,13 @@ def test_prefill_small_full_parity(env, number, S, Hq, Hkv, mode):
         k_u = op.budget_for_density(w.target_density, nb)
         rng = np.random.default_rng(S)
         args = {"k_uniform": k_u, "demand": rng.integers(1, nb, Hq).tolist()}
-    r = _run(sa, torch, w, x, args, workers=16)
+    r = _run(sa, torch, w, x, args, workers=16, out_dtype=out_dtype)
     assert r["status"] == 0
     ref_scores = _oracle_scores(w, x)
     P.check_scores(r["scores"], ref_scores)
     P.check_selection(r["idx"], r["cnt"], ref_scores, r["budgets"])
     P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block,
-                      range(Hq * nb), w.group)
+                      range(Hq * nb), w.group, bf16_out=out_dtype == "bfloat16")
 
 
 @pytest.mark.parametrize("budget", ["dense", "sink_diag"])
@@ -173,7 +175,7 @@ def test_prefill_full_size(env, number):
     x = generate.prefill_inputs(w)
     W = torch.cuda.get_device_properties(0).multi_processor_count
     r = _run(sa, torch, w, x, {"k_uniform": prof["k_uniform"], "demand": prof["demand"]},
-             schedule="lpt_grouped", workers=W)
+             schedule="lpt_grouped", workers=W, out_dtype="bfloat16")
     assert r["status"] == 0
     assert r["budgets"] == prof["budgets_maxmin"]
     ref_scores = oa.block_scores(P.pooled(x["q"], w.block), P.pooled(x["k"], w.block), w.group)
@@ -182,4 +184,5 @@ def test_prefill_full_size(env, number):
     P.check_scores(r["scores"][heads], ref_scores[heads])
     P.check_selection(r["idx"], r["cnt"], ref_scores, r["budgets"])
     items = P.sample_items(r["budgets"], w.nb, 16 if number == 4 else 64, seed=number)
-    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group)
+    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group,
+                      bf16_out=True)
