@@ -138,8 +138,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     if ws > 1:
         dist.init_process_group("nccl", device_id=dev)
-    w = workload(WORKLOAD)
-    prof = _profile(WORKLOAD)
+    w = workload(args.workload)
+    prof = _profile(args.workload)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     shape = sa.Shape.prefill(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim)
 
@@ -439,6 +439,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--schedule", default="lpt_grouped",
                     choices=["lpt", "lpt_grouped", "head_order"])
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4],
+                    help="prefill workload (3, the 128K Llama-3.1-8B shape, is the headline; "
+                         "the others serve small profiling captures)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -144,6 +144,7 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const flo
   if (!plan || !scores || !idx || !cnt) return SA_ERR_INVALID_ARG;
   if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
   if (kmax < plan->kmax) return SA_ERR_SHAPE;
+  if (plan->nb > 2048) return SA_ERR_UNSUPPORTED;
   if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
   sa_k::SelectArgs a;
   a.scores = scores;

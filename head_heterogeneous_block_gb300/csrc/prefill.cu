@@ -5,25 +5,31 @@
 // and then, for each selected key block j, computes S = Q K_j^T and
 // O += softmax(S) V_j with flash-style online softmax:
 //
-//   warp 0      TMA producer: Q tiles and the selected K / V blocks, each a
-//               128-byte-swizzled box of the [heads*S, d] view, into rings of
-//               shared-memory stages.
+//   warp 0      producer: reads the schedule, the block counts and the block
+//               lists (32 indices per load), publishes each item's metadata
+//               through a small shared-memory ring, and issues TMA loads of
+//               the Q tile and the selected K / V blocks (128-byte-swizzled
+//               boxes of the [heads*S, d] view) into rings of stages.
 //   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, bf16 inputs,
-//               fp32 accumulators in tensor memory.  S_j goes to one of two
-//               TMEM buffers so QK^T of block j+1 overlaps the softmax of
-//               block j; P_j is written back over S_j (bf16) and used as the
+//               fp32 accumulators in tensor memory.  S_j alternates between
+//               two TMEM buffers so Q K_{j+1}^T overlaps the softmax of block
+//               j; P_j is written back into S_j's columns (bf16) and is the
 //               TMEM A operand of P V.  O accumulates in TMEM.
-//   warps 2-5   softmax (one query row per thread): read S_j from TMEM, mask
-//               the diagonal block causally, keep the running max and sum,
-//               write P_j; rescale O in TMEM only when the max grew by more
-//               than 2^8 (otherwise the stale max is kept and cancels in the
-//               final division); epilogue O / l -> bf16, and the log-sum-exp.
+//   warps 2-9   softmax, two warpgroups: each row of the tile has one thread
+//               in each group, which take the left and right halves of the
+//               S columns (and of O).  The halves exchange their partial row
+//               maxima through shared memory, so both keep the same running
+//               max; O is rescaled in TMEM only when the max grew by more
+//               than 2^8 (the stale max cancels in the final division).  The
+//               normaliser sums the same bf16-rounded weights that enter P V.
+//               Epilogue: O / l in fp32 or bf16, and the log-sum-exp.
 //
 // The work items and their order come from the plan's LPT schedule (S-HPLB,
 // "Algoritmo Greedy"), with workers = CTAs instead of GPUs.
 // Every index read from idx / cnt / the schedule is range-checked; bad values
 // are clamped and flagged in the device status word, never dereferenced.
-// Every wait is bounded; on a timeout the CTA flags SA_DEV_TIMEOUT, lets its
+// Every wait (including the exchanges between the two softmax groups) is a
+// bounded mbarrier wait; on a timeout the CTA flags SA_DEV_TIMEOUT, lets its
 // copies and MMAs drain, frees its tensor memory and exits.
 
 #include <cuda_bf16.h>
@@ -48,23 +54,38 @@ struct Cfg {
   static constexpr int kQBytes = kM * D * 2;
   static constexpr int kKVBytes = BK * D * 2;
   static constexpr int kNQ = 2;                   // Q stages
-  static constexpr int kNK = 3;                   // K stages
+  static constexpr int kNK = 2;                   // K stages
   static constexpr int kNV = 2;                   // V stages
+  static constexpr int kHalfS = BK / 2;           // S columns per softmax group
+  static constexpr int kHalfO = D / 2;            // O columns per softmax group
   static constexpr uint32_t kS0 = 0, kS1 = BK, kO = 2 * BK;   // TMEM columns
   static constexpr uint32_t kTmemCols = (2 * BK + D <= 256) ? 256 : 512;
   static constexpr int kData = kNQ * kQBytes + kNK * kKVBytes + kNV * kKVBytes;
-  static constexpr int kThreads = 192;
-  static constexpr int kSmem = kData + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int kThreads = 320;
 };
 
-struct Bars {
+constexpr int kNI = 4;        // item-metadata ring slots
+constexpr int kSoftmaxThreads = 256;
+
+struct ItemInfo {
+  int32_t h, i, n, diag_last;   // n == 0: end of this worker's list
+};
+
+struct Shared {
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[3], k_empty[3];
+  uint64_t k_full[2], k_empty[2];
   uint64_t v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2];
-  uint64_t o_done;   // one phase per P.V (waited only before an O rescale)
-  uint64_t o_last;   // one phase per item, after its last P.V (epilogue)
-  uint64_t o_free, drain;
+  uint64_t o_done;        // one phase per P.V (waited only before an O rescale)
+  uint64_t o_last;        // one phase per item, after its last P.V (epilogue)
+  uint64_t o_free;        // one phase per item: the epilogue has read O
+  uint64_t drain;
+  uint64_t info_full[kNI], info_empty[kNI];
+  uint64_t xmax_bar[2];   // per block: both groups posted their partial maxima
+  uint64_t xsum_bar[2];   // per item: both groups posted their partial sums
+  ItemInfo info[kNI];
+  float xmax[2][2][128];  // [block parity][group][row]
+  float xsum[2][2][128];  // [item parity][group][row]
   uint32_t tmem_base;
   int abort;
 };
@@ -82,45 +103,9 @@ struct Params {
   int32_t* dev_status;
 };
 
-struct Item {
-  int32_t h, i, n;
-  const int32_t* list;
-};
-
-// Item at schedule position `pos`; n == 0 means "skip" (flagged).
-__device__ __forceinline__ Item load_item(const Params& p, int pos, bool report) {
-  Item r{0, 0, 0, nullptr};
-  const int32_t item = p.items[pos];
-  if (item < 0 || item >= p.num_items) {
-    if (report) atomicOr(p.dev_status, SA_DEV_BAD_ITEM);
-    return r;
-  }
-  r.h = item / p.nb;
-  r.i = item - r.h * p.nb;
-  const int32_t lim = min(p.kmax, r.i + 1);
-  int32_t n = p.cnt[item];
-  if (n < 1 || n > lim) {
-    if (report) atomicOr(p.dev_status, SA_DEV_BAD_COUNT);
-    n = max(1, min(n, lim));
-  }
-  r.n = n;
-  r.list = p.idx + size_t(item) * size_t(p.kmax);
-  return r;
-}
-
-__device__ __forceinline__ int32_t load_block(const Item& it, int t, const Params& p,
-                                              bool report) {
-  int32_t j = it.list[t];
-  if (j < 0 || j > it.i) {
-    if (report) atomicOr(p.dev_status, SA_DEV_BAD_INDEX);
-    j = 0;
-  }
-  return j;
-}
-
-__device__ __forceinline__ void raise_abort(Bars* bars, const Params& p) {
+__device__ __forceinline__ void raise_abort(Shared* sh, const Params& p) {
   atomicOr(p.dev_status, SA_DEV_TIMEOUT);
-  *(volatile int*)&bars->abort = 1;
+  *(volatile int*)&sh->abort = 1;
 }
 
 // Wait for the last `min(issued, stages)` loads of a ring to land.
@@ -131,7 +116,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, int 
 }
 
 template <int D, int BK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tq,
                              const __grid_constant__ CUtensorMap tk,
                              const __grid_constant__ CUtensorMap tv, const Params p) {
@@ -142,148 +127,211 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::kNQ * C::kQBytes;
   uint8_t* sV = sK + C::kNK * C::kKVBytes;
-  Bars* bars = reinterpret_cast<Bars*>(sV + C::kNV * C::kKVBytes);
-  volatile int* abort = &bars->abort;
+  Shared* sh = reinterpret_cast<Shared*>(sV + C::kNV * C::kKVBytes);
+  volatile int* abort = &sh->abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // This worker's slice of the schedule.
-  int32_t begin = p.wptr[blockIdx.x], end = p.wptr[blockIdx.x + 1];
-  if (begin < 0 || end > p.num_items || begin > end) {
-    if (threadIdx.x == 0) atomicOr(p.dev_status, SA_DEV_BAD_ITEM);
-    begin = end = 0;
-  }
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->q_full[s], 1);
-      mbar_init(&bars->q_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->p_full[s], 128);
+      mbar_init(&sh->q_full[s], 1);
+      mbar_init(&sh->q_empty[s], 1);
+      mbar_init(&sh->k_full[s], 1);
+      mbar_init(&sh->k_empty[s], 1);
+      mbar_init(&sh->v_full[s], 1);
+      mbar_init(&sh->v_empty[s], 1);
+      mbar_init(&sh->s_full[s], 1);
+      mbar_init(&sh->p_full[s], kSoftmaxThreads);
+      mbar_init(&sh->xmax_bar[s], kSoftmaxThreads);
+      mbar_init(&sh->xsum_bar[s], kSoftmaxThreads);
     }
-    for (int s = 0; s < 3; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
+    for (int s = 0; s < kNI; ++s) {
+      mbar_init(&sh->info_full[s], 1);
+      mbar_init(&sh->info_empty[s], 1 + kSoftmaxThreads / 32);
     }
-    mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->o_last, 1);
-    mbar_init(&bars->o_free, 128);
-    mbar_init(&bars->drain, 1);
-    bars->abort = 0;
+    mbar_init(&sh->o_done, 1);
+    mbar_init(&sh->o_last, 1);
+    mbar_init(&sh->o_free, kSoftmaxThreads);
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_alloc(&sh->tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
+  const uint32_t tmem = sh->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
+    // ------------------------------------------------------ producer warp
+    int32_t begin = p.wptr[blockIdx.x], end = p.wptr[blockIdx.x + 1];
+    if (begin < 0 || end > p.num_items || begin > end) {
+      if (lane == 0) atomicOr(p.dev_status, SA_DEV_BAD_ITEM);
+      begin = end = 0;
+    }
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      const uint64_t pol_kv = l2_policy_evict_last();
-      const uint64_t pol_q = l2_policy_evict_first();
-      uint32_t qi = 0, kissued = 0, vissued = 0;
-      bool ok = true;
-      for (int pos = begin; pos < end && ok; ++pos) {
-        const Item it = load_item(p, pos, true);
-        if (it.n == 0) continue;
-        const int g = it.h / p.G;
-        const int qs = qi % C::kNQ;
-        if (qi >= uint32_t(C::kNQ) &&
-            !mbar_wait(&bars->q_empty[qs], ((qi / C::kNQ) - 1) & 1, abort)) {
+    }
+    const uint64_t pol_kv = l2_policy_evict_last();
+    const uint64_t pol_q = l2_policy_evict_first();
+    uint32_t qi = 0, kiss = 0, viss = 0;
+    bool ok = true;
+    // the schedule entry is read one item ahead of its use
+    int32_t item_next = (begin < end) ? p.items[begin] : -1;
+    for (int pos = begin; pos < end && ok; ++pos) {
+      const int32_t item = item_next;
+      if (pos + 1 < end) item_next = p.items[pos + 1];
+      if (item < 0 || item >= p.num_items) {
+        if (lane == 0) atomicOr(p.dev_status, SA_DEV_BAD_ITEM);
+        continue;
+      }
+      const int32_t h = item / p.nb, i = item - h * p.nb;
+      const int32_t lim = min(p.kmax, i + 1);
+      int32_t n = p.cnt[item];
+      if (n < 1 || n > lim) {
+        if (lane == 0) atomicOr(p.dev_status, SA_DEV_BAD_COUNT);
+        n = max(1, min(n, lim));
+      }
+      const int32_t* list = p.idx + size_t(item) * size_t(p.kmax);
+      int32_t jl = (lane < n) ? list[lane] : 0;
+      const int32_t jlast = list[n - 1];
+      const int g = h / p.G;
+      if (lane == 0) {
+        // publish the item's metadata for the MMA and softmax warps
+        const int slot = qi % kNI;
+        if (qi >= uint32_t(kNI) &&
+            !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort))
           ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&bars->q_full[qs], C::kQBytes);
-#pragma unroll
-        for (int s = 0; s < C::kPanels; ++s)
-          tma_load_2d(sQ + qs * C::kQBytes + s * C::kQPanel, &tq, &bars->q_full[qs], s * 64,
-                      it.h * p.S + it.i * p.B, pol_q);
-        ++qi;
-        for (int t = 0; t < it.n; ++t) {
-          const int32_t j = load_block(it, t, p, true);
-          const int ks = kissued % C::kNK;
-          if (kissued >= uint32_t(C::kNK) &&
-              !mbar_wait(&bars->k_empty[ks], ((kissued / C::kNK) - 1) & 1, abort)) {
+        if (ok) {
+          sh->info[slot] = ItemInfo{h, i, n, jlast == i ? 1 : 0};
+          mbar_arrive(&sh->info_full[slot]);
+          const int qs = qi % C::kNQ;
+          if (qi >= uint32_t(C::kNQ) &&
+              !mbar_wait(&sh->q_empty[qs], ((qi / C::kNQ) - 1) & 1, abort))
             ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->k_full[ks], C::kKVBytes);
+          if (ok) {
+            mbar_arrive_expect_tx(&sh->q_full[qs], C::kQBytes);
 #pragma unroll
-          for (int s = 0; s < C::kPanels; ++s)
-            tma_load_2d(sK + ks * C::kKVBytes + s * C::kKVPanel, &tk, &bars->k_full[ks], s * 64,
-                        g * p.S + j * BK, pol_kv);
-          ++kissued;
-          const int vs = vissued % C::kNV;
-          if (vissued >= uint32_t(C::kNV) &&
-              !mbar_wait(&bars->v_empty[vs], ((vissued / C::kNV) - 1) & 1, abort)) {
-            ok = false;
-            break;
+            for (int s = 0; s < C::kPanels; ++s)
+              tma_load_2d(sQ + qs * C::kQBytes + s * C::kQPanel, &tq, &sh->q_full[qs], s * 64,
+                          h * p.S + i * p.B, pol_q);
           }
-          mbar_arrive_expect_tx(&bars->v_full[vs], C::kKVBytes);
-#pragma unroll
-          for (int s = 0; s < C::kPanels; ++s)
-            tma_load_2d(sV + vs * C::kKVBytes + s * C::kKVPanel, &tv, &bars->v_full[vs], s * 64,
-                        g * p.S + j * BK, pol_kv);
-          ++vissued;
         }
       }
-      if (!ok) raise_abort(bars, p);
-      // Copies still in flight must land before this CTA's shared memory goes.
-      drain_ring(bars->q_full, qi, C::kNQ);
-      drain_ring(bars->k_full, kissued, C::kNK);
-      drain_ring(bars->v_full, vissued, C::kNV);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      ++qi;
+      int32_t jprev = -1;
+      for (int t = 0; t < n; ++t) {
+        if ((t & 31) == 0 && t > 0) jl = (t + lane < n) ? list[t + lane] : 0;
+        int32_t j = __shfl_sync(0xffffffffu, jl, t & 31);
+        if (j < 0 || j > i || j <= jprev) {   // out of range or not ascending
+          if (lane == 0) atomicOr(p.dev_status, SA_DEV_BAD_INDEX);
+          if (j < 0 || j > i) j = 0;
+        }
+        jprev = j;
+        if (lane == 0) {
+          const int ks = kiss % C::kNK;
+          if (kiss >= uint32_t(C::kNK) &&
+              !mbar_wait(&sh->k_empty[ks], ((kiss / C::kNK) - 1) & 1, abort))
+            ok = false;
+          if (ok) {
+            mbar_arrive_expect_tx(&sh->k_full[ks], C::kKVBytes);
+#pragma unroll
+            for (int s = 0; s < C::kPanels; ++s)
+              tma_load_2d(sK + ks * C::kKVBytes + s * C::kKVPanel, &tk, &sh->k_full[ks],
+                          s * 64, g * p.S + j * BK, pol_kv);
+            ++kiss;
+            const int vs = viss % C::kNV;
+            if (viss >= uint32_t(C::kNV) &&
+                !mbar_wait(&sh->v_empty[vs], ((viss / C::kNV) - 1) & 1, abort))
+              ok = false;
+            if (ok) {
+              mbar_arrive_expect_tx(&sh->v_full[vs], C::kKVBytes);
+#pragma unroll
+              for (int s = 0; s < C::kPanels; ++s)
+                tma_load_2d(sV + vs * C::kKVBytes + s * C::kKVPanel, &tv, &sh->v_full[vs],
+                            s * 64, g * p.S + j * BK, pol_kv);
+              ++viss;
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+    }
+    if (lane == 0) {
+      if (ok) {
+        // end marker for the consumers
+        const int slot = qi % kNI;
+        if (qi >= uint32_t(kNI) &&
+            !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort))
+          ok = false;
+        if (ok) {
+          sh->info[slot] = ItemInfo{0, 0, 0, 0};
+          mbar_arrive(&sh->info_full[slot]);
+        }
+      }
+      if (!ok) raise_abort(sh, p);
+      // copies still in flight must land before this CTA's shared memory goes
+      drain_ring(sh->q_full, qi, C::kNQ);
+      drain_ring(sh->k_full, kiss, C::kNK);
+      drain_ring(sh->v_full, viss, C::kNV);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, BK, 0, 0);  // Q, K both K-major
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);   // P (TMEM), V MN-major
-      uint32_t qi = 0, kb = 0, items_done = 0;
+      uint32_t qi = 0, kb = 0;
       bool ok = true;
 
       auto issue_pv = [&](uint32_t b, bool first) -> bool {
         const int pb = b & 1;
-        if (!mbar_wait(&bars->p_full[pb], (b >> 1) & 1, abort)) return false;
+        if (!mbar_wait(&sh->p_full[pb], (b >> 1) & 1, abort)) return false;
         const int vs = b % C::kNV;
-        if (!mbar_wait(&bars->v_full[vs], (b / C::kNV) & 1, abort)) return false;
-        if (first && items_done > 0 && !mbar_wait(&bars->o_free, (items_done - 1) & 1, abort))
-          return false;
+        if (!mbar_wait(&sh->v_full[vs], (b / C::kNV) & 1, abort)) return false;
+        if (first && qi > 0 && !mbar_wait(&sh->o_free, (qi - 1) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t v_base = smem_u32(sV + vs * C::kKVBytes);
-        const uint32_t p_tmem = tmem + (pb ? C::kS1 : C::kS0);
+        const uint32_t s_col = pb ? C::kS1 : C::kS0;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
+          // keys [16kk, 16kk+16) sit in the P half of the group that owns them
+          const int half = (kk * 16) / C::kHalfS;
+          const uint32_t a_col = s_col + half * C::kHalfS + (kk * 16 - half * C::kHalfS) / 2;
           // 16 keys per step: 16 rows of 128 bytes in every d panel
           const uint64_t bd = smem_desc_sw128(v_base + kk * 16 * 128, C::kKVPanel, 1024);
-          mma_ts(tmem + C::kO, p_tmem + kk * 8, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+          mma_ts(tmem + C::kO, tmem + a_col, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
         }
-        mma_commit(&bars->v_empty[vs]);
-        mma_commit(&bars->o_done);
+        mma_commit(&sh->v_empty[vs]);
+        mma_commit(&sh->o_done);
         return true;
       };
 
-      for (int pos = begin; pos < end && ok; ++pos) {
-        const Item it = load_item(p, pos, false);
-        if (it.n == 0) continue;
+      for (;;) {
+        const int slot = qi % kNI;
+        if (!mbar_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        const int n = sh->info[slot].n;
+        mbar_arrive(&sh->info_empty[slot]);
+        if (n == 0) break;
         const int qs = qi % C::kNQ;
-        if (!mbar_wait(&bars->q_full[qs], (qi / C::kNQ) & 1, abort)) {
+        if (!mbar_wait(&sh->q_full[qs], (qi / C::kNQ) & 1, abort)) {
           ok = false;
           break;
         }
         const uint32_t q_base = smem_u32(sQ + qs * C::kQBytes);
-        for (int t = 0; t < it.n; ++t) {
+        for (int t = 0; t < n; ++t) {
           const int ks = kb % C::kNK;
-          if (!mbar_wait(&bars->k_full[ks], (kb / C::kNK) & 1, abort)) {
+          if (!mbar_wait(&sh->k_full[ks], (kb / C::kNK) & 1, abort)) {
             ok = false;
             break;
           }
@@ -295,15 +343,14 @@ __global__ void __launch_bounds__(192, 1)
             // 16 dims per step: panel kk/4, 32-byte column offset inside the
             // swizzle atom (the hardware applies the XOR on the full address)
             const uint32_t off = (kk % 4) * 32;
-            const uint64_t ad =
-                smem_desc_sw128(q_base + (kk / 4) * C::kQPanel + off, 16, 1024);
+            const uint64_t ad = smem_desc_sw128(q_base + (kk / 4) * C::kQPanel + off, 16, 1024);
             const uint64_t bd =
                 smem_desc_sw128(k_base + (kk / 4) * C::kKVPanel + off, 16, 1024);
             mma_ss(s_tmem, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[kb & 1]);
-          mma_commit(&bars->k_empty[ks]);
-          if (t == it.n - 1) mma_commit(&bars->q_empty[qs]);
+          mma_commit(&sh->s_full[kb & 1]);
+          mma_commit(&sh->k_empty[ks]);
+          if (t == n - 1) mma_commit(&sh->q_empty[qs]);
           if (t > 0 && !issue_pv(kb - 1, t == 1)) {
             ok = false;
             break;
@@ -311,60 +358,86 @@ __global__ void __launch_bounds__(192, 1)
           ++kb;
         }
         if (!ok) break;
-        if (!issue_pv(kb - 1, it.n == 1)) {
+        if (!issue_pv(kb - 1, n == 1)) {
           ok = false;
           break;
         }
-        mma_commit(&bars->o_last);
+        mma_commit(&sh->o_last);
         ++qi;
-        ++items_done;
       }
-      if (!ok) raise_abort(bars, p);
-      // Every MMA must be complete before the tensor memory is freed.
-      mma_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, nullptr);
+      if (!ok) raise_abort(sh, p);
+      // every MMA must be complete before the tensor memory is freed
+      mma_commit(&sh->drain);
+      mbar_wait(&sh->drain, 0, nullptr);
     }
   } else {
-    // ------------------------------------------------------ softmax warps
+    // ------------------------------------------------------ softmax groups
+    const int grp = (warp - 2) >> 2;              // 0: left half, 1: right half
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     const int row = quarter * 32 + lane;          // query row within the tile
     const uint32_t lanes = tmem + (uint32_t(quarter * 32) << 16);
     const float c = p.scale_log2;
-    uint32_t kb = 0, items_done = 0;
+    const uint32_t o_col = C::kO + grp * C::kHalfO;
+    uint32_t kb = 0, qi = 0;
     bool ok = true;
-    for (int pos = begin; pos < end && ok; ++pos) {
-      const Item it = load_item(p, pos, false);
-      if (it.n == 0) continue;
+    for (;;) {
+      const int slot = qi % kNI;
+      if (!mbar_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      const ItemInfo it = sh->info[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->info_empty[slot]);
+      if (it.n == 0) break;
       float m_used = -INFINITY, l = 0.f;
       for (int t = 0; t < it.n; ++t) {
-        const int32_t j = load_block(it, t, p, false);
         const int sb = kb & 1;
-        if (!mbar_wait(&bars->s_full[sb], (kb >> 1) & 1, abort)) {
+        if (!mbar_wait(&sh->s_full[sb], (kb >> 1) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t scol = sb ? C::kS1 : C::kS0;
-        uint32_t sr[BK / 32][32];
+        const uint32_t scol = (sb ? C::kS1 : C::kS0) + grp * C::kHalfS;
+        uint32_t sr[C::kHalfS / 32][32];
 #pragma unroll
-        for (int q = 0; q < BK / 32; ++q) tmem_ld32(lanes + scol + q * 32, sr[q]);
+        for (int q = 0; q < C::kHalfS / 32; ++q) tmem_ld32(lanes + scol + q * 32, sr[q]);
         tmem_ld_wait(sr[0]);
 #pragma unroll
-        for (int q = 1; q < BK / 32; ++q) reg_fence(sr[q]);
-        float s[BK];
+        for (int q = 1; q < C::kHalfS / 32; ++q) reg_fence(sr[q]);
+        float s[C::kHalfS];
 #pragma unroll
-        for (int q = 0; q < BK / 32; ++q)
+        for (int q = 0; q < C::kHalfS / 32; ++q)
 #pragma unroll
           for (int x = 0; x < 32; ++x) s[q * 32 + x] = __uint_as_float(sr[q][x]);
-        if (j == it.i) {
+        if (it.diag_last && t == it.n - 1) {
+          // key column grp*kHalfS + x is visible to row `row` when <= row
 #pragma unroll
-          for (int x = 0; x < BK; ++x)
-            if (x > row) s[x] = -INFINITY;
+          for (int x = 0; x < C::kHalfS; ++x)
+            if (grp * C::kHalfS + x > row) s[x] = -INFINITY;
         }
-        float mx = s[0];
+        // partial row maximum over eight independent chains
+        float mx[8];
 #pragma unroll
-        for (int x = 1; x < BK; ++x) mx = fmaxf(mx, s[x]);
-        const float m_blk = mx * c;
+        for (int a = 0; a < 8; ++a) mx[a] = s[a];
+#pragma unroll
+        for (int x = 8; x + 16 <= C::kHalfS; x += 16)
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx[a] = max3(mx[a], s[x + a], s[x + 8 + a]);
+        if constexpr ((C::kHalfS - 8) % 16 != 0) {
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx[a] = fmaxf(mx[a], s[C::kHalfS - 8 + a]);
+        }
+        const float mine = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]),
+                                fmaxf(mx[6], mx[7]));
+        // exchange with the other group (same row, other half of the columns)
+        sh->xmax[sb][grp][row] = mine;
+        mbar_arrive(&sh->xmax_bar[sb]);
+        if (!mbar_wait(&sh->xmax_bar[sb], (kb >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        const float m_blk = fmaxf(mine, sh->xmax[sb][grp ^ 1][row]) * c;
         if (t == 0) {
           m_used = m_blk;
         } else {
@@ -374,7 +447,7 @@ __global__ void __launch_bounds__(192, 1)
             // The parity wait is unambiguous: S of this block was committed
             // after P V of block kb-2, so at least kb-1 phases are complete,
             // and P V of this block is not issued yet.
-            if (!mbar_wait(&bars->o_done, (kb - 1) & 1, abort)) {
+            if (!mbar_wait(&sh->o_done, (kb - 1) & 1, abort)) {
               ok = false;
               break;
             }
@@ -386,56 +459,67 @@ __global__ void __launch_bounds__(192, 1)
               l *= alpha;
             }
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
+            for (int q = 0; q < C::kHalfO / 32; ++q) {
               uint32_t r[32];
-              tmem_ld32(lanes + C::kO + q * 32, r);
+              tmem_ld32(lanes + o_col + q * 32, r);
               tmem_ld_wait(r);
 #pragma unroll
               for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-              tmem_st32(lanes + C::kO + q * 32, r);
+              tmem_st32(lanes + o_col + q * 32, r);
             }
             tmem_st_wait();
           }
         }
-        float sum = 0.f;
+        // P = 2^(s*c - m) in bf16, written over this group's S columns; the
+        // normaliser sums the rounded values
+        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+        const float nm = -m_used;
+        uint32_t pk[C::kHalfS / 2];
 #pragma unroll
-        for (int q = 0; q < BK / 64; ++q) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const float p0 = ex2(fmaf(s[q * 64 + 2 * x], c, -m_used));
-            const float p1 = ex2(fmaf(s[q * 64 + 2 * x + 1], c, -m_used));
-            pk[x] = pack_bf16x2(p0, p1);
-            // normalise by the same rounded weights the P.V product uses
-            sum += __uint_as_float(pk[x] << 16) + __uint_as_float(pk[x] & 0xFFFF0000u);
-          }
-          tmem_st32(lanes + scol + q * 32, pk);
+        for (int x = 0; x < C::kHalfS / 2; ++x) {
+          float a0, a1;
+          fma2(a0, a1, s[2 * x], s[2 * x + 1], c, c, nm, nm);
+          pk[x] = pack_bf16x2(ex2(a0), ex2(a1));
+          if (x & 1)
+            add2(sum2, sum3, __uint_as_float(pk[x] << 16), __uint_as_float(pk[x] & 0xFFFF0000u));
+          else
+            add2(sum0, sum1, __uint_as_float(pk[x] << 16), __uint_as_float(pk[x] & 0xFFFF0000u));
+        }
+        if constexpr (C::kHalfS / 2 == 32) {
+          tmem_st32(lanes + scol, pk);
+        } else {
+          tmem_st16(lanes + scol, pk);
         }
         tmem_st_wait();
-        l += sum;
+        l += (sum0 + sum1) + (sum2 + sum3);
         tc_fence_before();
-        mbar_arrive(&bars->p_full[sb]);
+        mbar_arrive(&sh->p_full[sb]);
         ++kb;
       }
       if (!ok) break;
-      // ---- epilogue: O / l.  o_last has exactly one phase per item and
-      // this warp waits on every one of them.
-      if (!mbar_wait(&bars->o_last, items_done & 1, abort)) {
+      // ---- epilogue: exchange the partial sums, then O / l for this half.
+      // o_last has exactly one phase per item and this warp waits on every one.
+      sh->xsum[qi & 1][grp][row] = l;
+      mbar_arrive(&sh->xsum_bar[qi & 1]);
+      if (!mbar_wait(&sh->o_last, qi & 1, abort) ||
+          !mbar_wait(&sh->xsum_bar[qi & 1], (qi >> 1) & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float lt = l + sh->xsum[qi & 1][grp ^ 1][row];
+      const float inv_l = 1.f / lt;
       const bool store = row < p.B;
       const size_t orow = size_t(it.h) * p.S + size_t(it.i) * p.B + size_t(row);
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
+      for (int q = 0; q < C::kHalfO / 32; ++q) {
         uint32_t r[32];
-        tmem_ld32(lanes + C::kO + q * 32, r);
+        tmem_ld32(lanes + o_col + q * 32, r);
         tmem_ld_wait(r);
         if (!store) continue;
+        const int col = grp * C::kHalfO + q * 32;
         if (p.out_f32) {
-          uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + orow * D + q * 32);
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + orow * D + col);
 #pragma unroll
           for (int x = 0; x < 8; ++x)
             d4[x] = make_uint4(__float_as_uint(__uint_as_float(r[4 * x]) * inv_l),
@@ -443,26 +527,25 @@ __global__ void __launch_bounds__(192, 1)
                                __float_as_uint(__uint_as_float(r[4 * x + 2]) * inv_l),
                                __float_as_uint(__uint_as_float(r[4 * x + 3]) * inv_l));
         } else {
-          uint32_t pk[16];
+          uint32_t ob[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x)
-            pk[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
+            ob[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
                                 __uint_as_float(r[2 * x + 1]) * inv_l);
-          uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D +
-                                               q * 32);
+          uint4* d4 =
+              reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
 #pragma unroll
           for (int x = 0; x < 4; ++x)
-            d4[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+            d4[x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
         }
       }
-      if (p.lse && store)
-        p.lse[size_t(it.h) * p.S + size_t(it.i) * p.B + row] =
-            (m_used + log2f(l)) * 0.6931471805599453f;
+      if (p.lse && store && grp == 0)
+        p.lse[orow] = (m_used + log2f(lt)) * 0.6931471805599453f;
       tc_fence_before();
-      mbar_arrive(&bars->o_free);
-      ++items_done;
+      mbar_arrive(&sh->o_free);
+      ++qi;
     }
-    if (!ok) raise_abort(bars, p);
+    if (!ok) raise_abort(sh, p);
   }
 
   __syncthreads();
@@ -510,6 +593,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_
 template <int D, int BK>
 cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_failed) {
   using C = Cfg<D, BK>;
+  constexpr int kSmem = C::kData + int(sizeof(Shared)) + 1024;
+  static_assert(kSmem <= 232448, "shared memory budget");
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, a.q, uint64_t(a.Hq) * a.S, D, C::kM) ||
       !make_map(&tk, a.k, uint64_t(a.Hkv) * a.S, D, BK) ||
@@ -535,10 +620,10 @@ cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_fai
   p.lse = a.lse;
   p.dev_status = a.dev_status;
   auto kern = prefill_attention_kernel<D, BK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   if (a.num_workers == 0) return cudaSuccess;
-  kern<<<a.num_workers, C::kThreads, C::kSmem, st>>>(tq, tk, tv, p);
+  kern<<<a.num_workers, C::kThreads, kSmem, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// Select step: per-row top-k_h block selection (one warp per row).
+// Select step: per-row top-k_h block selection (one CTA per row).
 //
 // A prefill row (h, i) keeps min(k_h, i+1) blocks: the sink block 0 ("Riepilogo
 // Tecnico: Fluxion", "Intuizioni Chiave" 1), the diagonal block i, and the
@@ -6,11 +6,14 @@
 // retrieval head is the row i = nb-1; a decode streaming head keeps block 0
 // and the last window_blocks blocks ("Intuizioni Chiave" 2).
 //
-// The candidates are packed into 64-bit keys (order-preserving bits of the
-// fp32 score, then the complement of the block index, so larger keys win and
-// equal scores prefer the lower index) and sorted descending with a warp
-// bitonic sort in shared memory; the kept blocks are marked in a bitmap and
-// written out in ascending order with warp ballots.
+// The threshold is found by radix selection over the order-preserving bit
+// pattern of the fp32 scores: four passes, each a 256-bin shared-memory
+// histogram of the next 8 bits among the candidates that still match the
+// prefix, and a warp scan that picks the bin holding the k-th largest.  The
+// result is the exact k-th largest score T: every candidate above T is kept,
+// and of those equal to T the lowest indices are kept (ordered by a block
+// scan, only when ties straddle the threshold).  Kept blocks are marked in a
+// bitmap and written in ascending order with warp ballots.
 
 #include <cstdint>
 
@@ -19,21 +22,22 @@
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kThreads = 128;
+constexpr int kPerThread = 16;            // candidates per thread: nb <= 2048
+constexpr int kMaxWords = 2048 / 32;
 
-__device__ __forceinline__ uint64_t score_key(float s, int j) {
-  uint32_t u = __float_as_uint(s);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (uint64_t(u) << 32) | uint64_t(0xFFFFFFFFu - uint32_t(j));
+__device__ __forceinline__ uint32_t order_bits(float s) {
+  const uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kWarps * 32) select_kernel(sa_k::SelectArgs a, int n2) {
-  extern __shared__ uint64_t sh[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint64_t* keys = sh + size_t(warp) * n2;
-  uint32_t* bits = reinterpret_cast<uint32_t*>(sh + size_t(kWarps) * n2) + warp * (n2 / 32 + 1);
-  const int row = blockIdx.x * kWarps + warp;
-  if (row >= a.rows) return;
+__global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
+  __shared__ uint32_t bits[kMaxWords];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t ctl[4];
+  __shared__ uint32_t wsum[kThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
 
   int h, i;
   const float* srow;
@@ -48,74 +52,125 @@ __global__ void __launch_bounds__(kWarps * 32) select_kernel(sa_k::SelectArgs a,
   }
   const bool streaming = a.decode && a.kinds[h] == SA_HEAD_STREAMING;
   int32_t* out = a.idx + size_t(row) * a.kmax;
-
-  // Membership of block j: mandatory, window, or chosen by score.
   const int nwords = (i + 1 + 31) / 32;
-  for (int w = lane; w < nwords; w += 32) bits[w] = 0u;
-  __syncwarp();
+  for (int w = tid; w < nwords; w += kThreads) bits[w] = 0u;
+  __syncthreads();
 
-  int keep;
   if (streaming) {
     const int lo = max(1, a.nb - a.window_blocks);
-    keep = 1 + (a.nb - lo);
-    for (int j = lane; j <= i; j += 32)
+    for (int j = tid; j <= i; j += kThreads)
       if (j == 0 || j >= lo) atomicOr(&bits[j >> 5], 1u << (j & 31));
   } else {
-    keep = min(a.budgets[h], i + 1);
-    const int mandatory = (i == 0) ? 1 : 2;
-    const int rest = keep - mandatory;
-    const int ncand = max(0, i - 1);        // blocks 1..i-1
+    const int keep = min(a.budgets[h], i + 1);
+    const int rest = keep - ((i == 0) ? 1 : 2);
+    const int ncand = max(0, i - 1);          // blocks 1..i-1
     if (rest >= ncand) {
-      for (int j = lane; j <= i; j += 32) atomicOr(&bits[j >> 5], 1u << (j & 31));
+      for (int j = tid; j <= i; j += kThreads) atomicOr(&bits[j >> 5], 1u << (j & 31));
     } else {
-      if (lane == 0) {
+      if (tid == 0) {
         atomicOr(&bits[0], 1u);
         atomicOr(&bits[i >> 5], 1u << (i & 31));
       }
       if (rest > 0) {
-        int n = 1;
-        while (n < ncand) n <<= 1;
-        for (int t = lane; t < n; t += 32) keys[t] = (t < ncand) ? score_key(srow[t + 1], t + 1) : 0ull;
-        __syncwarp();
-        // bitonic sort, descending
-        for (int k = 2; k <= n; k <<= 1) {
-          for (int jj = k >> 1; jj > 0; jj >>= 1) {
-            for (int t = lane; t < n; t += 32) {
-              const int x = t ^ jj;
-              if (x > t) {
-                const uint64_t u = keys[t], v = keys[x];
-                const bool down = (t & k) == 0;   // this pair's run sorts descending
-                if (down ? (u < v) : (u > v)) {
-                  keys[t] = v;
-                  keys[x] = u;
+        uint32_t u[kPerThread];
+#pragma unroll
+        for (int r = 0; r < kPerThread; ++r) {
+          const int j = 1 + tid + r * kThreads;
+          u[r] = (j <= i - 1) ? order_bits(srow[j]) : 0u;
+        }
+        uint32_t prefix = 0, mask = 0, need = uint32_t(rest), eq_total = 0;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+          for (int b = tid; b < 256; b += kThreads) hist[b] = 0u;
+          __syncthreads();
+#pragma unroll
+          for (int r = 0; r < kPerThread; ++r) {
+            const int j = 1 + tid + r * kThreads;
+            if (j <= i - 1 && (u[r] & mask) == prefix) atomicAdd(&hist[(u[r] >> shift) & 255u], 1u);
+          }
+          __syncthreads();
+          if (warp == 0) {
+            // lane l holds bins 255-8l .. 248-8l (descending)
+            uint32_t c[8], local = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              c[k] = hist[255 - 8 * lane - k];
+              local += c[k];
+            }
+            uint32_t incl = local;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += v;
+            }
+            const uint32_t excl = incl - local;
+            if (excl < need && need <= incl) {
+              uint32_t acc = excl;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (acc + c[k] >= need) {
+                  ctl[0] = uint32_t(255 - 8 * lane - k);
+                  ctl[1] = acc;
+                  ctl[2] = c[k];
+                  break;
                 }
+                acc += c[k];
               }
             }
-            __syncwarp();
           }
+          __syncthreads();
+          const uint32_t b = ctl[0];
+          need -= ctl[1];
+          eq_total = ctl[2];
+          prefix |= b << shift;
+          mask |= 0xFFu << shift;
+          __syncthreads();
         }
-        for (int t = lane; t < rest; t += 32) {
-          const int j = int(0xFFFFFFFFu - uint32_t(keys[t] & 0xFFFFFFFFull));
-          atomicOr(&bits[j >> 5], 1u << (j & 31));
+        const uint32_t T = prefix;
+        if (eq_total == need) {
+          // every candidate >= T is kept
+#pragma unroll
+          for (int r = 0; r < kPerThread; ++r) {
+            const int j = 1 + tid + r * kThreads;
+            if (j <= i - 1 && u[r] >= T) atomicOr(&bits[j >> 5], 1u << (j & 31));
+          }
+        } else {
+          // ties straddle the threshold: above T all, equal to T by index
+          uint32_t taken = 0;
+          for (int r = 0; r < kPerThread; ++r) {
+            const int j = 1 + tid + r * kThreads;
+            const bool valid = j <= i - 1;
+            const bool eq = valid && u[r] == T;
+            const uint32_t m = __ballot_sync(0xffffffffu, eq);
+            if (lane == 0) wsum[warp] = __popc(m);
+            __syncthreads();
+            uint32_t before = taken;
+            for (int w = 0; w < warp; ++w) before += wsum[w];
+            before += __popc(m & ((1u << lane) - 1u));
+            if (valid && (u[r] > T || (eq && before < need)))
+              atomicOr(&bits[j >> 5], 1u << (j & 31));
+            for (int w = 0; w < kThreads / 32; ++w) taken += wsum[w];
+            __syncthreads();
+          }
         }
       }
     }
   }
-  __syncwarp();
+  __syncthreads();
 
-  // Emit ascending block indices, then pad with -1.
-  int written = 0;
-  for (int base = 0; base <= i; base += 32) {
-    const int j = base + lane;
-    const bool on = (j <= i) && ((bits[j >> 5] >> (j & 31)) & 1u);
-    const uint32_t m = __ballot_sync(0xffffffffu, on);
-    const int pos = written + __popc(m & ((1u << lane) - 1u));
-    if (on && pos < a.kmax) out[pos] = j;
-    written += __popc(m);
+  // Emit ascending block indices, then pad with -1 (warp 0).
+  if (warp == 0) {
+    int written = 0;
+    for (int base = 0; base <= i; base += 32) {
+      const int j = base + lane;
+      const bool on = (j <= i) && ((bits[j >> 5] >> (j & 31)) & 1u);
+      const uint32_t m = __ballot_sync(0xffffffffu, on);
+      const int pos = written + __popc(m & ((1u << lane) - 1u));
+      if (on && pos < a.kmax) out[pos] = j;
+      written += __popc(m);
+    }
+    for (int t = written + lane; t < a.kmax; t += 32) out[t] = -1;
+    if (lane == 0) a.cnt[row] = min(written, a.kmax);
   }
-  for (int t = written + lane; t < a.kmax; t += 32) out[t] = -1;
-  if (lane == 0) a.cnt[row] = min(written, a.kmax);
-  (void)keep;
 }
 
 }  // namespace
@@ -124,15 +179,8 @@ namespace sa_k {
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
-  int n2 = 32;
-  while (n2 < a.nb) n2 <<= 1;
-  const size_t smem = size_t(kWarps) * n2 * sizeof(uint64_t) +
-                      size_t(kWarps) * (n2 / 32 + 1) * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(smem));
-  if (e != cudaSuccess) return e;
-  const unsigned grid = unsigned((a.rows + kWarps - 1) / kWarps);
-  select_kernel<<<grid, kWarps * 32, smem, st>>>(a, n2);
+  if (a.nb > kPerThread * kThreads) return cudaErrorInvalidValue;
+  select_kernel<<<unsigned(a.rows), kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

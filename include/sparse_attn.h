@@ -206,8 +206,9 @@ sa_status sparse_attn_score(const sa_shape* shp, const void* q, const void* k,
  * Outputs: idx [rows][kmax] int32, each row ascending and padded with -1;
  * cnt [rows] int32; rows = Hq*nb (prefill, row h*nb+i) or Bt*Hq (decode,
  * row b*Hq+h).  kmax must be >= the plan's kmax (sparse_attn_plan_info).
+ * Rows of up to 2048 blocks are supported (nb <= 2048), else UNSUPPORTED.
  * Errors: INVALID_ARG, SHAPE (kmax too small, shape differs from the plan's),
- * NOT_UPLOADED, CUDA.
+ * UNSUPPORTED, NOT_UPLOADED, CUDA.
  */
 sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan,
                              const float* scores, int32_t* idx, int32_t* cnt,
