@@ -255,3 +255,21 @@ def sparse_attn_forward(shape: Shape, plan, q, k, v, idx, cnt, kmax: int, o, lse
 def sparse_attn_pool_kcache(shape: Shape, k, kbar, stream=None):
     _check(_lib.sparse_attn_pool_kcache(ctypes.byref(shape), _ptr(k), _ptr(kbar),
                                         _stream(stream)), "sparse_attn_pool_kcache")
+
+
+_noalloc = None
+
+
+def sparse_attn_score_noalloc(shape: Shape, q, k, scores, stream=None):
+    """Pooled block scores without a workspace (the library's fixed 32 MiB
+    scratch area); see the C declaration for the limit and the rules on
+    overlapping calls."""
+    global _noalloc
+    if _noalloc is None:
+        fn = _lib.sparse_attn_score_noalloc
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.POINTER(Shape), ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_void_p, ctypes.c_void_p]
+        _noalloc = fn
+    _check(_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(scores), _stream(stream)),
+           "sparse_attn_score_noalloc")

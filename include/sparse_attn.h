@@ -199,6 +199,32 @@ sa_status sparse_attn_score(const sa_shape* shp, const void* q, const void* k,
                             sa_stream_t stream);
 
 /*
+ * Index step for callers that cannot allocate device memory where they score
+ * a layer: code whose hot path must not allocate (cudaMalloc may synchronise
+ * the device and takes unbounded time), hosts that own all device memory
+ * through their own pool and hand a plugin only its inputs and outputs, and
+ * callers held to a memory budget fixed at start-up.  It computes exactly what
+ * sparse_attn_score computes, but keeps the pooled queries and keys in a
+ * fixed 32 MiB area of device memory that belongs to this library (every
+ * device that loads the library holds it until the process exits); the call
+ * allocates nothing and takes no workspace.  The pages have no counterpart of
+ * this entry point; it exists for deployment only.
+ *  - Limit: prefill shapes with (Hq + Hkv) * nb * d * 4 bytes <= 32 MiB (the
+ *    Llama-3.1-8B 128K shape needs 20 MiB); larger ones return
+ *    SA_ERR_UNSUPPORTED.  Decode shapes need no scratch and behave as
+ *    sparse_attn_score.
+ *  - The first call on each device looks up the area's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls on a device share the area.  Each call rewrites every pooled
+ *    vector it reads, so nothing has to be cleared, but calls whose execution
+ *    overlaps on the GPU (other streams, other host threads) race on it:
+ *    serialise them.
+ * Errors: as sparse_attn_score, plus UNSUPPORTED for the size limit.
+ */
+sa_status sparse_attn_score_noalloc(const sa_shape* shp, const void* q, const void* k,
+                                    float* scores, sa_stream_t stream);
+
+/*
  * Select: for prefill row (h, i) keep min(k_h, i+1) blocks: 0 and i always,
  * then the highest-scoring of 1..i-1, ties to the lower index.  For decode
  * retrieval heads the row is i = nb-1 with k_h = k_uniform; streaming heads
