@@ -29,7 +29,7 @@ SCHEDULES = {"lpt": SA_SCHED_LPT, "lpt_grouped": SA_SCHED_LPT_GROUPED,
              "head_order": SA_SCHED_HEAD_ORDER}
 SA_HEAD_RETRIEVAL, SA_HEAD_STREAMING = 0, 1
 SA_DTYPE_BF16, SA_DTYPE_F32 = 0, 1
-SA_DEV_BAD_INDEX, SA_DEV_BAD_COUNT, SA_DEV_TIMEOUT, SA_DEV_BAD_ITEM = 1, 2, 4, 8
+SA_DEV_BAD_INDEX, SA_DEV_BAD_COUNT, SA_DEV_TIMEOUT, SA_DEV_BAD_ITEM, SA_DEV_BAD_LAUNCH = 1, 2, 4, 8, 16
 
 
 class Shape(ctypes.Structure):

@@ -10,7 +10,7 @@
 //               through a small shared-memory ring, and issues TMA loads of
 //               the Q tile and the selected K / V blocks (128-byte-swizzled
 //               boxes of the [heads*S, d] view) into rings of stages.
-//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, bf16 inputs,
+//   warp 1      MMA issuer (one elected lane): tcgen05.mma kind::f16, bf16 inputs,
 //               fp32 accumulators in tensor memory.  S_j alternates between
 //               two TMEM buffers so Q K_{j+1}^T overlaps the softmax of block
 //               j; P_j is written back into S_j's columns (bf16) and is the
@@ -53,39 +53,45 @@ struct Cfg {
   static constexpr int kKVPanel = BK * 128;       // bytes of one K/V panel
   static constexpr int kQBytes = kM * D * 2;
   static constexpr int kKVBytes = BK * D * 2;
-  static constexpr int kNQ = 2;                   // Q stages
-  static constexpr int kNK = 2;                   // K stages
-  static constexpr int kNV = 2;                   // V stages
-  static constexpr int kHalfS = BK / 2;           // S columns per softmax group
-  static constexpr int kHalfO = D / 2;            // O columns per softmax group
-  static constexpr uint32_t kS0 = 0, kS1 = BK, kO = 2 * BK;   // TMEM columns
-  static constexpr uint32_t kTmemCols = (2 * BK + D <= 256) ? 256 : 512;
+  static constexpr int kNQ = 1;                   // Q stages
+  static constexpr int kNK = 3;                   // K stages
+  static constexpr int kNV = 3;                   // V stages (P.V trails Q.K^T by two blocks)
+  static constexpr int kNS = 3;                   // S buffers in tensor memory
+  static constexpr int kGroups = 4;               // softmax column groups
+  static constexpr int kCols = BK / kGroups;      // S columns per group
+  static constexpr int kOCols = D / kGroups;      // O columns per group
+  static constexpr uint32_t kO = kNS * BK;        // TMEM column of O
+  static constexpr uint32_t kTmemCols = (kNS * BK + D <= 256) ? 256 : 512;
   static constexpr int kData = kNQ * kQBytes + kNK * kKVBytes + kNV * kKVBytes;
-  static constexpr int kThreads = 320;
+  static constexpr int kPrefetch = 0;             // blocks ahead prefetched into L2 (0: off)
+  static_assert(kNS * BK + D <= 512, "tensor memory budget");
+  static_assert(kCols == 16 || kCols == 32, "group width");
+  static_assert(kOCols == 16 || kOCols == 32, "group width");
 };
 
-constexpr int kNI = 4;        // item-metadata ring slots
-constexpr int kSoftmaxThreads = 256;
+constexpr int kNI = 4;                 // item-metadata ring slots
+constexpr int kSoftmaxWarps = 16;      // warps 3..18
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kThreads = 96 + kSoftmaxThreads;   // + producer K/Q, MMA, producer V
 
 struct ItemInfo {
   int32_t h, i, n, diag_last;   // n == 0: end of this worker's list
 };
 
 struct Shared {
-  uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[2], k_empty[2];
-  uint64_t v_full[2], v_empty[2];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_done;        // one phase per P.V (waited only before an O rescale)
+  uint64_t q_full[1], q_empty[1];
+  uint64_t k_full[3], k_empty[3];
+  uint64_t v_full[3], v_empty[3];
+  uint64_t s_full[3];     // S of block b is in TMEM buffer b % 3
+  uint64_t p_full[3];     // P of block b written (every softmax group)
+  uint64_t pv_done[3];    // P.V of block b complete (waited only before an O rescale)
   uint64_t o_last;        // one phase per item, after its last P.V (epilogue)
-  uint64_t o_free;        // one phase per item: the epilogue has read O
+  uint64_t o_free;        // one phase per item: every group finished the epilogue
+  uint64_t xch_bar;       // exchange between the softmax groups
   uint64_t drain;
   uint64_t info_full[kNI], info_empty[kNI];
-  uint64_t xmax_bar[2];   // per block: both groups posted their partial maxima
-  uint64_t xsum_bar[2];   // per item: both groups posted their partial sums
   ItemInfo info[kNI];
-  float xmax[2][2][128];  // [block parity][group][row]
-  float xsum[2][2][128];  // [item parity][group][row]
+  float xch[4][128];      // [group][row]: partial row max per block, partial sum per item
   uint32_t tmem_base;
   int abort;
 };
@@ -115,16 +121,25 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, int 
     mbar_wait(&full[x % stages], (x / stages) & 1, nullptr);
 }
 
+// A block index as both producers use it: out-of-range entries become block 0.
+__device__ __forceinline__ int32_t clamp_block(int32_t j, int32_t i) {
+  return (j < 0 || j > i) ? 0 : j;
+}
+
 template <int D, int BK>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tq,
                              const __grid_constant__ CUtensorMap tk,
                              const __grid_constant__ CUtensorMap tv, const Params p) {
   using C = Cfg<D, BK>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  uint8_t* sQ = smem;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The data stages need 1024-byte alignment; the launch reserves no slack
+  // for it, so a misaligned window is reported instead of used.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.dev_status, SA_DEV_BAD_LAUNCH);
+    return;
+  }
+  uint8_t* sQ = smem_raw;
   uint8_t* sK = sQ + C::kNQ * C::kQBytes;
   uint8_t* sV = sK + C::kNK * C::kKVBytes;
   Shared* sh = reinterpret_cast<Shared*>(sV + C::kNV * C::kKVBytes);
@@ -134,25 +149,24 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sh->q_full[s], 1);
-      mbar_init(&sh->q_empty[s], 1);
+    mbar_init(&sh->q_full[0], 1);
+    mbar_init(&sh->q_empty[0], 1);
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&sh->k_full[s], 1);
       mbar_init(&sh->k_empty[s], 1);
       mbar_init(&sh->v_full[s], 1);
       mbar_init(&sh->v_empty[s], 1);
       mbar_init(&sh->s_full[s], 1);
       mbar_init(&sh->p_full[s], kSoftmaxThreads);
-      mbar_init(&sh->xmax_bar[s], kSoftmaxThreads);
-      mbar_init(&sh->xsum_bar[s], kSoftmaxThreads);
+      mbar_init(&sh->pv_done[s], 1);
     }
     for (int s = 0; s < kNI; ++s) {
       mbar_init(&sh->info_full[s], 1);
-      mbar_init(&sh->info_empty[s], 1 + kSoftmaxThreads / 32);
+      mbar_init(&sh->info_empty[s], 2 + kSoftmaxWarps);
     }
-    mbar_init(&sh->o_done, 1);
     mbar_init(&sh->o_last, 1);
     mbar_init(&sh->o_free, kSoftmaxThreads);
+    mbar_init(&sh->xch_bar, kSoftmaxThreads);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_mbar_init();
@@ -166,7 +180,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = sh->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------ producer warp
+    // ------------------------------------------------- producer: items, Q, K
     int32_t begin = p.wptr[blockIdx.x], end = p.wptr[blockIdx.x + 1];
     if (begin < 0 || end > p.num_items || begin > end) {
       if (lane == 0) atomicOr(p.dev_status, SA_DEV_BAD_ITEM);
@@ -179,7 +193,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     const uint64_t pol_kv = l2_policy_evict_last();
     const uint64_t pol_q = l2_policy_evict_first();
-    uint32_t qi = 0, kiss = 0, viss = 0;
+    uint32_t qi = 0, kiss = 0;
     bool ok = true;
     // the schedule entry is read one item ahead of its use
     int32_t item_next = (begin < end) ? p.items[begin] : -1;
@@ -201,8 +215,16 @@ __global__ void __launch_bounds__(320, 1)
       int32_t jl = (lane < n) ? list[lane] : 0;
       const int32_t jlast = list[n - 1];
       const int g = h / p.G;
+      // L2 prefetch of the first blocks (later ones are prefetched ahead below)
+      if (C::kPrefetch > 0 && lane < min(n, C::kPrefetch)) {
+        const int32_t jp = clamp_block(jl, i);
+        for (int s = 0; s < C::kPanels; ++s) {
+          tma_prefetch_2d(&tk, s * 64, g * p.S + jp * BK);
+          tma_prefetch_2d(&tv, s * 64, g * p.S + jp * BK);
+        }
+      }
       if (lane == 0) {
-        // publish the item's metadata for the MMA and softmax warps
+        // publish the item's metadata for the MMA, V-producer and softmax warps
         const int slot = qi % kNI;
         if (qi >= uint32_t(kNI) &&
             !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort))
@@ -210,16 +232,13 @@ __global__ void __launch_bounds__(320, 1)
         if (ok) {
           sh->info[slot] = ItemInfo{h, i, n, jlast == i ? 1 : 0};
           mbar_arrive(&sh->info_full[slot]);
-          const int qs = qi % C::kNQ;
-          if (qi >= uint32_t(C::kNQ) &&
-              !mbar_wait(&sh->q_empty[qs], ((qi / C::kNQ) - 1) & 1, abort))
-            ok = false;
+          if (qi >= 1 && !mbar_wait(&sh->q_empty[0], (qi - 1) & 1, abort)) ok = false;
           if (ok) {
-            mbar_arrive_expect_tx(&sh->q_full[qs], C::kQBytes);
+            mbar_arrive_expect_tx(&sh->q_full[0], C::kQBytes);
 #pragma unroll
             for (int s = 0; s < C::kPanels; ++s)
-              tma_load_2d(sQ + qs * C::kQBytes + s * C::kQPanel, &tq, &sh->q_full[qs], s * 64,
-                          h * p.S + i * p.B, pol_q);
+              tma_load_2d(sQ + s * C::kQPanel, &tq, &sh->q_full[0], s * 64, h * p.S + i * p.B,
+                          pol_q);
           }
         }
       }
@@ -229,13 +248,23 @@ __global__ void __launch_bounds__(320, 1)
       int32_t jprev = -1;
       for (int t = 0; t < n; ++t) {
         if ((t & 31) == 0 && t > 0) jl = (t + lane < n) ? list[t + lane] : 0;
-        int32_t j = __shfl_sync(0xffffffffu, jl, t & 31);
-        if (j < 0 || j > i || j <= jprev) {   // out of range or not ascending
+        const int32_t jraw = __shfl_sync(0xffffffffu, jl, t & 31);
+        // block kPrefetch positions ahead, into L2
+        const int tp = t + C::kPrefetch;
+        const int32_t jp = __shfl_sync(0xffffffffu, jl, tp & 31);
+        if (jraw < 0 || jraw > i || jraw <= jprev) {   // out of range or not ascending
           if (lane == 0) atomicOr(p.dev_status, SA_DEV_BAD_INDEX);
-          if (j < 0 || j > i) j = 0;
         }
-        jprev = j;
+        const int32_t j = clamp_block(jraw, i);
+        jprev = jraw;
         if (lane == 0) {
+          if (C::kPrefetch > 0 && tp < n && (tp & ~31) == (t & ~31)) {
+            const int32_t jq = clamp_block(jp, i);
+            for (int s = 0; s < C::kPanels; ++s) {
+              tma_prefetch_2d(&tk, s * 64, g * p.S + jq * BK);
+              tma_prefetch_2d(&tv, s * 64, g * p.S + jq * BK);
+            }
+          }
           const int ks = kiss % C::kNK;
           if (kiss >= uint32_t(C::kNK) &&
               !mbar_wait(&sh->k_empty[ks], ((kiss / C::kNK) - 1) & 1, abort))
@@ -247,18 +276,6 @@ __global__ void __launch_bounds__(320, 1)
               tma_load_2d(sK + ks * C::kKVBytes + s * C::kKVPanel, &tk, &sh->k_full[ks],
                           s * 64, g * p.S + j * BK, pol_kv);
             ++kiss;
-            const int vs = viss % C::kNV;
-            if (viss >= uint32_t(C::kNV) &&
-                !mbar_wait(&sh->v_empty[vs], ((viss / C::kNV) - 1) & 1, abort))
-              ok = false;
-            if (ok) {
-              mbar_arrive_expect_tx(&sh->v_full[vs], C::kKVBytes);
-#pragma unroll
-              for (int s = 0; s < C::kPanels; ++s)
-                tma_load_2d(sV + vs * C::kKVBytes + s * C::kKVPanel, &tv, &sh->v_full[vs],
-                            s * 64, g * p.S + j * BK, pol_kv);
-              ++viss;
-            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -281,105 +298,214 @@ __global__ void __launch_bounds__(320, 1)
       // copies still in flight must land before this CTA's shared memory goes
       drain_ring(sh->q_full, qi, C::kNQ);
       drain_ring(sh->k_full, kiss, C::kNK);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------- producer: V
+    // Runs apart from the K stream so K loads are never held up by V stages,
+    // which free two blocks later.
+    const uint64_t pol_kv = l2_policy_evict_last();
+    uint32_t qi = 0, viss = 0;
+    bool ok = true;
+    for (;;) {
+      const int slot = qi % kNI;
+      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      const ItemInfo it = sh->info[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->info_empty[slot]);
+      if (it.n == 0) break;
+      const int32_t* list = p.idx + (size_t(it.h) * p.nb + it.i) * size_t(p.kmax);
+      const int g = it.h / p.G;
+      int32_t jl = (lane < it.n) ? list[lane] : 0;
+      for (int t = 0; t < it.n; ++t) {
+        if ((t & 31) == 0 && t > 0) jl = (t + lane < it.n) ? list[t + lane] : 0;
+        const int32_t j = clamp_block(__shfl_sync(0xffffffffu, jl, t & 31), it.i);
+        if (lane == 0) {
+          const int vs = viss % C::kNV;
+          if (viss >= uint32_t(C::kNV) &&
+              !mbar_wait(&sh->v_empty[vs], ((viss / C::kNV) - 1) & 1, abort))
+            ok = false;
+          if (ok) {
+            mbar_arrive_expect_tx(&sh->v_full[vs], C::kKVBytes);
+#pragma unroll
+            for (int s = 0; s < C::kPanels; ++s)
+              tma_load_2d(sV + vs * C::kKVBytes + s * C::kKVPanel, &tv, &sh->v_full[vs],
+                          s * 64, g * p.S + j * BK, pol_kv);
+            ++viss;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      if (!ok) break;
+      ++qi;
+    }
+    if (lane == 0) {
+      if (!ok) raise_abort(sh, p);
       drain_ring(sh->v_full, viss, C::kNV);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(128, BK, 0, 0);  // Q, K both K-major
-      constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);   // P (TMEM), V MN-major
-      uint32_t qi = 0, kb = 0;
-      bool ok = true;
+    // ------------------------------------------------- MMA issuer
+    // The whole warp runs the loop (waits, descriptors); one elected lane
+    // issues the MMAs and commits.  Q.K^T of block b is issued two blocks
+    // ahead of P.V of block b-2, across item boundaries, so the tensor pipe
+    // has work while the softmax of the two blocks in between runs.
+    constexpr uint32_t idesc_qk = idesc_bf16(128, BK, 0, 0);  // Q, K both K-major
+    constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);   // P (TMEM), V MN-major
+    uint32_t qi = 0, kb = 0, pvn = 0;
+    // per pending block b, 4 bits at 4*(b % 4): opens its item, closes its
+    // item, its item is not the worker's first, parity of its item index
+    uint32_t pend = 0;
+    bool ok = true;
 
-      auto issue_pv = [&](uint32_t b, bool first) -> bool {
-        const int pb = b & 1;
-        if (!mbar_wait(&sh->p_full[pb], (b >> 1) & 1, abort)) return false;
-        const int vs = b % C::kNV;
-        if (!mbar_wait(&sh->v_full[vs], (b / C::kNV) & 1, abort)) return false;
-        if (first && qi > 0 && !mbar_wait(&sh->o_free, (qi - 1) & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t v_base = smem_u32(sV + vs * C::kKVBytes);
-        const uint32_t s_col = pb ? C::kS1 : C::kS0;
+    // Each step needs the K of the next Q.K^T and the P, V (and, for an
+    // item's first block, the freed O) of the next P.V.  Their phases are
+    // first tested together -- one barrier per lane, one try_wait for the
+    // whole warp, one ballot -- and only the ones not yet complete are
+    // waited on, so the issuing warp spends few round trips per step.
+    // K, V and S/P rings all have three stages: stage = block % 3 and the
+    // phase bit flips every three blocks; both are kept incrementally.
+    static_assert(C::kNK == 3 && C::kNV == 3 && C::kNS == 3, "shared ring indexing");
+    uint32_t qstage = 0, qphase = 0;     // block kb (next Q.K^T)
+    uint32_t pstage = 0, pphase = 0;     // block pvn (next P.V)
+
+    auto issue_pv = [&](uint32_t have) -> bool {
+      const uint32_t bits = (pend >> (4 * (pvn & 3))) & 15u;
+      const bool first = bits & 1u, last = bits & 2u;
+      if (!(have & 2u) && !warp_wait(&sh->p_full[pstage], pphase, abort)) return false;
+      if (!(have & 4u) && !warp_wait(&sh->v_full[pstage], pphase, abort)) return false;
+      // the previous item's epilogue must have read O before it is overwritten
+      if (first && (bits & 4u) && !(have & 8u) &&
+          !warp_wait(&sh->o_free, ((bits >> 3) & 1u) ^ 1u, abort))
+        return false;
+      tc_fence_after();
+      // 16 keys per step: 16 rows of 128 bytes in every d panel
+      const uint64_t vdesc =
+          smem_desc_sw128(smem_u32(sV + pstage * C::kKVBytes), C::kKVPanel, 1024);
+      const uint32_t s_col = tmem + pstage * BK;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          // keys [16kk, 16kk+16) sit in the P half of the group that owns them
-          const int half = (kk * 16) / C::kHalfS;
-          const uint32_t a_col = s_col + half * C::kHalfS + (kk * 16 - half * C::kHalfS) / 2;
-          // 16 keys per step: 16 rows of 128 bytes in every d panel
-          const uint64_t bd = smem_desc_sw128(v_base + kk * 16 * 128, C::kKVPanel, 1024);
-          mma_ts(tmem + C::kO, tmem + a_col, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+          // keys [16kk, 16kk+16) belong to group 16kk / kCols, whose P starts
+          // at that group's first S column
+          constexpr int kW = C::kCols;
+          const int grp = (kk * 16) / kW;
+          const uint32_t a_col = s_col + grp * kW + (kk * 16 - grp * kW) / 2;
+          mma_ts(tmem + C::kO, a_col, vdesc + uint64_t((kk * 16 * 128) >> 4), idesc_pv,
+                 (first && kk == 0) ? 0u : 1u);
         }
-        mma_commit(&sh->v_empty[vs]);
-        mma_commit(&sh->o_done);
-        return true;
-      };
+        mma_commit(&sh->v_empty[pstage]);
+        mma_commit(&sh->pv_done[pstage]);
+        if (last) mma_commit(&sh->o_last);
+      }
+      __syncwarp();
+      ++pvn;
+      if (++pstage == 3) {
+        pstage = 0;
+        pphase ^= 1u;
+      }
+      return true;
+    };
 
-      for (;;) {
-        const int slot = qi % kNI;
-        if (!mbar_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+    for (;;) {
+      const int slot = qi % kNI;
+      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      const int n = sh->info[slot].n;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->info_empty[slot]);
+      if (n == 0) break;
+      // while this item's Q tile is still in flight, give the tensor pipe the
+      // P.V products that are waiting
+      while (pvn < kb) {
+        bool qready = true;
+        if (lane == 0) qready = mbar_test(&sh->q_full[0], qi & 1);
+        if (__shfl_sync(0xffffffffu, qready ? 1 : 0, 0)) break;
+        if (!issue_pv(0)) {
           ok = false;
           break;
         }
-        const int n = sh->info[slot].n;
-        mbar_arrive(&sh->info_empty[slot]);
-        if (n == 0) break;
-        const int qs = qi % C::kNQ;
-        if (!mbar_wait(&sh->q_full[qs], (qi / C::kNQ) & 1, abort)) {
+      }
+      if (!ok) break;
+      if (!warp_wait(&sh->q_full[0], qi & 1, abort)) {
+        ok = false;
+        break;
+      }
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      for (int t = 0; t < n; ++t) {
+        // after this Q.K^T, P.V of block kb-2 follows (when it exists)
+        const bool with_pv = (kb + 1 - pvn) > 2;
+        const uint32_t pbits = (pend >> (4 * (pvn & 3))) & 15u;
+        const bool need_o = with_pv && (pbits & 1u) && (pbits & 4u);
+        // lane 0: K, 1: P, 2: V, 3: O (others repeat lane 0's test)
+        uint64_t* bar = &sh->k_full[qstage];
+        uint32_t par = qphase;
+        if (lane == 1 && with_pv) { bar = &sh->p_full[pstage]; par = pphase; }
+        if (lane == 2 && with_pv) { bar = &sh->v_full[pstage]; par = pphase; }
+        if (lane == 3 && need_o) { bar = &sh->o_free; par = ((pbits >> 3) & 1u) ^ 1u; }
+        const uint32_t have = __ballot_sync(0xffffffffu, mbar_test(bar, par)) & 15u;
+        if (!(have & 1u) && !warp_wait(&sh->k_full[qstage], qphase, abort)) {
           ok = false;
           break;
         }
-        const uint32_t q_base = smem_u32(sQ + qs * C::kQBytes);
-        for (int t = 0; t < n; ++t) {
-          const int ks = kb % C::kNK;
-          if (!mbar_wait(&sh->k_full[ks], (kb / C::kNK) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t k_base = smem_u32(sK + ks * C::kKVBytes);
-          const uint32_t s_tmem = tmem + ((kb & 1) ? C::kS1 : C::kS0);
+        tc_fence_after();
+        const uint64_t kdesc = smem_desc_sw128(smem_u32(sK + qstage * C::kKVBytes), 16, 1024);
+        // S buffer kb % 3 is free: P.V of block kb-3 was issued before (in-order pipe)
+        const uint32_t s_tmem = tmem + qstage * BK;
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // 16 dims per step: panel kk/4, 32-byte column offset inside the
             // swizzle atom (the hardware applies the XOR on the full address)
-            const uint32_t off = (kk % 4) * 32;
-            const uint64_t ad = smem_desc_sw128(q_base + (kk / 4) * C::kQPanel + off, 16, 1024);
-            const uint64_t bd =
-                smem_desc_sw128(k_base + (kk / 4) * C::kKVPanel + off, 16, 1024);
-            mma_ss(s_tmem, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            const uint32_t qoff = (kk / 4) * C::kQPanel + (kk % 4) * 32;
+            const uint32_t koff = (kk / 4) * C::kKVPanel + (kk % 4) * 32;
+            mma_ss(s_tmem, qdesc + uint64_t(qoff >> 4), kdesc + uint64_t(koff >> 4), idesc_qk,
+                   kk > 0 ? 1u : 0u);
           }
-          mma_commit(&sh->s_full[kb & 1]);
-          mma_commit(&sh->k_empty[ks]);
-          if (t == n - 1) mma_commit(&sh->q_empty[qs]);
-          if (t > 0 && !issue_pv(kb - 1, t == 1)) {
-            ok = false;
-            break;
-          }
-          ++kb;
+          mma_commit(&sh->s_full[qstage]);
+          mma_commit(&sh->k_empty[qstage]);
+          if (t == n - 1) mma_commit(&sh->q_empty[0]);
         }
-        if (!ok) break;
-        if (!issue_pv(kb - 1, n == 1)) {
+        __syncwarp();
+        const uint32_t bits = (t == 0 ? 1u : 0u) | (t == n - 1 ? 2u : 0u) |
+                              (qi > 0 ? 4u : 0u) | ((qi & 1u) << 3);
+        pend = (pend & ~(15u << (4 * (kb & 3)))) | (bits << (4 * (kb & 3)));
+        ++kb;
+        if (++qstage == 3) {
+          qstage = 0;
+          qphase ^= 1u;
+        }
+        if (with_pv && !issue_pv(have)) {
           ok = false;
           break;
         }
-        mma_commit(&sh->o_last);
-        ++qi;
       }
+      if (!ok) break;
+      ++qi;
+    }
+    while (ok && pvn < kb)
+      if (!issue_pv(0)) ok = false;
+    if (lane == 0) {
       if (!ok) raise_abort(sh, p);
       // every MMA must be complete before the tensor memory is freed
       mma_commit(&sh->drain);
       mbar_wait(&sh->drain, 0, nullptr);
     }
   } else {
-    // ------------------------------------------------------ softmax groups
-    const int grp = (warp - 2) >> 2;              // 0: left half, 1: right half
+    // ------------------------------------------------- softmax groups
+    const int grp = (warp - 3) >> 2;              // column group 0..3
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     const int row = quarter * 32 + lane;          // query row within the tile
     const uint32_t lanes = tmem + (uint32_t(quarter * 32) << 16);
     const float c = p.scale_log2;
-    const uint32_t o_col = C::kO + grp * C::kHalfO;
-    uint32_t kb = 0, qi = 0;
+    const uint32_t o_col = C::kO + grp * C::kOCols;
+    uint32_t kb = 0, qi = 0, xn = 0;   // xn: uses of the exchange buffer so far
     bool ok = true;
+    bool after_epilogue = false;
     for (;;) {
       const int slot = qi % kNI;
       if (!mbar_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
@@ -392,62 +518,109 @@ __global__ void __launch_bounds__(320, 1)
       if (it.n == 0) break;
       float m_used = -INFINITY, l = 0.f;
       for (int t = 0; t < it.n; ++t) {
-        const int sb = kb & 1;
-        if (!mbar_wait(&sh->s_full[sb], (kb >> 1) & 1, abort)) {
+        const int sb = kb % C::kNS;
+        if (!mbar_wait(&sh->s_full[sb], (kb / C::kNS) & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t scol = (sb ? C::kS1 : C::kS0) + grp * C::kHalfS;
-        uint32_t sr[C::kHalfS / 32][32];
+        const uint32_t scol = sb * BK + grp * C::kCols;
+        float s[C::kCols];
+        if constexpr (C::kCols == 32) {
+          uint32_t sr[32];
+          tmem_ld32(lanes + scol, sr);
+          tmem_ld_wait(sr);
 #pragma unroll
-        for (int q = 0; q < C::kHalfS / 32; ++q) tmem_ld32(lanes + scol + q * 32, sr[q]);
-        tmem_ld_wait(sr[0]);
-#pragma unroll
-        for (int q = 1; q < C::kHalfS / 32; ++q) reg_fence(sr[q]);
-        float s[C::kHalfS];
-#pragma unroll
-        for (int q = 0; q < C::kHalfS / 32; ++q)
-#pragma unroll
-          for (int x = 0; x < 32; ++x) s[q * 32 + x] = __uint_as_float(sr[q][x]);
-        if (it.diag_last && t == it.n - 1) {
-          // key column grp*kHalfS + x is visible to row `row` when <= row
-#pragma unroll
-          for (int x = 0; x < C::kHalfS; ++x)
-            if (grp * C::kHalfS + x > row) s[x] = -INFINITY;
-        }
-        // partial row maximum over eight independent chains
-        float mx[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mx[a] = s[a];
-#pragma unroll
-        for (int x = 8; x + 16 <= C::kHalfS; x += 16)
-#pragma unroll
-          for (int a = 0; a < 8; ++a) mx[a] = max3(mx[a], s[x + a], s[x + 8 + a]);
-        if constexpr ((C::kHalfS - 8) % 16 != 0) {
-#pragma unroll
-          for (int a = 0; a < 8; ++a) mx[a] = fmaxf(mx[a], s[C::kHalfS - 8 + a]);
-        }
-        const float mine = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]),
-                                fmaxf(mx[6], mx[7]));
-        // exchange with the other group (same row, other half of the columns)
-        sh->xmax[sb][grp][row] = mine;
-        mbar_arrive(&sh->xmax_bar[sb]);
-        if (!mbar_wait(&sh->xmax_bar[sb], (kb >> 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        const float m_blk = fmaxf(mine, sh->xmax[sb][grp ^ 1][row]) * c;
-        if (t == 0) {
-          m_used = m_blk;
+          for (int x = 0; x < 32; ++x) s[x] = __uint_as_float(sr[x]);
         } else {
+          uint32_t sr[16];
+          tmem_ld16(lanes + scol, sr);
+          tmem_ld_wait(sr);
+#pragma unroll
+          for (int x = 0; x < 16; ++x) s[x] = __uint_as_float(sr[x]);
+        }
+        if (it.diag_last && t == it.n - 1) {
+          // key column grp*kCols + x is visible to row `row` when <= row
+#pragma unroll
+          for (int x = 0; x < C::kCols; ++x)
+            if (grp * C::kCols + x > row) s[x] = -INFINITY;
+        }
+        // partial row maximum over four independent chains
+        float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int x = 4; x + 8 <= C::kCols; x += 8)
+#pragma unroll
+          for (int a = 0; a < 4; ++a) mx[a] = max3(mx[a], s[x + a], s[x + 4 + a]);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], s[C::kCols - 4 + a]);
+        const float mine = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
+        // Exchange with the other groups through the single buffer xch.  Its
+        // previous use must be over in every group: after a block, all have
+        // posted that block's P; after an epilogue, all have freed O.
+        if (xn > 0) {
+          const bool okw = after_epilogue
+                               ? mbar_wait(&sh->o_free, (qi - 1) & 1, abort)
+                               : mbar_wait(&sh->p_full[(kb - 1) % C::kNS],
+                                           ((kb - 1) / C::kNS) & 1, abort);
+          if (!okw) {
+            ok = false;
+            break;
+          }
+        }
+        sh->xch[grp][row] = mine;
+        mbar_arrive(&sh->xch_bar);
+        after_epilogue = false;
+        if (t == 0) {
+          // first block of the item: the row maximum must be known first
+          if (!mbar_wait(&sh->xch_bar, xn & 1, abort)) {
+            ok = false;
+            break;
+          }
+          m_used = max3(fmaxf(sh->xch[0][row], sh->xch[1][row]), sh->xch[2][row],
+                        sh->xch[3][row]) * c;
+        }
+        // P = 2^(s*c - m) in bf16 with the running maximum m_used, written
+        // over this group's S columns.  When the exchange shows that the
+        // block raised a row's maximum by more than 2^8 (rare), that row's P
+        // and sum are scaled down after O is.
+        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+        {
+          uint32_t pk[C::kCols / 2];
+          const float nm = -m_used;
+#pragma unroll
+          for (int x = 0; x < C::kCols / 2; ++x) {
+            float a0, a1;
+            fma2(a0, a1, s[2 * x], s[2 * x + 1], c, c, nm, nm);
+            pk[x] = pack_bf16x2(ex2(a0), ex2(a1));
+            // the normaliser sums the rounded values
+            if (x & 1)
+              add2(sum2, sum3, __uint_as_float(pk[x] << 16),
+                   __uint_as_float(pk[x] & 0xFFFF0000u));
+            else
+              add2(sum0, sum1, __uint_as_float(pk[x] << 16),
+                   __uint_as_float(pk[x] & 0xFFFF0000u));
+          }
+          if constexpr (C::kCols == 32) {
+            tmem_st16(lanes + scol, pk);
+          } else {
+            tmem_st8(lanes + scol, pk);
+          }
+        }
+        if (t > 0) {
+          if (!mbar_wait(&sh->xch_bar, xn & 1, abort)) {
+            ok = false;
+            break;
+          }
+          const float m_blk = max3(fmaxf(sh->xch[0][row], sh->xch[1][row]), sh->xch[2][row],
+                                   sh->xch[3][row]) * c;
           const bool need = m_blk > m_used + 8.0f;
           if (__any_sync(0xffffffffu, need)) {
             // O still receives P V of the previous block: let it finish first.
-            // The parity wait is unambiguous: S of this block was committed
-            // after P V of block kb-2, so at least kb-1 phases are complete,
-            // and P V of this block is not issued yet.
-            if (!mbar_wait(&sh->o_done, (kb - 1) & 1, abort)) {
+            // pv_done[(kb-1) % 3] is unambiguous here: S of this block was
+            // committed after P.V of block kb-3 was issued, so that earlier
+            // phase is complete, and P.V of block kb+2 cannot have run.
+            const uint32_t pb = kb - 1;
+            if (!mbar_wait(&sh->pv_done[pb % C::kNS], (pb / C::kNS) & 1, abort)) {
               ok = false;
               break;
             }
@@ -458,38 +631,49 @@ __global__ void __launch_bounds__(320, 1)
               m_used = m_blk;
               l *= alpha;
             }
-#pragma unroll
-            for (int q = 0; q < C::kHalfO / 32; ++q) {
+            if constexpr (C::kOCols == 32) {
               uint32_t r[32];
-              tmem_ld32(lanes + o_col + q * 32, r);
+              tmem_ld32(lanes + o_col, r);
               tmem_ld_wait(r);
 #pragma unroll
               for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-              tmem_st32(lanes + o_col + q * 32, r);
+              tmem_st32(lanes + o_col, r);
+            } else {
+              uint32_t r[16];
+              tmem_ld16(lanes + o_col, r);
+              tmem_ld_wait(r);
+#pragma unroll
+              for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+              tmem_st16(lanes + o_col, r);
             }
             tmem_st_wait();
+            // this row's P (already in TMEM) is scaled the same way; rows
+            // that keep their maximum scale by 1
+            float t0 = 0.f, t1 = 0.f;
+            uint32_t r[16];
+            tmem_ld16(lanes + scol, r);      // kCols / 2 <= 16 words used
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int x = 0; x < C::kCols / 2; ++x) {
+              r[x] = pack_bf16x2(__uint_as_float(r[x] << 16) * alpha,
+                                 __uint_as_float(r[x] & 0xFFFF0000u) * alpha);
+              t0 += __uint_as_float(r[x] << 16);
+              t1 += __uint_as_float(r[x] & 0xFFFF0000u);
+            }
+            if constexpr (C::kCols == 32) {
+              tmem_st16(lanes + scol, r);
+            } else {
+              uint32_t w[8];
+#pragma unroll
+              for (int x = 0; x < 8; ++x) w[x] = r[x];
+              tmem_st8(lanes + scol, w);
+            }
+            sum0 = t0;
+            sum1 = t1;
+            sum2 = sum3 = 0.f;
           }
         }
-        // P = 2^(s*c - m) in bf16, written over this group's S columns; the
-        // normaliser sums the rounded values
-        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-        const float nm = -m_used;
-        uint32_t pk[C::kHalfS / 2];
-#pragma unroll
-        for (int x = 0; x < C::kHalfS / 2; ++x) {
-          float a0, a1;
-          fma2(a0, a1, s[2 * x], s[2 * x + 1], c, c, nm, nm);
-          pk[x] = pack_bf16x2(ex2(a0), ex2(a1));
-          if (x & 1)
-            add2(sum2, sum3, __uint_as_float(pk[x] << 16), __uint_as_float(pk[x] & 0xFFFF0000u));
-          else
-            add2(sum0, sum1, __uint_as_float(pk[x] << 16), __uint_as_float(pk[x] & 0xFFFF0000u));
-        }
-        if constexpr (C::kHalfS / 2 == 32) {
-          tmem_st32(lanes + scol, pk);
-        } else {
-          tmem_st16(lanes + scol, pk);
-        }
+        ++xn;
         tmem_st_wait();
         l += (sum0 + sum1) + (sum2 + sum3);
         tc_fence_before();
@@ -497,45 +681,52 @@ __global__ void __launch_bounds__(320, 1)
         ++kb;
       }
       if (!ok) break;
-      // ---- epilogue: exchange the partial sums, then O / l for this half.
-      // o_last has exactly one phase per item and this warp waits on every one.
-      sh->xsum[qi & 1][grp][row] = l;
-      mbar_arrive(&sh->xsum_bar[qi & 1]);
-      if (!mbar_wait(&sh->o_last, qi & 1, abort) ||
-          !mbar_wait(&sh->xsum_bar[qi & 1], (qi >> 1) & 1, abort)) {
+      // ---- epilogue: exchange the partial sums, then O / l for this group's
+      // columns.  o_last has exactly one phase per item, waited on every time.
+      if (!mbar_wait(&sh->p_full[(kb - 1) % C::kNS], ((kb - 1) / C::kNS) & 1, abort)) {
         ok = false;
         break;
       }
+      sh->xch[grp][row] = l;
+      mbar_arrive(&sh->xch_bar);
+      if (!mbar_wait(&sh->o_last, qi & 1, abort) || !mbar_wait(&sh->xch_bar, xn & 1, abort)) {
+        ok = false;
+        break;
+      }
+      ++xn;
       tc_fence_after();
-      const float lt = l + sh->xsum[qi & 1][grp ^ 1][row];
+      const float lt = (sh->xch[0][row] + sh->xch[1][row]) + (sh->xch[2][row] + sh->xch[3][row]);
       const float inv_l = 1.f / lt;
       const bool store = row < p.B;
       const size_t orow = size_t(it.h) * p.S + size_t(it.i) * p.B + size_t(row);
-#pragma unroll
-      for (int q = 0; q < C::kHalfO / 32; ++q) {
-        uint32_t r[32];
-        tmem_ld32(lanes + o_col + q * 32, r);
+      const int col = grp * C::kOCols;
+      uint32_t r[C::kOCols];
+      if constexpr (C::kOCols == 32) {
+        tmem_ld32(lanes + o_col, r);
         tmem_ld_wait(r);
-        if (!store) continue;
-        const int col = grp * C::kHalfO + q * 32;
+      } else {
+        tmem_ld16(lanes + o_col, r);
+        tmem_ld_wait(r);
+      }
+      if (store) {
         if (p.out_f32) {
           uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + orow * D + col);
 #pragma unroll
-          for (int x = 0; x < 8; ++x)
+          for (int x = 0; x < C::kOCols / 4; ++x)
             d4[x] = make_uint4(__float_as_uint(__uint_as_float(r[4 * x]) * inv_l),
                                __float_as_uint(__uint_as_float(r[4 * x + 1]) * inv_l),
                                __float_as_uint(__uint_as_float(r[4 * x + 2]) * inv_l),
                                __float_as_uint(__uint_as_float(r[4 * x + 3]) * inv_l));
         } else {
-          uint32_t ob[16];
+          uint32_t ob[C::kOCols / 2];
 #pragma unroll
-          for (int x = 0; x < 16; ++x)
+          for (int x = 0; x < C::kOCols / 2; ++x)
             ob[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
                                 __uint_as_float(r[2 * x + 1]) * inv_l);
           uint4* d4 =
               reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
 #pragma unroll
-          for (int x = 0; x < 4; ++x)
+          for (int x = 0; x < C::kOCols / 8; ++x)
             d4[x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
         }
       }
@@ -543,6 +734,7 @@ __global__ void __launch_bounds__(320, 1)
         p.lse[orow] = (m_used + log2f(lt)) * 0.6931471805599453f;
       tc_fence_before();
       mbar_arrive(&sh->o_free);
+      after_epilogue = true;
       ++qi;
     }
     if (!ok) raise_abort(sh, p);
@@ -593,7 +785,8 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int d, int box_
 template <int D, int BK>
 cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_failed) {
   using C = Cfg<D, BK>;
-  constexpr int kSmem = C::kData + int(sizeof(Shared)) + 1024;
+  // data stages + the small shared block; the kernel checks the alignment
+  constexpr int kSmem = C::kData + int(sizeof(Shared));
   static_assert(kSmem <= 232448, "shared memory budget");
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, a.q, uint64_t(a.Hq) * a.S, D, C::kM) ||
@@ -623,7 +816,7 @@ cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_fai
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   if (a.num_workers == 0) return cudaSuccess;
-  kern<<<a.num_workers, C::kThreads, kSmem, st>>>(tq, tk, tv, p);
+  kern<<<a.num_workers, kThreads, kSmem, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -87,7 +87,9 @@ enum {
   SA_DEV_BAD_INDEX = 1,      /* a block index outside [0, i] was clamped     */
   SA_DEV_BAD_COUNT = 2,      /* a block count outside [1, min(kmax,i+1)]     */
   SA_DEV_TIMEOUT = 4,        /* a bounded wait gave up; outputs are invalid  */
-  SA_DEV_BAD_ITEM = 8        /* a schedule entry outside the item range      */
+  SA_DEV_BAD_ITEM = 8,       /* a schedule entry outside the item range      */
+  SA_DEV_BAD_LAUNCH = 16     /* the kernel found its shared memory misaligned
+                                and did nothing; outputs are not written     */
 };
 
 typedef struct sa_shape {
