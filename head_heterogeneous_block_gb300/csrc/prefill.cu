@@ -70,9 +70,11 @@ struct Cfg {
 };
 
 constexpr int kNI = 4;                 // item-metadata ring slots
-constexpr int kSoftmaxWarps = 16;      // warps 3..18
+constexpr int kSoftmaxWarps = 16;      // warps 4..19
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
-constexpr int kThreads = 96 + kSoftmaxThreads;   // + producer K/Q, MMA, producer V
+// warp 0: producer (items, Q, K); 1: Q.K^T issuer; 2: producer (V);
+// 3: P.V issuer -- one per scheduler -- then the softmax warps
+constexpr int kThreads = 128 + kSoftmaxThreads;
 
 struct ItemInfo {
   int32_t h, i, n, diag_last;   // n == 0: end of this worker's list
@@ -88,7 +90,7 @@ struct Shared {
   uint64_t o_last;        // one phase per item, after its last P.V (epilogue)
   uint64_t o_free;        // one phase per item: every group finished the epilogue
   uint64_t xch_bar;       // exchange between the softmax groups
-  uint64_t drain;
+  uint64_t drain_qk, drain_pv;
   uint64_t info_full[kNI], info_empty[kNI];
   ItemInfo info[kNI];
   float xch[4][128];      // [group][row]: partial row max per block, partial sum per item
@@ -162,12 +164,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kNI; ++s) {
       mbar_init(&sh->info_full[s], 1);
-      mbar_init(&sh->info_empty[s], 2 + kSoftmaxWarps);
+      mbar_init(&sh->info_empty[s], 3 + kSoftmaxWarps);
     }
     mbar_init(&sh->o_last, 1);
     mbar_init(&sh->o_free, kSoftmaxThreads);
     mbar_init(&sh->xch_bar, kSoftmaxThreads);
-    mbar_init(&sh->drain, 1);
+    mbar_init(&sh->drain_qk, 1);
+    mbar_init(&sh->drain_pv, 1);
     sh->abort = 0;
     fence_mbar_init();
   }
@@ -347,68 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_ring(sh->v_full, viss, C::kNV);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------- MMA issuer
-    // The whole warp runs the loop (waits, descriptors); one elected lane
-    // issues the MMAs and commits.  Q.K^T of block b is issued two blocks
-    // ahead of P.V of block b-2, across item boundaries, so the tensor pipe
-    // has work while the softmax of the two blocks in between runs.
+    // ------------------------------------------------- Q.K^T issuer
+    // The whole warp runs the loop; one elected lane issues and commits.
+    // S buffer b % 3 is reused once P.V of block b-3 has completed.  The
+    // barrier phases a step needs are tested together (one non-blocking test
+    // per lane, one ballot) and only the missing ones are waited on.
     constexpr uint32_t idesc_qk = idesc_bf16(128, BK, 0, 0);  // Q, K both K-major
-    constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);   // P (TMEM), V MN-major
-    uint32_t qi = 0, kb = 0, pvn = 0;
-    // per pending block b, 4 bits at 4*(b % 4): opens its item, closes its
-    // item, its item is not the worker's first, parity of its item index
-    uint32_t pend = 0;
+    static_assert(C::kNK == 3 && C::kNS == 3, "shared ring indexing");
+    uint32_t qi = 0, kb = 0, stage = 0, phase = 0;
     bool ok = true;
-
-    // Each step needs the K of the next Q.K^T and the P, V (and, for an
-    // item's first block, the freed O) of the next P.V.  Their phases are
-    // first tested together -- one barrier per lane, one try_wait for the
-    // whole warp, one ballot -- and only the ones not yet complete are
-    // waited on, so the issuing warp spends few round trips per step.
-    // K, V and S/P rings all have three stages: stage = block % 3 and the
-    // phase bit flips every three blocks; both are kept incrementally.
-    static_assert(C::kNK == 3 && C::kNV == 3 && C::kNS == 3, "shared ring indexing");
-    uint32_t qstage = 0, qphase = 0;     // block kb (next Q.K^T)
-    uint32_t pstage = 0, pphase = 0;     // block pvn (next P.V)
-
-    auto issue_pv = [&](uint32_t have) -> bool {
-      const uint32_t bits = (pend >> (4 * (pvn & 3))) & 15u;
-      const bool first = bits & 1u, last = bits & 2u;
-      if (!(have & 2u) && !warp_wait(&sh->p_full[pstage], pphase, abort)) return false;
-      if (!(have & 4u) && !warp_wait(&sh->v_full[pstage], pphase, abort)) return false;
-      // the previous item's epilogue must have read O before it is overwritten
-      if (first && (bits & 4u) && !(have & 8u) &&
-          !warp_wait(&sh->o_free, ((bits >> 3) & 1u) ^ 1u, abort))
-        return false;
-      tc_fence_after();
-      // 16 keys per step: 16 rows of 128 bytes in every d panel
-      const uint64_t vdesc =
-          smem_desc_sw128(smem_u32(sV + pstage * C::kKVBytes), C::kKVPanel, 1024);
-      const uint32_t s_col = tmem + pstage * BK;
-      if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // keys [16kk, 16kk+16) belong to group 16kk / kCols, whose P starts
-          // at that group's first S column
-          constexpr int kW = C::kCols;
-          const int grp = (kk * 16) / kW;
-          const uint32_t a_col = s_col + grp * kW + (kk * 16 - grp * kW) / 2;
-          mma_ts(tmem + C::kO, a_col, vdesc + uint64_t((kk * 16 * 128) >> 4), idesc_pv,
-                 (first && kk == 0) ? 0u : 1u);
-        }
-        mma_commit(&sh->v_empty[pstage]);
-        mma_commit(&sh->pv_done[pstage]);
-        if (last) mma_commit(&sh->o_last);
-      }
-      __syncwarp();
-      ++pvn;
-      if (++pstage == 3) {
-        pstage = 0;
-        pphase ^= 1u;
-      }
-      return true;
-    };
-
     for (;;) {
       const int slot = qi % kNI;
       if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
@@ -419,43 +369,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->info_empty[slot]);
       if (n == 0) break;
-      // while this item's Q tile is still in flight, give the tensor pipe the
-      // P.V products that are waiting
-      while (pvn < kb) {
-        bool qready = true;
-        if (lane == 0) qready = mbar_test(&sh->q_full[0], qi & 1);
-        if (__shfl_sync(0xffffffffu, qready ? 1 : 0, 0)) break;
-        if (!issue_pv(0)) {
-          ok = false;
-          break;
-        }
-      }
-      if (!ok) break;
       if (!warp_wait(&sh->q_full[0], qi & 1, abort)) {
         ok = false;
         break;
       }
       const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       for (int t = 0; t < n; ++t) {
-        // after this Q.K^T, P.V of block kb-2 follows (when it exists)
-        const bool with_pv = (kb + 1 - pvn) > 2;
-        const uint32_t pbits = (pend >> (4 * (pvn & 3))) & 15u;
-        const bool need_o = with_pv && (pbits & 1u) && (pbits & 4u);
-        // lane 0: K, 1: P, 2: V, 3: O (others repeat lane 0's test)
-        uint64_t* bar = &sh->k_full[qstage];
-        uint32_t par = qphase;
-        if (lane == 1 && with_pv) { bar = &sh->p_full[pstage]; par = pphase; }
-        if (lane == 2 && with_pv) { bar = &sh->v_full[pstage]; par = pphase; }
-        if (lane == 3 && need_o) { bar = &sh->o_free; par = ((pbits >> 3) & 1u) ^ 1u; }
-        const uint32_t have = __ballot_sync(0xffffffffu, mbar_test(bar, par)) & 15u;
-        if (!(have & 1u) && !warp_wait(&sh->k_full[qstage], qphase, abort)) {
+        // lane 0: K of this block; lane 1: P.V of block kb-3 (same S buffer)
+        const bool reuse = kb >= 3;
+        uint64_t* bar = &sh->k_full[stage];
+        uint32_t par = phase;
+        if (lane == 1 && reuse) {
+          bar = &sh->pv_done[stage];
+          par = phase ^ 1u;
+        }
+        const uint32_t have = __ballot_sync(0xffffffffu, mbar_test(bar, par));
+        if (!(have & 1u) && !warp_wait(&sh->k_full[stage], phase, abort)) {
+          ok = false;
+          break;
+        }
+        if (reuse && !(have & 2u) && !warp_wait(&sh->pv_done[stage], phase ^ 1u, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t kdesc = smem_desc_sw128(smem_u32(sK + qstage * C::kKVBytes), 16, 1024);
-        // S buffer kb % 3 is free: P.V of block kb-3 was issued before (in-order pipe)
-        const uint32_t s_tmem = tmem + qstage * BK;
+        const uint64_t kdesc = smem_desc_sw128(smem_u32(sK + stage * C::kKVBytes), 16, 1024);
+        const uint32_t s_tmem = tmem + stage * BK;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -466,38 +405,103 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(s_tmem, qdesc + uint64_t(qoff >> 4), kdesc + uint64_t(koff >> 4), idesc_qk,
                    kk > 0 ? 1u : 0u);
           }
-          mma_commit(&sh->s_full[qstage]);
-          mma_commit(&sh->k_empty[qstage]);
+          mma_commit(&sh->s_full[stage]);
+          mma_commit(&sh->k_empty[stage]);
           if (t == n - 1) mma_commit(&sh->q_empty[0]);
         }
         __syncwarp();
-        const uint32_t bits = (t == 0 ? 1u : 0u) | (t == n - 1 ? 2u : 0u) |
-                              (qi > 0 ? 4u : 0u) | ((qi & 1u) << 3);
-        pend = (pend & ~(15u << (4 * (kb & 3)))) | (bits << (4 * (kb & 3)));
         ++kb;
-        if (++qstage == 3) {
-          qstage = 0;
-          qphase ^= 1u;
-        }
-        if (with_pv && !issue_pv(have)) {
-          ok = false;
-          break;
+        if (++stage == 3) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
       if (!ok) break;
       ++qi;
     }
-    while (ok && pvn < kb)
-      if (!issue_pv(0)) ok = false;
     if (lane == 0) {
       if (!ok) raise_abort(sh, p);
       // every MMA must be complete before the tensor memory is freed
-      mma_commit(&sh->drain);
-      mbar_wait(&sh->drain, 0, nullptr);
+      mma_commit(&sh->drain_qk);
+      mbar_wait(&sh->drain_qk, 0, nullptr);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------- P.V issuer
+    constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);   // P (TMEM), V MN-major
+    static_assert(C::kNV == 3 && C::kNS == 3, "shared ring indexing");
+    uint32_t qi = 0, stage = 0, phase = 0;
+    bool ok = true;
+    for (;;) {
+      const int slot = qi % kNI;
+      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+        ok = false;
+        break;
+      }
+      const int n = sh->info[slot].n;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->info_empty[slot]);
+      if (n == 0) break;
+      for (int t = 0; t < n; ++t) {
+        const bool first = t == 0;
+        const bool need_o = first && qi > 0;   // previous item's epilogue must read O first
+        // lane 0: P, lane 1: V, lane 2: O
+        uint64_t* bar = &sh->p_full[stage];
+        uint32_t par = phase;
+        if (lane == 1) bar = &sh->v_full[stage];
+        if (lane == 2 && need_o) {
+          bar = &sh->o_free;
+          par = (qi - 1) & 1;
+        }
+        const uint32_t have = __ballot_sync(0xffffffffu, mbar_test(bar, par));
+        if (!(have & 1u) && !warp_wait(&sh->p_full[stage], phase, abort)) {
+          ok = false;
+          break;
+        }
+        if (!(have & 2u) && !warp_wait(&sh->v_full[stage], phase, abort)) {
+          ok = false;
+          break;
+        }
+        if (need_o && !(have & 4u) && !warp_wait(&sh->o_free, (qi - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // 16 keys per step: 16 rows of 128 bytes in every d panel
+        const uint64_t vdesc =
+            smem_desc_sw128(smem_u32(sV + stage * C::kKVBytes), C::kKVPanel, 1024);
+        const uint32_t s_col = tmem + stage * BK;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // keys [16kk, 16kk+16) belong to group 16kk / kCols, whose P starts
+            // at that group's first S column
+            constexpr int kW = C::kCols;
+            const int grp = (kk * 16) / kW;
+            const uint32_t a_col = s_col + grp * kW + (kk * 16 - grp * kW) / 2;
+            mma_ts(tmem + C::kO, a_col, vdesc + uint64_t((kk * 16 * 128) >> 4), idesc_pv,
+                   (first && kk == 0) ? 0u : 1u);
+          }
+          mma_commit(&sh->v_empty[stage]);
+          mma_commit(&sh->pv_done[stage]);
+          if (t == n - 1) mma_commit(&sh->o_last);
+        }
+        __syncwarp();
+        if (++stage == 3) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      ++qi;
+    }
+    if (lane == 0) {
+      if (!ok) raise_abort(sh, p);
+      mma_commit(&sh->drain_pv);
+      mbar_wait(&sh->drain_pv, 0, nullptr);
     }
   } else {
     // ------------------------------------------------- softmax groups
-    const int grp = (warp - 3) >> 2;              // column group 0..3
+    const int grp = (warp - 4) >> 2;              // column group 0..3
     const int quarter = warp & 3;                 // TMEM lane quarter of this warp
     const int row = quarter * 32 + lane;          // query row within the tile
     const uint32_t lanes = tmem + (uint32_t(quarter * 32) << 16);
@@ -616,9 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool need = m_blk > m_used + 8.0f;
           if (__any_sync(0xffffffffu, need)) {
             // O still receives P V of the previous block: let it finish first.
-            // pv_done[(kb-1) % 3] is unambiguous here: S of this block was
-            // committed after P.V of block kb-3 was issued, so that earlier
-            // phase is complete, and P.V of block kb+2 cannot have run.
+            // pv_done[(kb-1) % 3] is unambiguous here: this block's S buffer
+            // was reused only after P.V of block kb-3 completed, and P.V of
+            // block kb+2 cannot have run.
             const uint32_t pb = kb - 1;
             if (!mbar_wait(&sh->pv_done[pb % C::kNS], (pb / C::kNS) & 1, abort)) {
               ok = false;
