@@ -1,0 +1,63 @@
+"""The bench's multi-replica timing on two CPU ranks (gloo).
+
+With N > 1 every rank runs an independent replica of the layer; the job's time
+is the slowest rank's, and the reported throughput is all replicas' work over
+that time.  This checks that reduction with two processes on the host.
+"""
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank: int, world: int, port: int, out):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = [120.0, 150.0][rank]              # rank 1 is the slow replica
+        total = bench.max_over_ranks(local_ms, torch.device("cpu"))
+        value = bench.job_value(8.0e12, world, 10, total)
+        out.put((rank, total, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_value_two_ranks():
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, total, value in res:
+        assert total == 150.0                        # every rank sees the slowest time
+        # 2 replicas x 10 steps x 8 TFLOP over 0.15 s
+        assert value == pytest.approx(2 * 10 * 8.0 / 0.150)
+
+
+def test_single_process_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.max_over_ranks(3.5, torch.device("cpu")) == 3.5
+    assert bench.job_value(1e12, 1, 4, 2000.0) == pytest.approx(2.0)
