@@ -3,34 +3,39 @@
 // One persistent CTA per schedule worker walks that worker's (head,
 // query-block) items.  For every item it loads the 128-row query tile once
 // and then, for each selected key block j, computes S = Q K_j^T and
-// O += softmax(S) V_j with flash-style online softmax:
+// O += softmax(S) V_j with flash-style online softmax.  Twenty warps:
 //
 //   warp 0      producer: reads the schedule, the block counts and the block
 //               lists (32 indices per load), publishes each item's metadata
 //               through a small shared-memory ring, and issues TMA loads of
-//               the Q tile and the selected K / V blocks (128-byte-swizzled
-//               boxes of the [heads*S, d] view) into rings of stages.
-//   warp 1      MMA issuer (one elected lane): tcgen05.mma kind::f16, bf16 inputs,
-//               fp32 accumulators in tensor memory.  S_j alternates between
-//               two TMEM buffers so Q K_{j+1}^T overlaps the softmax of block
-//               j; P_j is written back into S_j's columns (bf16) and is the
-//               TMEM A operand of P V.  O accumulates in TMEM.
-//   warps 2-9   softmax, two warpgroups: each row of the tile has one thread
-//               in each group, which take the left and right halves of the
-//               S columns (and of O).  The halves exchange their partial row
-//               maxima through shared memory, so both keep the same running
-//               max; O is rescaled in TMEM only when the max grew by more
-//               than 2^8 (the stale max cancels in the final division).  The
-//               normaliser sums the same bf16-rounded weights that enter P V.
-//               Epilogue: O / l in fp32 or bf16, and the log-sum-exp.
+//               the Q tile and the selected K blocks (128-byte-swizzled boxes
+//               of the [heads*S, d] view) into a ring of stages.
+//   warp 2      producer of the V blocks (its own ring).
+//   warp 1      Q K^T issuer: tcgen05.mma kind::f16 (bf16 in, fp32 out), both
+//               operands from shared memory, into one of three S buffers in
+//               tensor memory; it runs up to three blocks ahead of P V.
+//   warp 3      P V issuer: P (bf16, written over its S buffer) is the
+//               tensor-memory A operand, V the shared-memory B operand, O
+//               accumulates in tensor memory.  The four control warps sit on
+//               the four schedulers.
+//   warps 4-19  softmax, four column groups of four warps: each thread owns
+//               one row of the tile and a quarter of its S columns (and of
+//               O's).  The groups exchange partial row maxima through a
+//               double-buffered shared array; a block's exponentials use the
+//               running maximum, and when the exchange shows that the block
+//               raised a row's maximum by more than 2^8 (rare), O and that
+//               row's P are scaled down before P V.  The stale maximum cancels
+//               in O / l.  The normaliser sums the same bf16-rounded weights
+//               that enter P V.  Epilogue: O / l in fp32 or bf16, and the
+//               log-sum-exp.
 //
 // The work items and their order come from the plan's LPT schedule (S-HPLB,
 // "Algoritmo Greedy"), with workers = CTAs instead of GPUs.
 // Every index read from idx / cnt / the schedule is range-checked; bad values
 // are clamped and flagged in the device status word, never dereferenced.
-// Every wait (including the exchanges between the two softmax groups) is a
-// bounded mbarrier wait; on a timeout the CTA flags SA_DEV_TIMEOUT, lets its
-// copies and MMAs drain, frees its tensor memory and exits.
+// Every wait is a bounded mbarrier wait; on a timeout the CTA flags
+// SA_DEV_TIMEOUT, lets its copies and MMAs drain, frees its tensor memory and
+// exits.
 
 #include <cuda_bf16.h>
 
@@ -55,7 +60,7 @@ struct Cfg {
   static constexpr int kKVBytes = BK * D * 2;
   static constexpr int kNQ = 1;                   // Q stages
   static constexpr int kNK = 3;                   // K stages
-  static constexpr int kNV = 3;                   // V stages (P.V trails Q.K^T by two blocks)
+  static constexpr int kNV = 2;                   // V stages (a V load has ~2 block periods)
   static constexpr int kNS = 3;                   // S buffers in tensor memory
   static constexpr int kGroups = 4;               // softmax column groups
   static constexpr int kCols = BK / kGroups;      // S columns per group
@@ -93,7 +98,8 @@ struct Shared {
   uint64_t drain_qk, drain_pv;
   uint64_t info_full[kNI], info_empty[kNI];
   ItemInfo info[kNI];
-  float xch[4][128];      // [group][row]: partial row max per block, partial sum per item
+  float xch[2][4][128];   // [use parity][group][row]: partial row max per block, or
+                          // partial sum per item; use u goes to buffer u & 1
   uint32_t tmem_base;
   int abort;
 };
@@ -428,8 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 3) {
     // ------------------------------------------------- P.V issuer
     constexpr uint32_t idesc_pv = idesc_bf16(128, D, 0, 1);   // P (TMEM), V MN-major
-    static_assert(C::kNV == 3 && C::kNS == 3, "shared ring indexing");
-    uint32_t qi = 0, stage = 0, phase = 0;
+    static_assert(C::kNS == 3, "S ring indexing");
+    uint32_t qi = 0, stage = 0, phase = 0;   // S / P buffers
+    uint32_t vstage = 0, vphase = 0;         // V ring
     bool ok = true;
     for (;;) {
       const int slot = qi % kNI;
@@ -447,7 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lane 0: P, lane 1: V, lane 2: O
         uint64_t* bar = &sh->p_full[stage];
         uint32_t par = phase;
-        if (lane == 1) bar = &sh->v_full[stage];
+        if (lane == 1) {
+          bar = &sh->v_full[vstage];
+          par = vphase;
+        }
         if (lane == 2 && need_o) {
           bar = &sh->o_free;
           par = (qi - 1) & 1;
@@ -457,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (!(have & 2u) && !warp_wait(&sh->v_full[stage], phase, abort)) {
+        if (!(have & 2u) && !warp_wait(&sh->v_full[vstage], vphase, abort)) {
           ok = false;
           break;
         }
@@ -468,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // 16 keys per step: 16 rows of 128 bytes in every d panel
         const uint64_t vdesc =
-            smem_desc_sw128(smem_u32(sV + stage * C::kKVBytes), C::kKVPanel, 1024);
+            smem_desc_sw128(smem_u32(sV + vstage * C::kKVBytes), C::kKVPanel, 1024);
         const uint32_t s_col = tmem + stage * BK;
         if (elect_one()) {
 #pragma unroll
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + C::kO, a_col, vdesc + uint64_t((kk * 16 * 128) >> 4), idesc_pv,
                    (first && kk == 0) ? 0u : 1u);
           }
-          mma_commit(&sh->v_empty[stage]);
+          mma_commit(&sh->v_empty[vstage]);
           mma_commit(&sh->pv_done[stage]);
           if (t == n - 1) mma_commit(&sh->o_last);
         }
@@ -489,6 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == 3) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (++vstage == C::kNV) {
+          vstage = 0;
+          vphase ^= 1u;
         }
       }
       if (!ok) break;
@@ -509,7 +523,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_col = C::kO + grp * C::kOCols;
     uint32_t kb = 0, qi = 0, xn = 0;   // xn: uses of the exchange buffer so far
     bool ok = true;
-    bool after_epilogue = false;
     for (;;) {
       const int slot = qi % kNI;
       if (!mbar_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
@@ -558,30 +571,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], s[C::kCols - 4 + a]);
         const float mine = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
-        // Exchange with the other groups through the single buffer xch.  Its
-        // previous use must be over in every group: after a block, all have
-        // posted that block's P; after an epilogue, all have freed O.
-        if (xn > 0) {
-          const bool okw = after_epilogue
-                               ? mbar_wait(&sh->o_free, (qi - 1) & 1, abort)
-                               : mbar_wait(&sh->p_full[(kb - 1) % C::kNS],
-                                           ((kb - 1) / C::kNS) & 1, abort);
-          if (!okw) {
-            ok = false;
-            break;
-          }
-        }
-        sh->xch[grp][row] = mine;
+        // Exchange with the other groups.  Use xn writes buffer xn & 1: every
+        // thread read use xn-2 before it posted use xn-1, and this thread saw
+        // use xn-1 complete, so that buffer is free.
+        float* xb = &sh->xch[xn & 1][0][0];
+        xb[grp * 128 + row] = mine;
         mbar_arrive(&sh->xch_bar);
-        after_epilogue = false;
         if (t == 0) {
           // first block of the item: the row maximum must be known first
           if (!mbar_wait(&sh->xch_bar, xn & 1, abort)) {
             ok = false;
             break;
           }
-          m_used = max3(fmaxf(sh->xch[0][row], sh->xch[1][row]), sh->xch[2][row],
-                        sh->xch[3][row]) * c;
+          m_used = max3(fmaxf(xb[row], xb[128 + row]), xb[256 + row], xb[384 + row]) * c;
         }
         // P = 2^(s*c - m) in bf16 with the running maximum m_used, written
         // over this group's S columns.  When the exchange shows that the
@@ -615,8 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const float m_blk = max3(fmaxf(sh->xch[0][row], sh->xch[1][row]), sh->xch[2][row],
-                                   sh->xch[3][row]) * c;
+          const float m_blk =
+              max3(fmaxf(xb[row], xb[128 + row]), xb[256 + row], xb[384 + row]) * c;
           const bool need = m_blk > m_used + 8.0f;
           if (__any_sync(0xffffffffu, need)) {
             // O still receives P V of the previous block: let it finish first.
@@ -685,13 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++kb;
       }
       if (!ok) break;
-      // ---- epilogue: exchange the partial sums, then O / l for this group's
-      // columns.  o_last has exactly one phase per item, waited on every time.
-      if (!mbar_wait(&sh->p_full[(kb - 1) % C::kNS], ((kb - 1) / C::kNS) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      sh->xch[grp][row] = l;
+      // ---- epilogue: exchange the partial sums (the same double buffer), then
+      // O / l for this group's columns.  o_last has exactly one phase per
+      // item, waited on every time.
+      float* xb = &sh->xch[xn & 1][0][0];
+      xb[grp * 128 + row] = l;
       mbar_arrive(&sh->xch_bar);
       if (!mbar_wait(&sh->o_last, qi & 1, abort) || !mbar_wait(&sh->xch_bar, xn & 1, abort)) {
         ok = false;
@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++xn;
       tc_fence_after();
-      const float lt = (sh->xch[0][row] + sh->xch[1][row]) + (sh->xch[2][row] + sh->xch[3][row]);
+      const float lt = (xb[row] + xb[128 + row]) + (xb[256 + row] + xb[384 + row]);
       const float inv_l = 1.f / lt;
       const bool store = row < p.B;
       const size_t orow = size_t(it.h) * p.S + size_t(it.i) * p.B + size_t(row);
@@ -738,7 +738,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[orow] = (m_used + log2f(lt)) * 0.6931471805599453f;
       tc_fence_before();
       mbar_arrive(&sh->o_free);
-      after_epilogue = true;
       ++qi;
     }
     if (!ok) raise_abort(sh, p);
