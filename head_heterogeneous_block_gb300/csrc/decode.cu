@@ -1,12 +1,13 @@
 // Decode attention over the selected KV blocks (HBM-bound).
 //
 // One CTA per (sequence, query head), four warps.  Each warp takes every
-// fourth selected block: lane t scores token t of the 32-token block against
-// the query (16-byte loads of the key row), the warp keeps an online softmax,
-// and then accumulates P V with lane l owning dimensions [4l, 4l+4) (each
-// value row is one coalesced 256-byte load across the warp).  Key and value
-// rows of a block are loaded together before any arithmetic, so a warp has
-// 16 KB in flight per block.  The four partial states are merged by their
+// fourth selected block.  Lane l owns dimensions [4l, 4l+4) of every key and
+// value row, so each row of the 32-token block is one coalesced 256-byte load
+// across the warp; key and value rows are loaded together before any
+// arithmetic (16 KB in flight per warp and block).  Every lane forms 32
+// partial dot products over its four dimensions; a reduce-scatter over the
+// warp (31 shuffles) leaves the score of token t in lane t, the warp keeps an
+// online softmax, and then accumulates P V in the same dimension layout.  The four partial states are merged by their
 // log-sum-exp.  Streaming and retrieval heads differ only in their block
 // lists ("Riepilogo Tecnico: Fluxion", "Intuizioni Chiave" 2).
 
@@ -23,6 +24,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kB = 32;
 constexpr int kWarps = 4;
+static_assert(kB == 32 && kD == 4 * 32, "lane t <-> token t, lane l <-> dims [4l, 4l+4)");
 
 __global__ void __launch_bounds__(kWarps * 32) decode_attention_kernel(sa_k::DecodeArgs a,
                                                                        float scale_log2) {
@@ -51,31 +53,43 @@ __global__ void __launch_bounds__(kWarps * 32) decode_attention_kernel(sa_k::Dec
 
   float m = -INFINITY, l = 0.f;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
+  const float q4[4] = {sq[4 * lane], sq[4 * lane + 1], sq[4 * lane + 2], sq[4 * lane + 3]};
   for (int t = warp; t < n; t += kWarps) {
     int j = list[t];
     if (j < 0 || j >= nb) {
       if (lane == 0) atomicOr(a.dev_status, SA_DEV_BAD_INDEX);
       j = 0;
     }
-    const uint4* krow = reinterpret_cast<const uint4*>(K + (size_t(j) * kB + lane) * kD);
+    const uint2* kcol = reinterpret_cast<const uint2*>(K + size_t(j) * kB * kD) + lane;
     const uint2* vcol = reinterpret_cast<const uint2*>(V + size_t(j) * kB * kD) + lane;
-    uint4 kv[kD / 8];
-    uint2 vv[kB];
+    uint2 kv[kB], vv[kB];
 #pragma unroll
-    for (int c = 0; c < kD / 8; ++c) kv[c] = __ldg(krow + c);
+    for (int u = 0; u < kB; ++u) kv[u] = __ldg(kcol + u * (kD / 4));
 #pragma unroll
     for (int u = 0; u < kB; ++u) vv[u] = __ldg(vcol + u * (kD / 4));
-    float s = 0.f;
+    // partial dot products of token u over this lane's four dimensions
+    float part[kB];
 #pragma unroll
-    for (int c = 0; c < kD / 8; ++c) {
-      const uint32_t w[4] = {kv[c].x, kv[c].y, kv[c].z, kv[c].w};
+    for (int u = 0; u < kB; ++u) {
+      float a = __uint_as_float(kv[u].x << 16) * q4[0];
+      a = fmaf(__uint_as_float(kv[u].x & 0xFFFF0000u), q4[1], a);
+      a = fmaf(__uint_as_float(kv[u].y << 16), q4[2], a);
+      part[u] = fmaf(__uint_as_float(kv[u].y & 0xFFFF0000u), q4[3], a);
+    }
+    // reduce-scatter: at width w each lane keeps the half of the tokens whose
+    // bit w matches its own and adds the partner's copy of that half; after
+    // five rounds lane t holds the full dot product of token t
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s = fmaf(__uint_as_float(w[e] << 16), sq[8 * c + 2 * e], s);
-        s = fmaf(__uint_as_float(w[e] & 0xFFFF0000u), sq[8 * c + 2 * e + 1], s);
+    for (int w = kB / 2; w >= 1; w >>= 1) {
+      const bool upper = (lane & w) != 0;
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const float send = upper ? part[i] : part[i + w];
+        const float keep = upper ? part[i + w] : part[i];
+        part[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
       }
     }
-    s *= scale_log2;
+    const float s = part[0] * scale_log2;
     float mb = s;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));

@@ -10,8 +10,9 @@
 //                  64x64 fp32 SIMT tile per CTA over the lower triangle (the
 //                  contraction is small -- d = 128 -- and selection needs fp32
 //                  accuracy, so no reduced-precision tensor path).
-// decode_scores    scores[b,h,j] = q[b,h] . kbar[b,g,j] * scale; one warp per
-//                  pooled key row serves all G query heads of the group.
+// decode_scores    scores[b,h,j] = q[b,h] . kbar[b,g,j] * scale; a warp takes
+//                  16 pooled key rows (coalesced, all in flight) for all G
+//                  query heads of the group and reduces with a reduce-scatter.
 
 #include <cuda_bf16.h>
 
@@ -117,8 +118,7 @@ __global__ void __launch_bounds__(256) prefill_scores_kernel(const float* __rest
   }
 }
 
-// CTA = (64 pooled rows, kv head g, sequence b); 8 warps.  D = 128.
-constexpr int kDecRows = 64;
+// CTA = (128 pooled rows, kv head g, sequence b); 8 warps of 16 rows.  D = 128.
 constexpr int kMaxGroup = 16;
 
 __global__ void __launch_bounds__(256) decode_scores_kernel(const __nv_bfloat16* __restrict__ q,
@@ -126,7 +126,12 @@ __global__ void __launch_bounds__(256) decode_scores_kernel(const __nv_bfloat16*
                                                             float* __restrict__ scores, int Hq,
                                                             int Hkv, int group, int nb,
                                                             float scale) {
-  constexpr int D = 128;
+  // Each warp scores 16 pooled key rows against every query head of the KV
+  // group.  Lane l holds dimensions [4(l%32).. ) of each row -- one coalesced
+  // 512-byte load per row, 16 rows in flight -- and forms partial dot products;
+  // a reduce-scatter over the 16 lanes of each half-warp (15 shuffles) and one
+  // exchange between the halves leave row r's score in lanes r and r + 16.
+  constexpr int D = 128, R = 16;
   __shared__ float sq[kMaxGroup][D];
   const int b = blockIdx.z, g = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -136,17 +141,33 @@ __global__ void __launch_bounds__(256) decode_scores_kernel(const __nv_bfloat16*
   }
   __syncthreads();
   const float4* kb = reinterpret_cast<const float4*>(kbar + (size_t(b) * Hkv + g) * nb * D);
-  for (int r = warp; r < kDecRows; r += 8) {
-    const int j = blockIdx.x * kDecRows + r;
-    if (j >= nb) break;
-    const float4 kv = __ldg(&kb[size_t(j) * (D / 4) + lane]);
-    for (int hh = 0; hh < group; ++hh) {
-      const float* qq = &sq[hh][lane * 4];
-      float s = kv.x * qq[0] + kv.y * qq[1] + kv.z * qq[2] + kv.w * qq[3];
+  const int j0 = (blockIdx.x * 8 + warp) * R;
+  if (j0 >= nb) return;
+  float4 kv[R];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) scores[(size_t(b) * Hq + g * group + hh) * nb + j] = s * scale;
+  for (int u = 0; u < R; ++u) {
+    const int j = min(j0 + u, nb - 1);        // rows past nb are read (in range) and not stored
+    kv[u] = __ldg(&kb[size_t(j) * (D / 4) + lane]);
+  }
+  for (int hh = 0; hh < group; ++hh) {
+    const float4 q4 = *reinterpret_cast<const float4*>(&sq[hh][lane * 4]);
+    float part[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u)
+      part[u] = fmaf(kv[u].x, q4.x, fmaf(kv[u].y, q4.y, fmaf(kv[u].z, q4.z, kv[u].w * q4.w)));
+#pragma unroll
+    for (int w = R / 2; w >= 1; w >>= 1) {
+      const bool upper = (lane & w) != 0;
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const float send = upper ? part[i] : part[i + w];
+        const float keep = upper ? part[i + w] : part[i];
+        part[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+      }
     }
+    const float sc = part[0] + __shfl_xor_sync(0xffffffffu, part[0], 16);
+    const int j = j0 + (lane & (R - 1));
+    if (lane < R && j < nb) scores[(size_t(b) * Hq + g * group + hh) * nb + j] = sc * scale;
   }
 }
 
@@ -178,7 +199,8 @@ cudaError_t launch_prefill_scores(const float* qbar, const float* kbar, float* s
 cudaError_t launch_decode_scores(const void* q, const float* kbar, float* scores, int Bt, int Hq,
                                  int group, int nb, int d, float scale, cudaStream_t st) {
   if (d != 128 || group > kMaxGroup) return cudaErrorInvalidValue;
-  const dim3 grid(unsigned((nb + kDecRows - 1) / kDecRows), unsigned(Hq / group), unsigned(Bt));
+  // 8 warps x 16 rows per CTA
+  const dim3 grid(unsigned((nb + 127) / 128), unsigned(Hq / group), unsigned(Bt));
   decode_scores_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(q), kbar, scores,
                                              Hq, Hq / group, group, nb, scale);
   return cudaGetLastError();
