@@ -72,6 +72,35 @@ def select_all(scores: np.ndarray, budgets, kmax: int):
     return idx, cnt
 
 
+def group_scores(scores: np.ndarray, group: int) -> np.ndarray:
+    """Group-pooled block scores: the mean over the G query heads of a KV group.
+
+    scores [Hq, nb, nb] (fp64, -inf above the diagonal) -> [Hkv, nb, nb].  With
+    one list per group, one fetched K/V block serves all G heads (Fluxion,
+    group-level access); the mean of the heads' scores is the reading used to
+    rank blocks for the whole group.
+    """
+    Hq, nb, _ = scores.shape
+    return scores.reshape(Hq // group, group, nb, nb).mean(axis=1)
+
+
+def select_all_grouped(scores: np.ndarray, budgets, group: int, kmax: int):
+    """Group-shared selection: for every (g, i) the blocks chosen by select_row
+    on the group-pooled scores with the group's budget, given to each of the
+    group's query heads.  Same output layout as select_all."""
+    Hq, nb, _ = scores.shape
+    gs = group_scores(scores, group)
+    idx = np.full((Hq, nb, kmax), -1, np.int32)
+    cnt = np.zeros((Hq, nb), np.int32)
+    for g in range(Hq // group):
+        for i in range(nb):
+            sel = select_row(gs[g, i], i, budgets[g * group])
+            for h in range(g * group, (g + 1) * group):
+                idx[h, i, :len(sel)] = sel
+                cnt[h, i] = len(sel)
+    return idx, cnt
+
+
 def attend_item(q: np.ndarray, k: np.ndarray, v: np.ndarray, i: int,
                 blocks, B: int):
     """Causal softmax attention of query block i over the listed key blocks.

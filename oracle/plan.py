@@ -81,6 +81,22 @@ def maxmin_shift(k_uniform: int, demand: list[int], k_min: int, nb: int) -> list
     return k
 
 
+def group_budgets(budgets: list[int], group: int) -> list[int]:
+    """Budgets when the G query heads of a KV group share one block list.
+
+    Fluxion models access at the level of the GQA group ("Riepilogo Tecnico:
+    Fluxion", "Intuizioni Chiave": one KV block fetched serves every query head
+    of its group).  Reading: the shared list of a group gets the largest of its
+    heads' budgets, so no head attends fewer blocks than its own budget.
+    Returned per query head (equal within a group).
+    """
+    out = []
+    for h in range(len(budgets)):
+        g = h // group
+        out.append(max(budgets[g * group:(g + 1) * group]))
+    return out
+
+
 def item_costs(budgets: list[int], nb: int) -> list[int]:
     """Cost of work item (h, i), id h*nb+i: the blocks it attends, min(k_h, i+1).
 
