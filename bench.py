@@ -259,6 +259,35 @@ def run_ours(args):
                       "mean_load_blocks": round(inf["total_blocks"] / sms, 1)}
         p.close()
 
+    # ---- GQA-group-shared selection (one block list per KV group), same inputs
+    group_shared = None
+    if not args.no_variants:
+        lg = PrefillLayer(shape, prof["k_uniform"], demand=prof["demand"], k_min=prof["k_min"],
+                          num_workers=sms, schedule=args.schedule, device=dev,
+                          group_shared=True)
+        for _ in range(2):
+            lg(t["q"], t["k"], t["v"], stream=stream)
+        evg = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(5)]
+        for e in evg:
+            e[0].record(stream)
+            lg.score(t["q"], t["k"], stream=stream)
+            e[1].record(stream)
+            lg.select(stream=stream)
+            e[2].record(stream)
+            lg.attend(t["q"], t["k"], t["v"], stream=stream)
+            e[3].record(stream)
+        torch.cuda.synchronize(dev)
+        g_fwd = statistics.mean(e[2].elapsed_time(e[3]) for e in evg)
+        g_flops = _attention_flops(lg.total_blocks, w.block, w.head_dim)
+        group_shared = {
+            "ms_per_layer": round(statistics.mean(e[0].elapsed_time(e[3]) for e in evg), 4),
+            "select_ms": round(statistics.mean(e[1].elapsed_time(e[2]) for e in evg), 4),
+            "forward_ms": round(g_fwd, 4), "selected_blocks": lg.total_blocks,
+            "forward_tflops": round(g_flops / (g_fwd * 1e-3) / 1e12, 1),
+            "budgets": "largest Max-Min budget of each KV group's heads",
+            "device_status": int(lg.dev_status.item())}
+        del lg
+
     # ---- end to end through the public API with host buffers
     out_host = torch.empty((w.num_q_heads, w.seq_len, w.head_dim), dtype=torch.bfloat16,
                            pin_memory=True)
@@ -311,6 +340,7 @@ def run_ours(args):
                      "traffic": _forward_traffic(args.workload),
                      "algorithmic_flops_per_launch": attn_flops},
         "schedules": sched,
+        "group_shared": group_shared,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 5 * args.steps,
@@ -482,6 +512,8 @@ def main():
                          "the others serve small profiling captures)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the group-shared selection variant")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -55,7 +55,7 @@ class _PlanParams(ctypes.Structure):
     _fields_ = [("demand", ctypes.POINTER(ctypes.c_int32)), ("k_uniform", ctypes.c_int32),
                 ("k_min", ctypes.c_int32), ("head_kind", ctypes.POINTER(ctypes.c_uint8)),
                 ("window_blocks", ctypes.c_int32), ("num_workers", ctypes.c_int32),
-                ("schedule", ctypes.c_int32)]
+                ("schedule", ctypes.c_int32), ("group_shared", ctypes.c_int32)]
 
 
 class SparseAttnError(RuntimeError):
@@ -188,7 +188,7 @@ class Plan:
 
 def sparse_attn_plan(shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
                      head_kind=None, window_blocks: int = 0, num_workers: int = 152,
-                     schedule="lpt") -> Plan:
+                     schedule="lpt", group_shared: bool = False) -> Plan:
     if isinstance(schedule, str):
         schedule = SCHEDULES[schedule]
     params = _PlanParams()
@@ -206,6 +206,7 @@ def sparse_attn_plan(shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
     params.window_blocks = window_blocks
     params.num_workers = num_workers
     params.schedule = schedule
+    params.group_shared = 1 if group_shared else 0
     out = ctypes.c_void_p()
     _check(_lib.sparse_attn_plan(ctypes.byref(shape), ctypes.byref(params), ctypes.byref(out)),
            "sparse_attn_plan")

@@ -156,7 +156,10 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const flo
   a.nb = plan->nb;
   a.Hq = shp->num_q_heads;
   a.decode = shp->mode == SA_MODE_DECODE;
-  a.rows = a.decode ? shp->batch * shp->num_q_heads : shp->num_q_heads * plan->nb;
+  a.group = plan->group;
+  a.group_shared = plan->group_shared;
+  a.rows = a.decode ? shp->batch * shp->num_q_heads
+                    : (plan->group_shared ? shp->num_kv_heads : shp->num_q_heads) * plan->nb;
   a.window_blocks = plan->window_blocks;
   return cuda_status(sa_k::launch_select(a, reinterpret_cast<cudaStream_t>(stream)));
 }

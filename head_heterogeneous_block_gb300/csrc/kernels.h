@@ -33,6 +33,8 @@ struct SelectArgs {
   int32_t rows;             // Hq*nb (prefill) or Bt*Hq (decode)
   int32_t decode;           // 0 / 1
   int32_t window_blocks;    // decode streaming heads
+  int32_t group;            // G = Hq / Hkv
+  int32_t group_shared;     // prefill: one row per (KV group, query block)
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 

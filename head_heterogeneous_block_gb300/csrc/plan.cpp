@@ -190,7 +190,17 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* p, sa_plan
     if (shp->mode == SA_MODE_PREFILL) {
       if (p->head_kind) { delete plan; return SA_ERR_INVALID_ARG; }
       if (p->num_workers < 1) { delete plan; return SA_ERR_INVALID_ARG; }
+      if (p->group_shared != 0 && p->group_shared != 1) { delete plan; return SA_ERR_INVALID_ARG; }
       plan->budgets = sa_host::maxmin_shift(p->k_uniform, p->demand, H, p->k_min, nb);
+      plan->group_shared = p->group_shared;
+      if (p->group_shared) {
+        // a shared list gets the largest of its heads' budgets
+        for (int32_t g = 0; g < shp->num_kv_heads; ++g) {
+          int32_t k = 0;
+          for (int32_t x = 0; x < plan->group; ++x) k = std::max(k, plan->budgets[g * plan->group + x]);
+          for (int32_t x = 0; x < plan->group; ++x) plan->budgets[g * plan->group + x] = k;
+        }
+      }
       plan->num_workers = p->num_workers;
       sa_host::build_schedule(plan->budgets, nb, plan->group, p->num_workers, p->schedule,
                               plan->wptr, plan->items, plan->loads);
@@ -203,7 +213,7 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* p, sa_plan
         plan->makespan = std::max(plan->makespan, l);
       }
     } else {
-      if (p->demand) { delete plan; return SA_ERR_INVALID_ARG; }
+      if (p->demand || p->group_shared) { delete plan; return SA_ERR_INVALID_ARG; }
       bool any_streaming = false;
       if (p->head_kind) {
         for (int32_t h = 0; h < H; ++h) {

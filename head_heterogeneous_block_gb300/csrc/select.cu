@@ -1,4 +1,7 @@
-// Select step: per-row top-k_h block selection (one CTA per row).
+// Select step: per-row top-k_h block selection (one CTA per row).  With a
+// group-shared plan a row is (KV group, query block): the candidates are
+// ranked by the sum of the group's heads' scores (the order of their mean)
+// and the list is written for every head of the group.
 //
 // A prefill row (h, i) keeps min(k_h, i+1) blocks: the sink block 0 ("Riepilogo
 // Tecnico: Fluxion", "Intuizioni Chiave" 1), the diagonal block i, and the
@@ -39,19 +42,25 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
 
-  int h, i;
+  int h, i, G = 1;
   const float* srow;
   if (a.decode) {
     h = row % a.Hq;
     i = a.nb - 1;
     srow = a.scores + size_t(row) * a.nb;
+  } else if (a.group_shared) {
+    G = a.group;
+    const int g = row / a.nb;
+    i = row - g * a.nb;
+    h = g * G;                                  // the group's first head
+    srow = a.scores + (size_t(h) * a.nb + i) * a.nb;
   } else {
     h = row / a.nb;
     i = row - h * a.nb;
     srow = a.scores + (size_t(h) * a.nb + i) * a.nb;
   }
+  const size_t head_stride = size_t(a.nb) * a.nb;   // between heads' score rows
   const bool streaming = a.decode && a.kinds[h] == SA_HEAD_STREAMING;
-  int32_t* out = a.idx + size_t(row) * a.kmax;
   const int nwords = (i + 1 + 31) / 32;
   for (int w = tid; w < nwords; w += kThreads) bits[w] = 0u;
   __syncthreads();
@@ -76,7 +85,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
 #pragma unroll
         for (int r = 0; r < kPerThread; ++r) {
           const int j = 1 + tid + r * kThreads;
-          u[r] = (j <= i - 1) ? order_bits(srow[j]) : 0u;
+          float sc = 0.f;
+          if (j <= i - 1)
+            for (int x = 0; x < G; ++x) sc += srow[x * head_stride + j];
+          u[r] = (j <= i - 1) ? order_bits(sc) : 0u;
         }
         uint32_t prefix = 0, mask = 0, need = uint32_t(rest), eq_total = 0;
         for (int shift = 24; shift >= 0; shift -= 8) {
@@ -157,19 +169,25 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
   }
   __syncthreads();
 
-  // Emit ascending block indices, then pad with -1 (warp 0).
+  // Emit ascending block indices, then pad with -1 (warp 0), into the row of
+  // every head that shares the list.
   if (warp == 0) {
+    const size_t orow = a.decode ? size_t(row) : size_t(h) * a.nb + i;
     int written = 0;
     for (int base = 0; base <= i; base += 32) {
       const int j = base + lane;
       const bool on = (j <= i) && ((bits[j >> 5] >> (j & 31)) & 1u);
       const uint32_t m = __ballot_sync(0xffffffffu, on);
       const int pos = written + __popc(m & ((1u << lane) - 1u));
-      if (on && pos < a.kmax) out[pos] = j;
+      if (on && pos < a.kmax)
+        for (int x = 0; x < G; ++x) a.idx[(orow + size_t(x) * a.nb) * a.kmax + pos] = j;
       written += __popc(m);
     }
-    for (int t = written + lane; t < a.kmax; t += 32) out[t] = -1;
-    if (lane == 0) a.cnt[row] = min(written, a.kmax);
+    for (int x = 0; x < G; ++x) {
+      int32_t* out = a.idx + (orow + size_t(x) * a.nb) * a.kmax;
+      for (int t = written + lane; t < a.kmax; t += 32) out[t] = -1;
+      if (lane == 0) a.cnt[orow + size_t(x) * a.nb] = min(written, a.kmax);
+    }
   }
 }
 

@@ -117,6 +117,13 @@ typedef struct sa_plan_params {
   int32_t num_workers;      /* prefill: persistent workers W >= 1; one CTA
                                runs one worker                              */
   int32_t schedule;         /* SA_SCHED_*                                   */
+  int32_t group_shared;     /* prefill: 0 = one block list per query head;
+                               1 = one list per KV group (GQA-group-shared
+                               selection): the G heads of a group share the
+                               blocks chosen on their summed scores, with the
+                               largest of their budgets.  Must be 0 for decode.
+                               (Fluxion, "Intuizioni Chiave": group-level KV
+                               access.)                                      */
 } sa_plan_params;
 
 typedef struct sa_plan sa_plan;
@@ -231,6 +238,10 @@ sa_status sparse_attn_score_noalloc(const sa_shape* shp, const void* q, const vo
  * then the highest-scoring of 1..i-1, ties to the lower index.  For decode
  * retrieval heads the row is i = nb-1 with k_h = k_uniform; streaming heads
  * get block 0 and the last window_blocks blocks.
+ * Group-shared plans (sa_plan_params.group_shared = 1, prefill): one list per
+ * (KV group g, row i), chosen as above on the sum over the group's G heads of
+ * their scores (the order of their mean) with the group's budget, and written
+ * to the rows of all G heads.
  * Outputs: idx [rows][kmax] int32, each row ascending and padded with -1;
  * cnt [rows] int32; rows = Hq*nb (prefill, row h*nb+i) or Bt*Hq (decode,
  * row b*Hq+h).  kmax must be >= the plan's kmax (sparse_attn_plan_info).

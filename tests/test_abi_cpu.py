@@ -207,3 +207,34 @@ def test_device_calls_reject_bad_arguments_before_launch(sa):
     n = ctypes.c_size_t()
     assert lib.sparse_attn_score_workspace_size(s, ctypes.byref(n)) == 0
     assert n.value == (8 + 2) * 64 * 64 * 4
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_group_shared_plan_matches_oracle(sa, seed):
+    # one list per KV group: every head of a group gets the group's largest
+    # Max-Min budget, and the schedule is built on those budgets
+    r = random.Random(100 + seed)
+    Hkv = r.choice([1, 2, 4])
+    G = r.choice([1, 2, 4, 7])
+    Hq = Hkv * G
+    B, nb = 64, r.randint(2, 40)
+    W = r.randint(1, 20)
+    policy = r.choice(["lpt", "lpt_grouped", "head_order"])
+    k_u = r.randint(2, nb)
+    demand = [r.randint(0, nb + 3) for _ in range(Hq)]
+    from oracle import plan as op
+    shape = sa.Shape.prefill(nb * B, B, Hq, Hkv, 64)
+    got = sa.sparse_attn_plan(shape, k_u, demand=demand, num_workers=W, schedule=policy,
+                              group_shared=True).get()
+    k = op.group_budgets(op.maxmin_shift(k_u, demand, 2, nb), G)
+    wptr, items, loads = op.schedule(k, nb, W, policy, G)
+    assert got["budgets"].tolist() == k
+    assert got["wptr"].tolist() == wptr
+    assert got["items"].tolist() == items
+    assert got["loads"].tolist() == loads
+
+
+def test_group_shared_is_prefill_only(sa):
+    shape = sa.Shape.decode(4096, 32, 8, 2, 128, 2)
+    with pytest.raises(sa.SparseAttnError):
+        sa.sparse_attn_plan(shape, 8, num_workers=1, group_shared=True)

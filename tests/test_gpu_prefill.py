@@ -186,3 +186,66 @@ def test_prefill_full_size(env, number):
     items = P.sample_items(r["budgets"], w.nb, 16 if number == 4 else 64, seed=number)
     P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group,
                       bf16_out=True)
+
+
+def _check_group_shared(r, x, w, args_budgets):
+    """Group-shared selection: one list per (KV group, row), equal across the
+    group's heads, matching the oracle's selection on the group-pooled scores;
+    attention checked on the GPU's own lists."""
+    from oracle import attention as oa
+    from oracle import plan as op
+    from tests import _parity as P
+    G, nb = w.group, w.nb
+    assert r["budgets"] == op.group_budgets(args_budgets, G)
+    idx, cnt = r["idx"], r["cnt"]
+    for g in range(w.num_kv_heads):
+        for hh in range(1, G):
+            assert np.array_equal(idx[g * G], idx[g * G + hh])
+            assert np.array_equal(cnt[g * G], cnt[g * G + hh])
+    ref_scores = _oracle_scores(w, x)
+    P.check_scores(r["scores"], ref_scores)
+    per_head = np.repeat(oa.group_scores(ref_scores, G), G, axis=0)
+    P.check_selection(idx, cnt, per_head, r["budgets"])
+    return ref_scores
+
+
+@pytest.mark.parametrize("number,S,Hq,Hkv", [(1, 4096, 8, 2), (2, 4096, 8, 2), (2, 2432, 8, 8),
+                                             (2, 8192, 16, 4)])
+def test_prefill_group_shared_parity(env, number, S, Hq, Hkv):
+    sa, torch = env
+    from oracle import plan as op
+    from tests import _parity as P
+    from workloads import generate, scaled, workload
+    w = scaled(workload(number), S, Hq, Hkv)
+    x = generate.prefill_inputs(w)
+    nb = w.nb
+    k_u = max(2, op.budget_for_density(w.target_density, nb))
+    rng = np.random.default_rng(S + 7)
+    demand = rng.integers(1, nb, Hq).tolist()
+    r = _run(sa, torch, w, x, {"k_uniform": k_u, "demand": demand, "group_shared": True},
+             workers=16)
+    assert r["status"] == 0
+    _check_group_shared(r, x, w, op.maxmin_shift(k_u, demand, 2, nb))
+    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, range(Hq * nb),
+                      w.group)
+
+
+def test_prefill_group_shared_full_size(env):
+    """The 128K Llama-3.1-8B workload with one list per KV group, in the
+    bench's launch configuration; selection checked on every row, attention on
+    sampled items."""
+    sa, torch = env
+    from tests import _parity as P
+    from workloads import generate, workload
+    w = workload(3)
+    prof = json.load(open(os.path.join(ROOT, "workloads", "demands.json")))["3"]
+    x = generate.prefill_inputs(w)
+    W = torch.cuda.get_device_properties(0).multi_processor_count
+    r = _run(sa, torch, w, x, {"k_uniform": prof["k_uniform"], "demand": prof["demand"],
+                               "group_shared": True},
+             schedule="lpt_grouped", workers=W, out_dtype="bfloat16")
+    assert r["status"] == 0
+    _check_group_shared(r, x, w, prof["budgets_maxmin"])
+    items = P.sample_items(r["budgets"], w.nb, 32, seed=33)
+    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group,
+                      bf16_out=True)
