@@ -288,6 +288,29 @@ def run_ours(args):
             "device_status": int(lg.dev_status.item())}
         del lg
 
+    # ---- output-aware demands (calibration signal only; same kernels)
+    output_aware = None
+    if not args.no_variants and "output_aware" in prof:
+        oa = prof["output_aware"]
+        lo = PrefillLayer(shape, prof["k_uniform"], demand=oa["demand"], k_min=prof["k_min"],
+                          num_workers=sms, schedule=args.schedule, device=dev)
+        for _ in range(2):
+            lo(t["q"], t["k"], t["v"], stream=stream)
+        evo = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(5)]
+        for e in evo:
+            e[0].record(stream)
+            lo(t["q"], t["k"], t["v"], stream=stream)
+            e[1].record(stream)
+        torch.cuda.synchronize(dev)
+        o_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evo)
+        output_aware = {
+            "ms_per_layer": round(o_ms, 4), "selected_blocks": lo.total_blocks,
+            "makespan_blocks": lo.plan.info()["makespan"],
+            "demand_range": [min(oa["demand"]), max(oa["demand"])],
+            "budget_range": [min(oa["budgets_maxmin"]), max(oa["budgets_maxmin"])],
+            "device_status": int(lo.dev_status.item())}
+        del lo
+
     # ---- end to end through the public API with host buffers
     out_host = torch.empty((w.num_q_heads, w.seq_len, w.head_dim), dtype=torch.bfloat16,
                            pin_memory=True)
@@ -341,6 +364,7 @@ def run_ours(args):
                      "algorithmic_flops_per_launch": attn_flops},
         "schedules": sched,
         "group_shared": group_shared,
+        "output_aware_demands": output_aware,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 5 * args.steps,
@@ -513,7 +537,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the group-shared selection variant")
+                    help="skip the group-shared selection and output-aware demand variants")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

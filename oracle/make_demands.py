@@ -11,7 +11,14 @@ Workloads 1-3 calibrate on a draw with their own heads (scales s_h) and a
 separate seed at min(S, 8192) tokens.  Workload 4 draws its head densities
 from a lognormal (its recipe), clamped to [density(2), 1].
 
+With --output-aware it adds, for the calibrated workloads, the output-aware
+demand signal (Fluxion, "Intuizioni Chiave" 1): per head, the fraction of
+causal blocks needed to keep the sparse output within a tolerance of the full
+output, the tolerance scaled by the head's relative output norm.  The result
+goes under "output_aware" beside the mass-based profile, which is left as is.
+
 Usage:  python -m oracle.make_demands [--out workloads/demands.json]
+        python -m oracle.make_demands --output-aware [--workloads 1,2,3]
 """
 from __future__ import annotations
 
@@ -33,6 +40,7 @@ from workloads import WORKLOADS, generate  # noqa: E402
 
 K_MIN = 2
 COVER = 0.9
+EPS = 0.1          # output-aware: relative output deviation allowed for a mean head
 
 
 def _head_density(args):
@@ -43,6 +51,48 @@ def _head_density(args):
     q = generate.bf16_to_f64(x["q"][0])
     k = generate.bf16_to_f64(x["k"][0])
     return calib.head_density(q, k, w.block, COVER)
+
+
+def _calib_qkv(number, h):
+    w = WORKLOADS[number]
+    x = generate.prefill_inputs(w, tensors="qkv", heads=[h], kv_heads=[h // w.group],
+                                seed=w.calib_seed, seq_len=w.calib_len)
+    return (generate.bf16_to_f64(x["q"][0]), generate.bf16_to_f64(x["k"][0]),
+            generate.bf16_to_f64(x["v"][0]))
+
+
+def _head_norm(args):
+    number, h = args
+    q, k, v = _calib_qkv(number, h)
+    return calib.head_output_norm(q, k, v, WORKLOADS[number].block)
+
+
+def _head_output_density(args):
+    number, h, eps = args
+    q, k, v = _calib_qkv(number, h)
+    return calib.head_output_density(q, k, v, WORKLOADS[number].block, eps)
+
+
+def profile_output_aware(number: int, pool) -> dict:
+    w = WORKLOADS[number]
+    nb = w.nb
+    k_u = plan.budget_for_density(w.target_density, nb)
+    heads = range(w.num_q_heads)
+    norms = list(pool.map(_head_norm, [(number, h) for h in heads]))
+    tol = calib.output_aware_tolerances(norms, EPS)
+    rho = list(pool.map(_head_output_density, [(number, h, tol[h]) for h in heads]))
+    demand = [calib.demand_for_density(r, nb) for r in rho]
+    budgets = plan.maxmin_shift(k_u, demand, K_MIN, nb)
+    return {
+        "source": (f"output deviation <= {EPS} x (mean head output norm / head's) on the "
+                   f"calibration draw (seed {w.calib_seed}, {w.calib_len} tokens)"),
+        "eps": EPS, "output_norm": [round(float(x), 12) for x in norms],
+        "tolerance": [round(float(x), 12) for x in tol],
+        "density": [round(float(r), 12) for r in rho], "demand": demand,
+        "budgets_maxmin": budgets,
+        "mean_density_after_shift": sum(plan.kept_blocks(k, nb) for k in budgets)
+        / (w.num_q_heads * plan.causal_blocks(nb)),
+    }
 
 
 def profile(number: int, pool=None) -> dict:
@@ -78,6 +128,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=os.path.join(ROOT, "workloads", "demands.json"))
     ap.add_argument("--workloads", default="1,2,3,4")
+    ap.add_argument("--output-aware", action="store_true")
     args = ap.parse_args()
     out = {}
     if os.path.exists(args.out):
@@ -87,7 +138,18 @@ def main():
     with ctx.Pool(max(1, os.cpu_count() or 1)) as pool:
         for n in [int(x) for x in args.workloads.split(",")]:
             t = time.time()
+            if args.output_aware:
+                if WORKLOADS[n].demand_source != "coverage":
+                    continue
+                out[str(n)]["output_aware"] = profile_output_aware(n, pool)
+                oa = out[str(n)]["output_aware"]
+                print(f"workload {n} output-aware: {time.time() - t:.1f}s demand "
+                      f"{min(oa['demand'])}..{max(oa['demand'])}", flush=True)
+                continue
+            prev = out.get(str(n), {}).get("output_aware")
             out[str(n)] = profile(n, pool)
+            if prev is not None:
+                out[str(n)]["output_aware"] = prev
             print(f"workload {n}: {time.time() - t:.1f}s k_u={out[str(n)]['k_uniform']} "
                   f"demand range {min(out[str(n)]['demand'])}..{max(out[str(n)]['demand'])}",
                   flush=True)

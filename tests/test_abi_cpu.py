@@ -238,3 +238,23 @@ def test_group_shared_is_prefill_only(sa):
     shape = sa.Shape.decode(4096, 32, 8, 2, 128, 2)
     with pytest.raises(sa.SparseAttnError):
         sa.sparse_attn_plan(shape, 8, num_workers=1, group_shared=True)
+
+
+@pytest.mark.parametrize("number", [1, 2, 3])
+def test_output_aware_profile_plans_match_oracle(sa, number):
+    # the stored output-aware demands shift to the stored budgets under the
+    # oracle's Max-Min, and the library's plan gives the same budgets
+    from oracle import plan as op
+    from workloads import workload
+    prof = json.load(open(os.path.join(ROOT, "workloads", "demands.json")))[str(number)]
+    if "output_aware" not in prof:
+        pytest.skip("no output-aware profile stored")
+    oa = prof["output_aware"]
+    w = workload(number)
+    k = op.maxmin_shift(prof["k_uniform"], oa["demand"], prof["k_min"], w.nb)
+    assert k == oa["budgets_maxmin"]
+    assert sum(k) == prof["k_uniform"] * w.num_q_heads
+    shape = sa.Shape.prefill(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim)
+    got = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=oa["demand"],
+                              k_min=prof["k_min"], num_workers=152).get()
+    assert got["budgets"].tolist() == k
