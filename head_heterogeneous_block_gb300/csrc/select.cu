@@ -82,13 +82,23 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
       }
       if (rest > 0) {
         uint32_t u[kPerThread];
+        if (G == 1) {
+          // all of a thread's candidate loads in flight together
 #pragma unroll
-        for (int r = 0; r < kPerThread; ++r) {
-          const int j = 1 + tid + r * kThreads;
-          float sc = 0.f;
-          if (j <= i - 1)
-            for (int x = 0; x < G; ++x) sc += srow[x * head_stride + j];
-          u[r] = (j <= i - 1) ? order_bits(sc) : 0u;
+          for (int r = 0; r < kPerThread; ++r) {
+            const int j = 1 + tid + r * kThreads;
+            u[r] = (j <= i - 1) ? order_bits(srow[j]) : 0u;
+          }
+        } else {
+          // group-shared rows rank by the sum of the group's heads' scores
+#pragma unroll
+          for (int r = 0; r < kPerThread; ++r) {
+            const int j = 1 + tid + r * kThreads;
+            float sc = 0.f;
+            if (j <= i - 1)
+              for (int x = 0; x < G; ++x) sc += srow[x * head_stride + j];
+            u[r] = (j <= i - 1) ? order_bits(sc) : 0u;
+          }
         }
         uint32_t prefix = 0, mask = 0, need = uint32_t(rest), eq_total = 0;
         for (int shift = 24; shift >= 0; shift -= 8) {
@@ -173,19 +183,24 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
   // every head that shares the list.
   if (warp == 0) {
     const size_t orow = a.decode ? size_t(row) : size_t(h) * a.nb + i;
+    int32_t* out = a.idx + orow * a.kmax;
     int written = 0;
     for (int base = 0; base <= i; base += 32) {
       const int j = base + lane;
       const bool on = (j <= i) && ((bits[j >> 5] >> (j & 31)) & 1u);
       const uint32_t m = __ballot_sync(0xffffffffu, on);
       const int pos = written + __popc(m & ((1u << lane) - 1u));
-      if (on && pos < a.kmax)
-        for (int x = 0; x < G; ++x) a.idx[(orow + size_t(x) * a.nb) * a.kmax + pos] = j;
+      if (on && pos < a.kmax) out[pos] = j;
       written += __popc(m);
     }
-    for (int x = 0; x < G; ++x) {
-      int32_t* out = a.idx + (orow + size_t(x) * a.nb) * a.kmax;
-      for (int t = written + lane; t < a.kmax; t += 32) out[t] = -1;
+    for (int t = written + lane; t < a.kmax; t += 32) out[t] = -1;
+    if (lane == 0) a.cnt[orow] = min(written, a.kmax);
+    // the other heads of a group-shared row get copies of the list (written
+    // above by the warp's lanes: order those writes before the reads)
+    __syncwarp();
+    for (int x = 1; x < G; ++x) {
+      int32_t* dst = a.idx + (orow + size_t(x) * a.nb) * a.kmax;
+      for (int t = lane; t < a.kmax; t += 32) dst[t] = out[t];
       if (lane == 0) a.cnt[orow + size_t(x) * a.nb] = min(written, a.kmax);
     }
   }
