@@ -72,6 +72,48 @@ def select_all(scores: np.ndarray, budgets, kmax: int):
     return idx, cnt
 
 
+def block_probabilities(scores_row: np.ndarray, i: int) -> np.ndarray:
+    """Softmax over the causal blocks j <= i of a row's pooled scores: the
+    row's estimate of how its attention mass falls on each block (fp64)."""
+    s = scores_row[:i + 1].astype(np.float64)
+    e = np.exp(s - s.max())
+    return e / e.sum()
+
+
+def select_row_topp(scores_row: np.ndarray, i: int, p: float) -> list[int]:
+    """Top-p block selection, the adaptive alternative the S-HPLB pages compare
+    against (Italian summary, "Sparsità Eterogenea"; Chinese summary, "Top-p
+    方法的局限"): the number of blocks a row keeps depends on its data.
+
+    Reading: keep the sink block 0 and the diagonal block i, then blocks of
+    1..i-1 by probability (score) descending, ties to the lower index, until
+    the kept blocks' cumulative probability reaches p.  Ascending order.
+    """
+    prob = block_probabilities(scores_row, i)
+    chosen = sorted({0, i})
+    acc = float(sum(prob[j] for j in chosen))
+    rest = np.arange(1, i)
+    for j in rest[np.lexsort((rest, -prob[rest]))]:
+        if acc >= p:
+            break
+        chosen.append(int(j))
+        acc += float(prob[j])
+    return sorted(chosen)
+
+
+def select_all_topp(scores: np.ndarray, p: float, kmax: int):
+    """select_row_topp for every (h, i); same layout as select_all."""
+    Hq, nb, _ = scores.shape
+    idx = np.full((Hq, nb, kmax), -1, np.int32)
+    cnt = np.zeros((Hq, nb), np.int32)
+    for h in range(Hq):
+        for i in range(nb):
+            sel = select_row_topp(scores[h, i], i, p)
+            idx[h, i, :len(sel)] = sel
+            cnt[h, i] = len(sel)
+    return idx, cnt
+
+
 def group_scores(scores: np.ndarray, group: int) -> np.ndarray:
     """Group-pooled block scores: the mean over the G query heads of a KV group.
 

@@ -165,5 +165,19 @@ def schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int 
     return wptr, items, loads
 
 
+def schedule_from_costs(costs: list[int], workers: int):
+    """LPT over given item costs (e.g. the block counts a data-dependent
+    selection produced): items by cost descending, ties lower id, each to the
+    least-loaded worker.  Returns (wptr, items, loads) as schedule()."""
+    order = sorted(range(len(costs)), key=lambda x: (-costs[x], x))
+    lists, loads = lpt_assign(order, costs, workers)
+    wptr = [0]
+    items = []
+    for lst in lists:
+        items.extend(lst)
+        wptr.append(len(items))
+    return wptr, items, loads
+
+
 def makespan(loads: list[int]) -> int:
     return max(loads) if loads else 0

@@ -249,3 +249,26 @@ def test_prefill_group_shared_full_size(env):
     items = P.sample_items(r["budgets"], w.nb, 32, seed=33)
     P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group,
                       bf16_out=True)
+
+
+def test_prefill_largest_rows(env):
+    """d 64 / B 64 at 131072 tokens: rows of nb = 2048 blocks, the largest the
+    select kernel takes; selection checked on every row, attention sampled."""
+    sa, torch = env
+    from oracle import plan as op
+    from tests import _parity as P
+    from workloads import generate, scaled, workload
+    w = scaled(workload(1), 131072, 4, 1)
+    assert w.nb == 2048
+    x = generate.prefill_inputs(w)
+    k_u = op.budget_for_density(0.02, w.nb)
+    rng = np.random.default_rng(2048)
+    args = {"k_uniform": k_u, "demand": rng.integers(2, 4 * k_u, w.num_q_heads).tolist()}
+    r = _run(sa, torch, w, x, args, workers=152, out_dtype="bfloat16")
+    assert r["status"] == 0
+    ref_scores = _oracle_scores(w, x)
+    P.check_scores(r["scores"], ref_scores)
+    P.check_selection(r["idx"], r["cnt"], ref_scores, r["budgets"])
+    items = P.sample_items(r["budgets"], w.nb, 24, seed=2048)
+    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group,
+                      bf16_out=True)
