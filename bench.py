@@ -311,6 +311,41 @@ def run_ours(args):
             "device_status": int(lo.dev_status.item())}
         del lo
 
+    # ---- top-p selection (data-dependent counts) at the plan's mean density:
+    # a static head-order schedule against the LPT rebuilt on the GPU
+    topp = None
+    if not args.no_variants:
+        p_thr = layer.total_blocks / (w.num_q_heads * w.nb * (w.nb + 1) / 2)
+        tidx = torch.empty(w.num_q_heads * w.nb * w.nb, dtype=torch.int32, device=dev)
+        tcnt = torch.empty(w.num_q_heads * w.nb, dtype=torch.int32, device=dev)
+        res = {}
+        for mode in ("head_order_static", "lpt_rebuilt"):
+            pl = sa.sparse_attn_plan(shape, prof["k_uniform"], k_min=prof["k_min"],
+                                     num_workers=sms,
+                                     schedule="head_order" if mode == "head_order_static"
+                                     else "lpt")
+            pl.upload()
+            ev_t = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            for rep in range(3):
+                ev_t[0].record(stream)
+                sa.sparse_attn_select_topp(shape, pl, layer.scores, p_thr, tidx, tcnt, w.nb,
+                                           stream=stream)
+                ev_t[1].record(stream)
+                if mode == "lpt_rebuilt":
+                    pl.rebuild(tcnt, stream=stream)
+                ev_t[2].record(stream)
+                sa.sparse_attn_forward(shape, pl, t["q"], t["k"], t["v"], tidx, tcnt, w.nb,
+                                       layer.out, None, layer.dev_status, stream)
+                ev_t[3].record(stream)
+            torch.cuda.synchronize(dev)
+            res[mode] = {"select_ms": round(ev_t[0].elapsed_time(ev_t[1]), 4),
+                         "rebuild_ms": round(ev_t[1].elapsed_time(ev_t[2]), 4),
+                         "forward_ms": round(ev_t[2].elapsed_time(ev_t[3]), 4)}
+            pl.close()
+        topp = {"p": round(p_thr, 5), "selected_blocks": int(tcnt.sum().item()),
+                "device_status": int(layer.dev_status.item()), **res}
+        del tidx, tcnt
+
     # ---- end to end through the public API with host buffers
     out_host = torch.empty((w.num_q_heads, w.seq_len, w.head_dim), dtype=torch.bfloat16,
                            pin_memory=True)
@@ -365,6 +400,7 @@ def run_ours(args):
         "schedules": sched,
         "group_shared": group_shared,
         "output_aware_demands": output_aware,
+        "topp": topp,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 5 * args.steps,
@@ -537,7 +573,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the group-shared selection and output-aware demand variants")
+                    help="skip the group-shared, output-aware and top-p variants")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -92,6 +92,10 @@ def _load():
         "sparse_attn_forward": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P, P, I32,
                                                P, I32, P, P, P]),
         "sparse_attn_pool_kcache": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P]),
+        "sparse_attn_select_topp": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, ctypes.c_float,
+                                                   P, P, I32, P]),
+        "sparse_attn_plan_rebuild": (ctypes.c_int, [P, P, P]),
+        "sparse_attn_plan_device_schedule": (ctypes.c_int, [P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -174,6 +178,17 @@ class Plan:
     def upload(self, stream=None):
         _check(_lib.sparse_attn_plan_upload(self._h, _stream(stream)), "sparse_attn_plan_upload")
 
+    def rebuild(self, cnt, stream=None):
+        """LPT schedule rebuilt on the GPU from device block counts cnt [Hq*nb]."""
+        _check(_lib.sparse_attn_plan_rebuild(self._h, _ptr(cnt), _stream(stream)),
+               "sparse_attn_plan_rebuild")
+
+    def device_schedule(self, wptr, items, stream=None):
+        """Copy the device schedule (wptr [W+1], items [N]) into the given buffers."""
+        _check(_lib.sparse_attn_plan_device_schedule(self._h, _ptr(wptr), _ptr(items),
+                                                     _stream(stream)),
+               "sparse_attn_plan_device_schedule")
+
     def close(self):
         if self._h is not None and self._h.value:
             _lib.sparse_attn_plan_destroy(self._h)
@@ -231,6 +246,13 @@ def sparse_attn_score(shape: Shape, q, k, scores, ws=None, ws_bytes: int | None 
 def sparse_attn_select(shape: Shape, plan: Plan, scores, idx, cnt, kmax: int, stream=None):
     _check(_lib.sparse_attn_select(ctypes.byref(shape), plan.handle, _ptr(scores), _ptr(idx),
                                    _ptr(cnt), kmax, _stream(stream)), "sparse_attn_select")
+
+
+def sparse_attn_select_topp(shape: Shape, plan: Plan, scores, p: float, idx, cnt, kmax: int,
+                            stream=None):
+    _check(_lib.sparse_attn_select_topp(ctypes.byref(shape), plan.handle, _ptr(scores),
+                                        float(p), _ptr(idx), _ptr(cnt), kmax, _stream(stream)),
+           "sparse_attn_select_topp")
 
 
 def _out_dtype(o, o_dtype):

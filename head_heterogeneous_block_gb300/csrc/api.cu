@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -31,8 +32,10 @@ void free_device(sa_plan* p) {
     cudaFree(p->d_kinds);
     cudaFree(p->d_wptr);
     cudaFree(p->d_items);
+    cudaFree(p->d_scratch);
     if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
   }
+  p->d_scratch = nullptr;
   p->d_budgets = nullptr;
   p->d_kinds = nullptr;
   p->d_wptr = nullptr;
@@ -162,6 +165,62 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const flo
                     : (plan->group_shared ? shp->num_kv_heads : shp->num_q_heads) * plan->nb;
   a.window_blocks = plan->window_blocks;
   return cuda_status(sa_k::launch_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_select_topp(const sa_shape* shp, const sa_plan* plan, const float* scores,
+                                  float p, int32_t* idx, int32_t* cnt, int32_t kmax,
+                                  sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!plan || !scores || !idx || !cnt || !(p == p)) return SA_ERR_INVALID_ARG;
+  if (shp->mode != SA_MODE_PREFILL) return SA_ERR_INVALID_ARG;
+  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+  if (kmax < plan->nb) return SA_ERR_SHAPE;
+  if (plan->nb > 2048) return SA_ERR_UNSUPPORTED;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  sa_k::TopPArgs a;
+  a.scores = scores;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.kmax = kmax;
+  a.nb = plan->nb;
+  a.rows = shp->num_q_heads * plan->nb;
+  a.p = p;
+  return cuda_status(sa_k::launch_select_topp(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_plan_rebuild(sa_plan* plan, const int32_t* cnt, sa_stream_t stream) {
+  if (!plan || !cnt) return SA_ERR_INVALID_ARG;
+  if (plan->shape.mode != SA_MODE_PREFILL) return SA_ERR_INVALID_ARG;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  if (plan->num_workers > 256 || plan->nb > 2048) return SA_ERR_UNSUPPORTED;
+  if (plan->items.size() > (size_t(1) << 19)) return SA_ERR_UNSUPPORTED;
+  const int32_t n = int32_t(plan->items.size());
+  if (!plan->d_scratch) {
+    cudaError_t e = cudaMalloc(&plan->d_scratch, size_t(2) * std::max(n, 1) * sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  sa_k::RebuildArgs a;
+  a.cnt = cnt;
+  a.wptr = plan->d_wptr;
+  a.items = plan->d_items;
+  a.scratch = plan->d_scratch;
+  a.num_items = n;
+  a.num_workers = plan->num_workers;
+  return cuda_status(sa_k::launch_lpt_rebuild(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_plan_device_schedule(const sa_plan* plan, int32_t* wptr, int32_t* items,
+                                           sa_stream_t stream) {
+  if (!plan || !wptr || !items) return SA_ERR_INVALID_ARG;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(wptr, plan->d_wptr, plan->wptr.size() * sizeof(int32_t),
+                                  cudaMemcpyDefault, st);
+  if (e == cudaSuccess && !plan->items.empty())
+    e = cudaMemcpyAsync(items, plan->d_items, plan->items.size() * sizeof(int32_t),
+                        cudaMemcpyDefault, st);
+  return cuda_status(e);
 }
 
 sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const void* q,

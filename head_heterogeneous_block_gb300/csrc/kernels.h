@@ -38,6 +38,26 @@ struct SelectArgs {
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
+struct TopPArgs {           // prefill rows only
+  const float* scores;
+  int32_t* idx;
+  int32_t* cnt;
+  int32_t kmax;             // >= nb
+  int32_t nb;
+  int32_t rows;             // Hq*nb
+  float p;
+};
+cudaError_t launch_select_topp(const TopPArgs& a, cudaStream_t st);
+
+struct RebuildArgs {
+  const int32_t* cnt;       // [N] blocks per item (the item's cost)
+  int32_t* wptr;            // [W+1] out
+  int32_t* items;           // [N] out
+  int32_t* scratch;         // [2N]
+  int32_t num_items, num_workers;
+};
+cudaError_t launch_lpt_rebuild(const RebuildArgs& a, cudaStream_t st);
+
 struct PrefillArgs {
   const void* q;
   const void* k;

@@ -206,9 +206,214 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
   }
 }
 
+// Top-p selection of prefill row (h, i): block probabilities are the
+// softmax of the row's pooled scores over j <= i; the row keeps blocks 0 and
+// i, then blocks of 1..i-1 by score (ties to the lower index) until the kept
+// probability reaches p.  Probabilities are summed in 64-bit fixed point (units
+// of 2^-32 of the row's total), so the result does not depend on the order of
+// the additions.  The threshold is found as in select_kernel, with histograms
+// of probability mass next to the counts.
+__global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a) {
+  __shared__ uint32_t bits[kMaxWords];
+  __shared__ unsigned long long hmass[256];
+  __shared__ uint32_t hcount[256];
+  __shared__ float redf[kThreads / 32];
+  __shared__ unsigned long long ctl_m[2];
+  __shared__ uint32_t ctl[2];
+  __shared__ uint32_t wsum[kThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
+  const int h = row / a.nb, i = row - h * a.nb;
+  const float* srow = a.scores + (size_t(h) * a.nb + i) * a.nb;
+  const int nwords = (i + 1 + 31) / 32;
+  for (int w = tid; w < nwords; w += kThreads) bits[w] = 0u;
+
+  // scores of blocks j = tid + r*kThreads (all j <= i, mandatory ones included)
+  float sv[kPerThread];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    const int j = tid + r * kThreads;
+    sv[r] = (j <= i) ? srow[j] : -INFINITY;
+    mx = fmaxf(mx, sv[r]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) redf[warp] = mx;
+  __syncthreads();
+  mx = redf[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) mx = fmaxf(mx, redf[w]);
+  __syncthreads();
+  float e[kPerThread], tot = 0.f;
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    const int j = tid + r * kThreads;
+    e[r] = (j <= i) ? exp2f((sv[r] - mx) * 1.4426950408889634f) : 0.f;
+    tot += e[r];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if (lane == 0) redf[warp] = tot;
+  __syncthreads();
+  tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) tot += redf[w];   // same order in every thread
+  const float scale = 4294967296.0f / tot;                  // 2^32 / total
+  // fixed-point masses; the mandatory blocks' mass is taken first
+  unsigned long long q[kPerThread];
+  unsigned long long mand = 0;
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    const int j = tid + r * kThreads;
+    q[r] = (j <= i) ? (unsigned long long)(e[r] * scale) : 0ull;
+    if (j == 0 || j == i) mand += q[r];
+  }
+  if (tid == 0) ctl_m[0] = 0ull;
+  __syncthreads();
+  if (mand) atomicAdd(&ctl_m[0], mand);
+  if (tid == 0) {
+    atomicOr(&bits[0], 1u);
+    atomicOr(&bits[i >> 5], 1u << (i & 31));
+  }
+  __syncthreads();
+  const double pd = double(a.p) * 4294967296.0;
+  const unsigned long long goal = pd >= 1.8e19 ? ~0ull : (unsigned long long)ceil(pd);
+  const unsigned long long have = ctl_m[0];
+  __syncthreads();
+  if (i >= 2 && goal > have) {
+    unsigned long long need = goal - have;           // mass wanted from blocks 1..i-1
+    uint32_t u[kPerThread];
+    unsigned long long cand = 0;
+#pragma unroll
+    for (int r = 0; r < kPerThread; ++r) {
+      const int j = tid + r * kThreads;
+      const bool c = j >= 1 && j <= i - 1;
+      u[r] = c ? order_bits(sv[r]) : 0u;
+      if (c) cand += q[r];
+    }
+    if (tid == 0) ctl_m[1] = 0ull;
+    __syncthreads();
+    atomicAdd(&ctl_m[1], cand);
+    __syncthreads();
+    if (ctl_m[1] <= need) {
+      // even every candidate does not reach p: keep them all
+      for (int j = 1 + tid; j <= i - 1; j += kThreads) atomicOr(&bits[j >> 5], 1u << (j & 31));
+    } else {
+      uint32_t prefix = 0, mask = 0, eq_count = 0;
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += kThreads) {
+          hmass[b] = 0ull;
+          hcount[b] = 0u;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kPerThread; ++r) {
+          const int j = tid + r * kThreads;
+          if (j >= 1 && j <= i - 1 && (u[r] & mask) == prefix) {
+            const uint32_t b = (u[r] >> shift) & 255u;
+            atomicAdd(&hmass[b], q[r]);
+            atomicAdd(&hcount[b], 1u);
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+          // lane l holds bins 255-8l .. 248-8l (descending)
+          unsigned long long mb[8], local = 0;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            mb[k] = hmass[255 - 8 * lane - k];
+            local += mb[k];
+          }
+          unsigned long long incl = local;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          const unsigned long long excl = incl - local;
+          if (excl < need && need <= incl) {
+            unsigned long long acc = excl;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (acc + mb[k] >= need) {
+                ctl[0] = uint32_t(255 - 8 * lane - k);
+                ctl[1] = hcount[255 - 8 * lane - k];
+                ctl_m[0] = acc;                          // mass of the higher bins
+                break;
+              }
+              acc += mb[k];
+            }
+          }
+        }
+        __syncthreads();
+        const uint32_t b = ctl[0];
+        need -= ctl_m[0];
+        eq_count = ctl[1];
+        prefix |= b << shift;
+        mask |= 0xFFu << shift;
+        __syncthreads();
+      }
+      const uint32_t T = prefix;
+      // candidates above T are all kept; of those equal to T (equal masses),
+      // the lowest indices, as many as the remaining mass needs
+      unsigned long long qT = 0;
+#pragma unroll
+      for (int r = 0; r < kPerThread; ++r) {
+        const int j = tid + r * kThreads;
+        if (j >= 1 && j <= i - 1 && u[r] == T) qT = q[r];
+      }
+      if (tid == 0) ctl_m[1] = 0ull;
+      __syncthreads();
+      if (qT) atomicMax(&ctl_m[1], qT);
+      __syncthreads();
+      qT = ctl_m[1];
+      uint32_t take = qT ? uint32_t((need + qT - 1) / qT) : eq_count;
+      take = max(1u, min(take, eq_count));
+      uint32_t taken = 0;
+      for (int r = 0; r < kPerThread; ++r) {
+        const int j = tid + r * kThreads;
+        const bool valid = j >= 1 && j <= i - 1;
+        const bool eq = valid && u[r] == T;
+        const uint32_t m = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) wsum[warp] = __popc(m);
+        __syncthreads();
+        uint32_t before = taken;
+        for (int w = 0; w < warp; ++w) before += wsum[w];
+        before += __popc(m & ((1u << lane) - 1u));
+        if (valid && (u[r] > T || (eq && before < take))) atomicOr(&bits[j >> 5], 1u << (j & 31));
+        for (int w = 0; w < kThreads / 32; ++w) taken += wsum[w];
+        __syncthreads();
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int32_t* out = a.idx + size_t(row) * a.kmax;
+    int written = 0;
+    for (int base = 0; base <= i; base += 32) {
+      const int j = base + lane;
+      const bool on = (j <= i) && ((bits[j >> 5] >> (j & 31)) & 1u);
+      const uint32_t m = __ballot_sync(0xffffffffu, on);
+      const int pos = written + __popc(m & ((1u << lane) - 1u));
+      if (on && pos < a.kmax) out[pos] = j;
+      written += __popc(m);
+    }
+    for (int t = written + lane; t < a.kmax; t += 32) out[t] = -1;
+    if (lane == 0) a.cnt[row] = min(written, a.kmax);
+  }
+}
+
 }  // namespace
 
 namespace sa_k {
+
+cudaError_t launch_select_topp(const TopPArgs& a, cudaStream_t st) {
+  if (a.rows == 0) return cudaSuccess;
+  if (a.nb > kPerThread * kThreads) return cudaErrorInvalidValue;
+  select_topp_kernel<<<unsigned(a.rows), kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;

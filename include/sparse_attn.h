@@ -254,6 +254,48 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan,
                              int32_t kmax, sa_stream_t stream);
 
 /*
+ * Top-p selection, the data-dependent alternative the S-HPLB pages compare
+ * against (Italian summary, "Sparsita' Eterogenea": an adaptive top-p budget
+ * fixes accuracy but makes every head's work different).  Prefill only.
+ * Row (h, i): block probabilities are the softmax of the row's pooled scores
+ * over j <= i; the row keeps blocks 0 and i, then blocks of 1..i-1 by score
+ * (ties: lower index) until the kept probability reaches p (p >= 1 keeps the
+ * row's all blocks, p <= 0 only 0 and i).  Probabilities are summed in 64-bit
+ * fixed point (2^-32 of the row's total), so results are reproducible.
+ * Outputs as sparse_attn_select; kmax must be >= nb since a row may keep all
+ * its blocks.  The plan's budgets are not used; its schedule assumes them, so
+ * rebuild it from cnt (sparse_attn_plan_rebuild) before the forward.
+ * Errors: INVALID_ARG (NULL, NaN p, decode), SHAPE, UNSUPPORTED (nb > 2048),
+ * NOT_UPLOADED, CUDA.
+ */
+sa_status sparse_attn_select_topp(const sa_shape* shp, const sa_plan* plan,
+                                  const float* scores, float p, int32_t* idx,
+                                  int32_t* cnt, int32_t kmax, sa_stream_t stream);
+
+/*
+ * Rebuild a prefill plan's device schedule from device block counts
+ * cnt [Hq*nb] (e.g. from sparse_attn_select_topp), on the GPU: LPT with item
+ * cost cnt[item] -- items by cost descending (ties: lower id), each to the
+ * least-loaded worker (ties: lowest worker) -- written over the plan's device
+ * wptr / items, which sparse_attn_forward reads.  One single-CTA kernel on
+ * `stream` (about 148 KB of shared memory); the first call allocates 2*N
+ * int32 of scratch, owned by the plan.  Counts outside [0, 2048] are clamped
+ * to it.  The host copy of the schedule (sparse_attn_plan_get / _info) is not
+ * changed.  Up to 256 workers, nb <= 2048 and N = Hq*nb <= 2^19 items, else
+ * UNSUPPORTED.
+ * Errors: INVALID_ARG (NULL, decode plan), NOT_UPLOADED, UNSUPPORTED, CUDA.
+ */
+sa_status sparse_attn_plan_rebuild(sa_plan* plan, const int32_t* cnt, sa_stream_t stream);
+
+/*
+ * Copy the plan's device schedule (wptr [W+1], items [N]) into caller
+ * buffers, host or device (cudaMemcpyDefault), asynchronously on `stream`.
+ * Errors: INVALID_ARG, NOT_UPLOADED, CUDA.
+ */
+sa_status sparse_attn_plan_device_schedule(const sa_plan* plan, int32_t* wptr,
+                                           int32_t* items, sa_stream_t stream);
+
+/*
  * Attention over the selected blocks.
  * Prefill: o[h, t] = sum_u softmax_u(q[h,t] . k[g,u] / sqrt(d)) v[g,u] over
  *   the keys u of the blocks idx[h*nb+i][0..cnt) with u <= t (only the

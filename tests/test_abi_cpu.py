@@ -258,3 +258,26 @@ def test_output_aware_profile_plans_match_oracle(sa, number):
     got = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=oa["demand"],
                               k_min=prof["k_min"], num_workers=152).get()
     assert got["budgets"].tolist() == k
+
+
+def test_topp_and_rebuild_reject_bad_arguments_before_launch(sa):
+    shape = sa.Shape.prefill(4096, 64, 8, 2, 64)
+    plan = sa.sparse_attn_plan(shape, 9, num_workers=4)
+    lib, P = sa._lib, 8192
+    s = ctypes.byref(shape)
+    nb = shape.nb
+    # not uploaded; kmax below nb; NaN threshold; null output
+    assert lib.sparse_attn_select_topp(s, plan.handle, P, 0.9, P, P, nb, None) == 8
+    assert lib.sparse_attn_select_topp(s, plan.handle, P, 0.9, P, P, nb - 1, None) == 2
+    assert lib.sparse_attn_select_topp(s, plan.handle, P, float("nan"), P, P, nb, None) == 1
+    assert lib.sparse_attn_select_topp(s, plan.handle, P, 0.9, None, P, nb, None) == 1
+    # decode shapes have no top-p rows
+    dshape = sa.Shape.decode(4096, 32, 8, 2, 128, 2)
+    dplan = sa.sparse_attn_plan(dshape, 8, num_workers=1)
+    assert lib.sparse_attn_select_topp(ctypes.byref(dshape), dplan.handle, P, 0.9, P, P, 128,
+                                       None) == 1
+    # rebuild: not uploaded, decode plan, null counts
+    assert lib.sparse_attn_plan_rebuild(plan.handle, P, None) == 8
+    assert lib.sparse_attn_plan_rebuild(dplan.handle, P, None) == 1
+    assert lib.sparse_attn_plan_rebuild(plan.handle, None, None) == 1
+    assert lib.sparse_attn_plan_device_schedule(plan.handle, P, P, None) == 8
