@@ -312,16 +312,19 @@ def run_ours(args):
         del lo
 
     # ---- top-p selection (data-dependent counts) at the plan's mean density:
-    # a static head-order schedule against the LPT rebuilt on the GPU
+    # static schedules (head order; LPT over the top-k budgets) against the
+    # LPT rebuilt on the GPU from the selected counts
     topp = None
     if not args.no_variants:
         p_thr = layer.total_blocks / (w.num_q_heads * w.nb * (w.nb + 1) / 2)
         tidx = torch.empty(w.num_q_heads * w.nb * w.nb, dtype=torch.int32, device=dev)
         tcnt = torch.empty(w.num_q_heads * w.nb, dtype=torch.int32, device=dev)
         res = {}
-        for mode in ("head_order_static", "lpt_rebuilt"):
+        swptr = torch.empty(sms + 1, dtype=torch.int32, device=dev)
+        sitems = torch.empty(w.num_q_heads * w.nb, dtype=torch.int32, device=dev)
+        for mode in ("head_order_static", "lpt_static", "lpt_rebuilt"):
             pl = sa.sparse_attn_plan(shape, prof["k_uniform"], k_min=prof["k_min"],
-                                     num_workers=sms,
+                                     demand=prof["demand"], num_workers=sms,
                                      schedule="head_order" if mode == "head_order_static"
                                      else "lpt")
             pl.upload()
@@ -337,14 +340,20 @@ def run_ours(args):
                 sa.sparse_attn_forward(shape, pl, t["q"], t["k"], t["v"], tidx, tcnt, w.nb,
                                        layer.out, None, layer.dev_status, stream)
                 ev_t[3].record(stream)
+            pl.device_schedule(swptr, sitems, stream=stream)
             torch.cuda.synchronize(dev)
+            # makespan in selected blocks of the schedule the forward ran
+            cw = np.cumsum(np.concatenate([[0], tcnt.cpu().numpy()[sitems.cpu().numpy()]]))
+            wp = swptr.cpu().numpy()
             res[mode] = {"select_ms": round(ev_t[0].elapsed_time(ev_t[1]), 4),
                          "rebuild_ms": round(ev_t[1].elapsed_time(ev_t[2]), 4),
-                         "forward_ms": round(ev_t[2].elapsed_time(ev_t[3]), 4)}
+                         "forward_ms": round(ev_t[2].elapsed_time(ev_t[3]), 4),
+                         "makespan_blocks": int((cw[wp[1:]] - cw[wp[:-1]]).max())}
             pl.close()
         topp = {"p": round(p_thr, 5), "selected_blocks": int(tcnt.sum().item()),
+                "mean_load_blocks": round(float(tcnt.sum().item()) / sms, 1),
                 "device_status": int(layer.dev_status.item()), **res}
-        del tidx, tcnt
+        del tidx, tcnt, swptr, sitems
 
     # ---- end to end through the public API with host buffers
     out_host = torch.empty((w.num_q_heads, w.seq_len, w.head_dim), dtype=torch.bfloat16,

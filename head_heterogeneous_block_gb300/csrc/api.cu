@@ -197,7 +197,7 @@ sa_status sparse_attn_plan_rebuild(sa_plan* plan, const int32_t* cnt, sa_stream_
   if (plan->items.size() > (size_t(1) << 19)) return SA_ERR_UNSUPPORTED;
   const int32_t n = int32_t(plan->items.size());
   if (!plan->d_scratch) {
-    cudaError_t e = cudaMalloc(&plan->d_scratch, size_t(2) * std::max(n, 1) * sizeof(int32_t));
+    cudaError_t e = cudaMalloc(&plan->d_scratch, size_t(3) * std::max(n, 1) * sizeof(int32_t));
     if (e != cudaSuccess) return cuda_status(e);
   }
   sa_k::RebuildArgs a;

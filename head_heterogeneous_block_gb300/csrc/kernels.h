@@ -53,7 +53,7 @@ struct RebuildArgs {
   const int32_t* cnt;       // [N] blocks per item (the item's cost)
   int32_t* wptr;            // [W+1] out
   int32_t* items;           // [N] out
-  int32_t* scratch;         // [2N]
+  int32_t* scratch;         // [3N]
   int32_t num_items, num_workers;
 };
 cudaError_t launch_lpt_rebuild(const RebuildArgs& a, cudaStream_t st);

@@ -29,7 +29,7 @@ struct sa_plan {
   uint8_t* d_kinds = nullptr;
   int32_t* d_wptr = nullptr;
   int32_t* d_items = nullptr;
-  int32_t* d_scratch = nullptr;   // sparse_attn_plan_rebuild: 2N int32
+  int32_t* d_scratch = nullptr;   // sparse_attn_plan_rebuild: 3N int32
 };
 
 namespace sa_host {

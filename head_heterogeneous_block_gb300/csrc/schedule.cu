@@ -5,7 +5,11 @@
 // same greedy longest-first multiway partition as the host plan (S-HPLB,
 // "Algoritmo Greedy"): items by cost descending, ties to the lower item id,
 // each given to the least-loaded worker, ties to the lowest worker id.  The
-// result is the CSR schedule the forward kernel reads (wptr [W+1], items [N]).
+// result is the CSR schedule the forward kernel reads (wptr [W+1], items [N]),
+// each worker's items listed in item order: items are head-major, so the
+// CTAs, walking their lists at a similar pace, tend to read the same KV head
+// at the same time (with costs that vary per row, assignment order would mix
+// all heads at every moment).
 //
 // One CTA of 16 warps:
 //   1. stable counting sort by cost, descending (all warps): per-warp chunk
@@ -13,11 +17,12 @@
 //      in item-id order (lanes with equal cost ranked by lane);
 //   2. the greedy (warp 0), placed one run of equal-cost items at a time (see
 //      below): the same assignment as walking the items one by one, without a
-//      sequential step per item.  Each sorted position gets (worker, index in
-//      that worker's list);
-//   3. CSR (all warps): worker offsets, then every item straight to its slot.
-// Scratch (sorted items and their (worker, index), 2 x N int32) is caller
-// memory; num_items <= 2^19 keeps every load and index in 32 bits.
+//      sequential step per item;
+//   3. CSR (all warps): worker offsets, then a stable scatter of the items by
+//      worker, in item order (per-warp chunk histograms, as in 1).
+// Scratch (sorted items, the worker of each sorted position, the worker of
+// each item: 3 x N int32) is caller memory; num_items <= 2^19 keeps every
+// load in 32 bits.
 
 #include <cstdint>
 
@@ -29,7 +34,6 @@ constexpr int kMaxCost = 2048;          // costs are block counts: 1..nb <= 2048
 constexpr int kMaxWorkers = 256;
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kIdxBits = 20;            // index within a worker's list
 constexpr int kMaxItems = 1 << 19;
 
 struct RebuildSmem {
@@ -38,10 +42,10 @@ struct RebuildSmem {
   int16_t runs[kMaxCost + 1];           // the costs that occur, descending
   int32_t wbase[kMaxWorkers];
   // the workers taking pairs in a run, compacted in id order: sort key
-  // (L mod c, compacted index), then L / c, pair count, list length and id
+  // (L mod c, compacted index), then L / c, pair count and id
   uint32_t key[kMaxWorkers];
   uint32_t sq[kMaxWorkers], sn[kMaxWorkers];
-  int32_t sw[kMaxWorkers], sc[kMaxWorkers];
+  int32_t sw[kMaxWorkers];
 };
 
 __device__ __forceinline__ int clamp_cost(int c) {
@@ -55,7 +59,8 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_rebuild_kernel(sa_k::RebuildA
   const uint32_t lt = (1u << lane) - 1u;
   const int N = a.num_items, W = a.num_workers;
   int32_t* sorted = a.scratch;             // [N] item ids, cost descending
-  int32_t* where = a.scratch + N;          // [N] (worker, index) of sorted[s]
+  int32_t* where = a.scratch + N;          // [N] worker of sorted[s]
+  int32_t* owner = a.scratch + 2 * N;      // [N] worker of item x
 
   // ---- 1. stable counting sort by cost, descending
   for (int i = tid; i < kWarps * (kMaxCost + 1); i += kThreads) (&sh.tab[0][0])[i] = 0;
@@ -151,12 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_rebuild_kernel(sa_k::RebuildA
       if (c == 0) {
         // zero cost: every item goes to the least-loaded worker, loads unchanged
         const int w0 = int(__reduce_min_sync(0xffffffffu, v == mn ? wmin : 0xFFFFFFFFu));
-        int32_t n0 = 0;
-#pragma unroll
-        for (int j = 0; j < kSlots; ++j)
-          if (lane + 32 * j == w0) n0 = Cn[j];
-        n0 = __shfl_sync(0xffffffffu, n0, w0 & 31);
-        for (int k = lane; k < r; k += 32) where[start + k] = (w0 << kIdxBits) | (n0 + k);
+        for (int k = lane; k < r; k += 32) where[start + k] = w0;
 #pragma unroll
         for (int j = 0; j < kSlots; ++j)
           if (lane + 32 * j == w0) Cn[j] += r;
@@ -213,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_rebuild_kernel(sa_k::RebuildA
             sh.key[k] = (Lr[j] << 8) | uint32_t(k);      // c <= 2048, k < 256
             sh.sq[k] = Lq[j];
             sh.sn[k] = Nn[j];
-            sh.sc[k] = Cn[j];
             sh.sw[k] = w;
           }
           A += __popc(act);
@@ -249,16 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_rebuild_kernel(sa_k::RebuildA
         for (int t = 0; t < kSlots; ++t)
           if (lane + 32 * t < A) kk[t] = sh.key[lane + 32 * t];
       }
-      uint32_t tq[kSlots], tn[kSlots], tw[kSlots], tc[kSlots];
+      uint32_t tq[kSlots], tn[kSlots], tw[kSlots];
       uint32_t qlo = 0xFFFFFFFFu, qhi = 0;
 #pragma unroll
       for (int t = 0; t < kSlots; ++t) {
-        tq[t] = tn[t] = tw[t] = tc[t] = 0;
+        tq[t] = tn[t] = tw[t] = 0;
         if (lane + 32 * t < A) {
           const int k = int(kk[t] & 0xFFu);
           tq[t] = sh.sq[k];
           tn[t] = sh.sn[k];
-          tc[t] = uint32_t(sh.sc[k]);
           tw[t] = uint32_t(sh.sw[k]);
           qlo = min(qlo, tq[t]);
           qhi = max(qhi, tq[t] + tn[t] - 1);
@@ -276,8 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_rebuild_kernel(sa_k::RebuildA
             const bool on = tq[t] <= qv && qv < tq[t] + tn[t];
             const uint32_t m = __ballot_sync(0xffffffffu, on);
             const int at = start + pos + __popc(m & lt);
-            if (on && at < end)
-              where[at] = int32_t((tw[t] << kIdxBits) | (tc[t] + (qv - tq[t])));
+            if (on && at < end) where[at] = int32_t(tw[t]);
             pos += __popc(m);
           }
         }
@@ -312,12 +309,39 @@ __global__ void __launch_bounds__(kThreads, 1) lpt_rebuild_kernel(sa_k::RebuildA
   }
   __syncthreads();
 
-  // ---- 3b. every item to its slot in its worker's list
-  for (int s = tid; s < N; s += kThreads) {
-    const int32_t p = where[s];
-    const int w = p >> kIdxBits;
-    const int slot = w < W ? sh.wbase[w] + (p & ((1 << kIdxBits) - 1)) : N;
-    if (slot < N) a.items[slot] = sorted[s];
+  // ---- 3b. the worker of every item, then a stable scatter by worker in
+  // item order: chunk counts per worker, their offsets from the worker
+  // offsets, and each warp's chunk in order (lanes with equal worker ranked
+  // by lane)
+  for (int s = tid; s < N; s += kThreads) owner[sorted[s]] = where[s];
+  for (int i = tid; i < kWarps * kMaxWorkers; i += kThreads) sh.tab[i / kMaxWorkers][i % kMaxWorkers] = 0;
+  __syncthreads();
+  for (int x = x0 + lane; x < x1; x += 32) {
+    const int w = owner[x];
+    if (w >= 0 && w < W) atomicAdd(&sh.tab[warp][w], 1);
+  }
+  __syncthreads();
+  for (int w = tid; w < W; w += kThreads) {
+    int32_t run = sh.wbase[w];
+    for (int k = 0; k < kWarps; ++k) {
+      const int32_t t = sh.tab[k][w];
+      sh.tab[k][w] = run;
+      run += t;
+    }
+  }
+  __syncthreads();
+  for (int base = x0; base < x1; base += 32) {
+    const int x = base + lane;
+    int w = x < x1 ? owner[x] : -1;
+    if (w >= W) w = -1;
+    const uint32_t same = __match_any_sync(0xffffffffu, w);
+    if (w >= 0) {
+      const int slot = sh.tab[warp][w] + __popc(same & lt);
+      if (slot < N) a.items[slot] = x;
+    }
+    __syncwarp();
+    if (w >= 0 && lane == __ffs(same) - 1) sh.tab[warp][w] += __popc(same);
+    __syncwarp();
   }
 }
 

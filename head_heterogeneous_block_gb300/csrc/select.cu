@@ -215,11 +215,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
 // of probability mass next to the counts.
 __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a) {
   __shared__ uint32_t bits[kMaxWords];
-  __shared__ unsigned long long hmass[256];
-  __shared__ uint32_t hcount[256];
+  __shared__ unsigned long long hmass[kThreads / 32][256];   // one histogram per warp
+  __shared__ uint32_t hcount[kThreads / 32][256];
   __shared__ float redf[kThreads / 32];
   __shared__ unsigned long long ctl_m[2];
-  __shared__ uint32_t ctl[2];
+  __shared__ uint32_t ctl[3];
   __shared__ uint32_t wsum[kThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
@@ -260,13 +260,15 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
 #pragma unroll
   for (int w = 0; w < kThreads / 32; ++w) tot += redf[w];   // same order in every thread
   const float scale = 4294967296.0f / tot;                  // 2^32 / total
-  // fixed-point masses; the mandatory blocks' mass is taken first
-  unsigned long long q[kPerThread];
+  // fixed-point masses (a block's share is at most 2^32, kept as 2^32 - 1);
+  // the mandatory blocks' mass is taken first
+  uint32_t q[kPerThread];
   unsigned long long mand = 0;
 #pragma unroll
   for (int r = 0; r < kPerThread; ++r) {
     const int j = tid + r * kThreads;
-    q[r] = (j <= i) ? (unsigned long long)(e[r] * scale) : 0ull;
+    const float x = e[r] * scale;
+    q[r] = (j <= i) ? (x >= 4294967296.0f ? 0xFFFFFFFFu : uint32_t(x)) : 0u;
     if (j == 0 || j == i) mand += q[r];
   }
   if (tid == 0) ctl_m[0] = 0ull;
@@ -302,9 +304,9 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
     } else {
       uint32_t prefix = 0, mask = 0, eq_count = 0;
       for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int b = tid; b < 256; b += kThreads) {
-          hmass[b] = 0ull;
-          hcount[b] = 0u;
+        for (int b = tid; b < (kThreads / 32) * 256; b += kThreads) {
+          (&hmass[0][0])[b] = 0ull;
+          (&hcount[0][0])[b] = 0u;
         }
         __syncthreads();
 #pragma unroll
@@ -312,17 +314,19 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
           const int j = tid + r * kThreads;
           if (j >= 1 && j <= i - 1 && (u[r] & mask) == prefix) {
             const uint32_t b = (u[r] >> shift) & 255u;
-            atomicAdd(&hmass[b], q[r]);
-            atomicAdd(&hcount[b], 1u);
+            atomicAdd(&hmass[warp][b], (unsigned long long)q[r]);
+            atomicAdd(&hcount[warp][b], 1u);
           }
         }
         __syncthreads();
         if (warp == 0) {
-          // lane l holds bins 255-8l .. 248-8l (descending)
+          // lane l holds bins 255-8l .. 248-8l (descending), summed over warps
           unsigned long long mb[8], local = 0;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            mb[k] = hmass[255 - 8 * lane - k];
+            mb[k] = 0ull;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) mb[k] += hmass[w][255 - 8 * lane - k];
             local += mb[k];
           }
           unsigned long long incl = local;
@@ -337,8 +341,11 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               if (acc + mb[k] >= need) {
+                uint32_t n = 0;
+#pragma unroll
+                for (int w = 0; w < kThreads / 32; ++w) n += hcount[w][255 - 8 * lane - k];
                 ctl[0] = uint32_t(255 - 8 * lane - k);
-                ctl[1] = hcount[255 - 8 * lane - k];
+                ctl[1] = n;
                 ctl_m[0] = acc;                          // mass of the higher bins
                 break;
               }
@@ -353,6 +360,18 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
         prefix |= b << shift;
         mask |= 0xFFu << shift;
         __syncthreads();
+        if (eq_count == 1 && shift > 0) {
+          // one candidate left in the bin: it is the threshold
+#pragma unroll
+          for (int r = 0; r < kPerThread; ++r) {
+            const int j = tid + r * kThreads;
+            if (j >= 1 && j <= i - 1 && (u[r] & mask) == prefix) ctl[2] = u[r];
+          }
+          __syncthreads();
+          prefix = ctl[2];
+          __syncthreads();
+          break;
+        }
       }
       const uint32_t T = prefix;
       // candidates above T are all kept; of those equal to T (equal masses),
@@ -370,6 +389,14 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
       qT = ctl_m[1];
       uint32_t take = qT ? uint32_t((need + qT - 1) / qT) : eq_count;
       take = max(1u, min(take, eq_count));
+      if (take == eq_count) {
+        // every candidate at T is kept: no order among them is needed
+#pragma unroll
+        for (int r = 0; r < kPerThread; ++r) {
+          const int j = tid + r * kThreads;
+          if (j >= 1 && j <= i - 1 && u[r] >= T) atomicOr(&bits[j >> 5], 1u << (j & 31));
+        }
+      } else {
       uint32_t taken = 0;
       for (int r = 0; r < kPerThread; ++r) {
         const int j = tid + r * kThreads;
@@ -384,6 +411,7 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
         if (valid && (u[r] > T || (eq && before < take))) atomicOr(&bits[j >> 5], 1u << (j & 31));
         for (int w = 0; w < kThreads / 32; ++w) taken += wsum[w];
         __syncthreads();
+      }
       }
     }
   }

@@ -277,9 +277,11 @@ sa_status sparse_attn_select_topp(const sa_shape* shp, const sa_plan* plan,
  * cnt [Hq*nb] (e.g. from sparse_attn_select_topp), on the GPU: LPT with item
  * cost cnt[item] -- items by cost descending (ties: lower id), each to the
  * least-loaded worker (ties: lowest worker) -- written over the plan's device
- * wptr / items, which sparse_attn_forward reads.  One single-CTA kernel on
- * `stream` (about 148 KB of shared memory); the first call allocates 2*N
- * int32 of scratch, owned by the plan.  Counts outside [0, 2048] are clamped
+ * wptr / items, which sparse_attn_forward reads.  Each worker's items are
+ * listed in ascending item id (head-major), so that CTAs running at the same
+ * time tend to read the same KV head.  One single-CTA kernel on `stream`
+ * (about 148 KB of shared memory); the first call allocates 3*N int32 of
+ * scratch, owned by the plan.  Counts outside [0, 2048] are clamped
  * to it.  The host copy of the schedule (sparse_attn_plan_get / _info) is not
  * changed.  Up to 256 workers, nb <= 2048 and N = Hq*nb <= 2^19 items, else
  * UNSUPPORTED.

@@ -165,12 +165,18 @@ def schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int 
     return wptr, items, loads
 
 
-def schedule_from_costs(costs: list[int], workers: int):
+def schedule_from_costs(costs: list[int], workers: int, within: str = "assignment"):
     """LPT over given item costs (e.g. the block counts a data-dependent
     selection produced): items by cost descending, ties lower id, each to the
-    least-loaded worker.  Returns (wptr, items, loads) as schedule()."""
+    least-loaded worker.  Each worker's list is in assignment order, or with
+    within="item" in ascending item id.  Returns (wptr, items, loads) as
+    schedule()."""
     order = sorted(range(len(costs)), key=lambda x: (-costs[x], x))
     lists, loads = lpt_assign(order, costs, workers)
+    if within == "item":
+        lists = [sorted(lst) for lst in lists]
+    elif within != "assignment":
+        raise ValueError(within)
     wptr = [0]
     items = []
     for lst in lists:

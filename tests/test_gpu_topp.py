@@ -97,9 +97,11 @@ def test_topp_selection_and_device_rebuild(env, number, S, Hq, Hkv, p):
         for i in range(nb):
             assert np.all(g_idx[h, i, g_cnt[h, i]:] == -1)
             check_topp_row(g_idx[h, i, :g_cnt[h, i]], ref_scores[h, i], i, p)
-    # the device schedule is exactly the oracle's LPT on the GPU's own counts
+    # the device schedule is exactly the oracle's LPT on the GPU's own counts,
+    # each worker's list in item order
     wptr, items = _device_schedule(torch, layer, W, Hq * nb)
-    want_wptr, want_items, _ = op.schedule_from_costs(g_cnt.reshape(-1).tolist(), W)
+    want_wptr, want_items, _ = op.schedule_from_costs(g_cnt.reshape(-1).tolist(), W,
+                                                      within="item")
     assert wptr == want_wptr and items == want_items
     P.check_attention(out.cpu().numpy(), lse.view(Hq, S).cpu().numpy(), x, g_idx, g_cnt,
                       w.block, range(Hq * nb), w.group)
@@ -122,7 +124,7 @@ def test_device_rebuild_matches_oracle_lpt(env, W):
     items = torch.empty(8 * nb, dtype=torch.int32, device="cuda")
     plan.device_schedule(wptr, items)
     torch.cuda.synchronize()
-    want_wptr, want_items, _ = op.schedule_from_costs(costs.tolist(), W)
+    want_wptr, want_items, _ = op.schedule_from_costs(costs.tolist(), W, within="item")
     assert wptr.cpu().tolist() == want_wptr
     assert items.cpu().tolist() == want_items
 
@@ -153,7 +155,8 @@ def test_device_rebuild_full_size_and_clamped_counts(env, W, kind):
     items = torch.empty(n, dtype=torch.int32, device="cuda")
     plan.device_schedule(wptr, items)
     torch.cuda.synchronize()
-    want_wptr, want_items, _ = op.schedule_from_costs(np.clip(costs, 0, 2048).tolist(), W)
+    want_wptr, want_items, _ = op.schedule_from_costs(np.clip(costs, 0, 2048).tolist(), W,
+                                                      within="item")
     assert wptr.cpu().tolist() == want_wptr
     assert items.cpu().tolist() == want_items
 

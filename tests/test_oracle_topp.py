@@ -92,3 +92,14 @@ def test_lpt_over_costs_is_a_partition_within_grahams_bound():
         opt = min(max(sum(costs[x] for x in range(len(costs)) if a[x] == w) for w in range(W))
                   for a in itertools.product(range(W), repeat=len(costs)))
         assert max(loads) <= (4 / 3 - 1 / (3 * W)) * opt + 1e-9
+
+
+def test_item_order_keeps_each_workers_set_and_sorts_it():
+    r = np.random.default_rng(26)
+    costs = [int(x) for x in r.integers(0, 40, 200)]
+    a_wptr, a_items, a_loads = P.schedule_from_costs(costs, 7)
+    i_wptr, i_items, i_loads = P.schedule_from_costs(costs, 7, within="item")
+    assert a_wptr == i_wptr and a_loads == i_loads
+    for w in range(7):
+        lst = i_items[i_wptr[w]:i_wptr[w + 1]]
+        assert lst == sorted(a_items[a_wptr[w]:a_wptr[w + 1]])
