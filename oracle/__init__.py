@@ -29,6 +29,7 @@ Sources (page title, then section):
 
 Modules: ``plan`` (budgets and schedules), ``calib`` (coverage calibration to
 demands), ``attention`` (pooling, scores, selection, sparse prefill attention),
-``decode`` (the decode step).  Every function is pinned by CPU tests against
+``decode`` (the decode step), ``granularity`` (per-head block sizes and
+budgets for decode retrieval heads).  Every function is pinned by CPU tests against
 closed forms, brute force, or library routines (see ``tests/test_oracle_*``).
 """

@@ -68,19 +68,23 @@ def decode_select(scores: np.ndarray, kinds, budget: int, window_blocks: int):
 
 
 def decode_attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, idx: np.ndarray,
-                  cnt: np.ndarray, B: int):
+                  cnt: np.ndarray, B):
     """Softmax attention of each new query over its selected blocks.
 
+    B is the block size in tokens, one for all heads or one per head (a
+    head's block j covers tokens [j*B_h, (j+1)*B_h)).
     Returns (o [Bt, Hq, d], lse [Bt, Hq]) in fp64.
     """
     Bt, Hq, d = q.shape
     group = Hq // k.shape[1]
+    sizes = [int(B)] * Hq if np.isscalar(B) else [int(x) for x in B]
     o = np.empty((Bt, Hq, d))
     lse = np.empty((Bt, Hq))
     for b in range(Bt):
         for h in range(Hq):
             blocks = idx[b, h, :cnt[b, h]]
-            u = np.concatenate([np.arange(j * B, (j + 1) * B) for j in blocks])
+            Bh = sizes[h]
+            u = np.concatenate([np.arange(j * Bh, (j + 1) * Bh) for j in blocks])
             ku = k[b, h // group, u].astype(np.float64)
             vu = v[b, h // group, u].astype(np.float64)
             logits = ku @ q[b, h].astype(np.float64) / math.sqrt(d)

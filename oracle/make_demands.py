@@ -17,8 +17,15 @@ causal blocks needed to keep the sparse output within a tolerance of the full
 output, the tolerance scaled by the head's relative output norm.  The result
 goes under "output_aware" beside the mass-based profile, which is left as is.
 
+With --granularity it writes, for the decode workload, each retrieval head's
+selection block size and budget (Fluxion, "Intuizioni Chiave" 2 and its
+granularity-budget selector): on a calibration draw, every head keeps at least
+the attention mass of the default selection, and each KV group takes the sizes
+that move the fewest bytes per decode step (``oracle.granularity``).
+
 Usage:  python -m oracle.make_demands [--out workloads/demands.json]
         python -m oracle.make_demands --output-aware [--workloads 1,2,3]
+        python -m oracle.make_demands --granularity [--workloads 5]
 """
 from __future__ import annotations
 
@@ -35,7 +42,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from oracle import calib, plan  # noqa: E402
+from oracle import calib, granularity, plan  # noqa: E402
 from workloads import WORKLOADS, generate  # noqa: E402
 
 K_MIN = 2
@@ -95,6 +102,35 @@ def profile_output_aware(number: int, pool) -> dict:
     }
 
 
+GRANULARITIES = (16, 32, 64, 128)   # candidate block sizes of a retrieval head
+
+
+def profile_granularity(number: int) -> dict:
+    w = WORKLOADS[number]
+    kinds = generate.head_kinds(w)
+    x = generate.decode_inputs(w, tensors="qk", batches=[0], seed=w.calib_seed)
+    q = generate.bf16_to_f64(x["q"][0])
+    k = generate.bf16_to_f64(x["k"][0])
+    g0, k0 = w.block, w.budget_tokens // w.block
+    sizes = sorted(set(GRANULARITIES) | {g0})
+    masses = {h: {g: granularity.decode_block_mass(q[h], k[h // w.group], g) for g in sizes}
+              for h in range(w.num_q_heads) if kinds[h] != granularity.STREAMING}
+    res = granularity.choose_granularity(masses, kinds, w.group, g0, k0, GRANULARITIES,
+                                         w.seq_len, w.head_dim)
+    return {
+        "workload": w.name,
+        "source": (f"decode query of a calibration draw (seed {w.calib_seed}, one sequence, "
+                   f"{w.seq_len} tokens): each retrieval head keeps at least the attention "
+                   f"mass of the default selection ({k0} blocks of {g0}); per KV group the "
+                   f"block sizes that move the fewest bytes per step"),
+        "candidates": list(GRANULARITIES), "g0": g0, "k0": k0,
+        "gran": res["gran"], "budget": res["budget"],
+        "target": [round(float(t), 12) for t in res["target"]],
+        "kept": [round(float(t), 12) for t in res["kept"]],
+        "bytes": res["bytes"], "bytes_default": res["bytes_default"],
+    }
+
+
 def profile(number: int, pool=None) -> dict:
     w = WORKLOADS[number]
     nb = w.nb
@@ -129,11 +165,26 @@ def main():
     ap.add_argument("--out", default=os.path.join(ROOT, "workloads", "demands.json"))
     ap.add_argument("--workloads", default="1,2,3,4")
     ap.add_argument("--output-aware", action="store_true")
+    ap.add_argument("--granularity", action="store_true")
     args = ap.parse_args()
     out = {}
     if os.path.exists(args.out):
         with open(args.out) as f:
             out = json.load(f)
+    if args.granularity:
+        nums = [int(x) for x in args.workloads.split(",")] if args.workloads != "1,2,3,4" else [5]
+        for n in nums:
+            if WORKLOADS[n].demand_source != "decode":
+                continue
+            t = time.time()
+            out.setdefault(str(n), {})["granularity"] = profile_granularity(n)
+            gr = out[str(n)]["granularity"]
+            print(f"workload {n} granularity: {time.time() - t:.1f}s sizes {gr['gran']} "
+                  f"bytes {gr['bytes']} vs {gr['bytes_default']}", flush=True)
+        with open(args.out, "w") as f:
+            json.dump(out, f, indent=1)
+            f.write("\n")
+        return
     ctx = mp.get_context("spawn")
     with ctx.Pool(max(1, os.cpu_count() or 1)) as pool:
         for n in [int(x) for x in args.workloads.split(",")]:
