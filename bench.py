@@ -447,14 +447,17 @@ def bench_decode(dev, stream):
     for _ in range(3):
         step(t["q"], t["k"], t["v"], stream=stream)
     # flush L2 between decode steps (the cache is 2 GB but one step touches
-    # ~0.5 GB, which would otherwise partly stay in L2)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    times, fwd = [], []
+    # ~0.5 GB, which would otherwise partly stay in L2) by reading a buffer
+    # twice its size: reading leaves clean lines, so the next step's loads do
+    # not pay for writing the flush back
+    flush = torch.zeros(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    times, fwd, sco = [], [], []
     for _ in range(10):
-        flush.zero_()
-        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        flush.max()
+        e0, e1, e2, es = (torch.cuda.Event(enable_timing=True) for _ in range(4))
         e0.record(stream)
         sa.sparse_attn_score(shape, t["q"], step.kbar, step.scores, None, 0, stream=stream)
+        es.record(stream)
         sa.sparse_attn_select(shape, step.plan, step.scores, step.idx, step.cnt, step.kmax,
                               stream=stream)
         e1.record(stream)
@@ -464,6 +467,7 @@ def bench_decode(dev, stream):
         torch.cuda.synchronize(dev)
         times.append(e0.elapsed_time(e2))
         fwd.append(e1.elapsed_time(e2))
+        sco.append(e0.elapsed_time(es))
     a.record(stream)
     step.build_cache(t["k"], stream=stream)
     b.record(stream)
@@ -484,12 +488,82 @@ def bench_decode(dev, stream):
     q_o = 2 * w.batch * w.num_q_heads * w.head_dim * 2
     fwd_ms = statistics.median(fwd)
     peaks = _peaks()
-    return {"workload": w.name, "ms_per_step": round(statistics.median(times), 4),
-            "forward_ms": round(fwd_ms, 4),
-            "forward_gbs": round((kv_bytes + q_o) / (fwd_ms * 1e-3) / 1e9, 1),
-            "forward_frac_hbm": round((kv_bytes + q_o) / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-            "touched_kv_bytes": kv_bytes, "kbar_bytes": kbar_bytes,
-            "kcache_pool_ms": round(a.elapsed_time(b), 4), "l2": "flushed between steps"}
+    res = {"workload": w.name, "ms_per_step": round(statistics.median(times), 4),
+           "score_ms": round(statistics.median(sco), 4),
+           "select_ms": round(statistics.median(times) - statistics.median(sco) - fwd_ms, 4),
+           "forward_ms": round(fwd_ms, 4),
+           "forward_gbs": round((kv_bytes + q_o) / (fwd_ms * 1e-3) / 1e9, 1),
+           "forward_frac_hbm": round((kv_bytes + q_o) / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+           "touched_kv_bytes": kv_bytes, "kbar_bytes": kbar_bytes,
+           "kcache_pool_ms": round(a.elapsed_time(b), 4),
+           "l2": "flushed between steps (a 256 MB read)"}
+    del step
+    res["block_sizes"] = bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush)
+    return res
+
+
+def bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush):
+    """The decode step with each retrieval head's block size and budget chosen
+    offline (per KV group, at least the default selection's attention mass at
+    the fewest bytes), against the default step timed above."""
+    import numpy as np
+    import torch
+
+    import head_heterogeneous_block_gb300 as sa
+    from head_heterogeneous_block_gb300.layer import DecodeStep
+
+    with open(os.path.join(ROOT, "workloads", "demands.json")) as f:
+        prof = json.load(f)[str(w.number)]["granularity"]
+    step = DecodeStep(shape, 2, kinds, w.window_tokens // w.block, device=dev,
+                      granularity=prof["gran"], head_budget=prof["budget"])
+    step.build_cache(t["k"], stream=stream)
+    for _ in range(3):
+        step(t["q"], t["k"], t["v"], stream=stream)
+    times, fwd, sco = [], [], []
+    for _ in range(10):
+        flush.max()
+        e0, e1, e2, es = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        e0.record(stream)
+        sa.sparse_attn_score_plan(shape, step.plan, t["q"], step.kbar, step.scores, stream=stream)
+        es.record(stream)
+        sa.sparse_attn_select(shape, step.plan, step.scores, step.idx, step.cnt, step.kmax,
+                              stream=stream)
+        e1.record(stream)
+        sa.sparse_attn_forward(shape, step.plan, t["q"], t["k"], t["v"], step.idx, step.cnt,
+                               step.kmax, step.out, None, step.dev_status, stream=stream)
+        e2.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e2))
+        fwd.append(e1.elapsed_time(e2))
+        sco.append(e0.elapsed_time(es))
+    # touched bytes: union of selected tokens per (sequence, kv head), K and V;
+    # pooled keys: each block size a group's retrieval heads use, once
+    idx = step.idx.view(w.batch, w.num_q_heads, step.kmax).cpu().numpy()
+    cnt = step.cnt.view(w.batch, w.num_q_heads).cpu().numpy()
+    size = [prof["gran"][h] if kinds[h] != 1 else w.block for h in range(w.num_q_heads)]
+    G = w.group
+    tokens = 0
+    kbar_bytes = 0
+    for g in range(w.num_kv_heads):
+        used = {size[h] for h in range(g * G, (g + 1) * G) if kinds[h] != 1}
+        kbar_bytes += w.batch * sum((w.seq_len // s) * w.head_dim * 4 for s in used)
+        for bb in range(w.batch):
+            mask = np.zeros(w.seq_len, bool)
+            for h in range(g * G, (g + 1) * G):
+                for j in idx[bb, h, :cnt[bb, h]].tolist():
+                    mask[j * size[h]:(j + 1) * size[h]] = True
+            tokens += int(mask.sum())
+    status = int(step.dev_status.item())
+    return {"ms_per_step": round(statistics.median(times), 4),
+            "score_ms": round(statistics.median(sco), 4),
+            "select_ms": round(statistics.median(times) - statistics.median(sco)
+                               - statistics.median(fwd), 4),
+            "forward_ms": round(statistics.median(fwd), 4),
+            "touched_kv_bytes": tokens * w.head_dim * 2 * 2, "kbar_bytes": kbar_bytes,
+            "sizes": sorted(set(size[h] for h in range(w.num_q_heads) if kinds[h] != 1)),
+            "modelled_bytes_per_sequence": prof["bytes"],
+            "modelled_bytes_per_sequence_default": prof["bytes_default"],
+            "device_status": status}
 
 
 def cpu_baseline(args, sample_seconds: float):

@@ -20,6 +20,7 @@ __all__ = [
     "Shape", "Plan", "SparseAttnError", "sparse_attn_plan", "sparse_attn_score",
     "sparse_attn_score_workspace_size", "sparse_attn_select", "sparse_attn_forward",
     "sparse_attn_pool_kcache", "sa_status_string", "library_path",
+    "sparse_attn_select_topp", "sparse_attn_pool_kcache_plan", "sparse_attn_score_plan",
 ]
 
 SA_OK = 0
@@ -55,7 +56,9 @@ class _PlanParams(ctypes.Structure):
     _fields_ = [("demand", ctypes.POINTER(ctypes.c_int32)), ("k_uniform", ctypes.c_int32),
                 ("k_min", ctypes.c_int32), ("head_kind", ctypes.POINTER(ctypes.c_uint8)),
                 ("window_blocks", ctypes.c_int32), ("num_workers", ctypes.c_int32),
-                ("schedule", ctypes.c_int32), ("group_shared", ctypes.c_int32)]
+                ("schedule", ctypes.c_int32), ("group_shared", ctypes.c_int32),
+                ("granularity", ctypes.POINTER(ctypes.c_int32)),
+                ("head_budget", ctypes.POINTER(ctypes.c_int32))]
 
 
 class SparseAttnError(RuntimeError):
@@ -96,6 +99,11 @@ def _load():
                                                    P, P, I32, P]),
         "sparse_attn_plan_rebuild": (ctypes.c_int, [P, P, P]),
         "sparse_attn_plan_device_schedule": (ctypes.c_int, [P, P, P, P]),
+        "sparse_attn_plan_decode_layout": (ctypes.c_int, [P, ctypes.POINTER(I32), P,
+                                                          ctypes.POINTER(I64),
+                                                          ctypes.POINTER(I32)]),
+        "sparse_attn_pool_kcache_plan": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P]),
+        "sparse_attn_score_plan": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -189,6 +197,17 @@ class Plan:
                                                      _stream(stream)),
                "sparse_attn_plan_device_schedule")
 
+    def decode_layout(self) -> dict:
+        """Decode: the retrieval heads' block sizes, the floats of their pooled
+        key caches together, and the score row stride."""
+        n, floats, stride = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
+        sizes = np.zeros(8, np.int32)
+        _check(_lib.sparse_attn_plan_decode_layout(self._h, ctypes.byref(n), sizes.ctypes.data,
+                                                   ctypes.byref(floats), ctypes.byref(stride)),
+               "sparse_attn_plan_decode_layout")
+        return {"sizes": [int(x) for x in sizes[:n.value]], "kcache_floats": floats.value,
+                "score_stride": stride.value}
+
     def close(self):
         if self._h is not None and self._h.value:
             _lib.sparse_attn_plan_destroy(self._h)
@@ -203,7 +222,8 @@ class Plan:
 
 def sparse_attn_plan(shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
                      head_kind=None, window_blocks: int = 0, num_workers: int = 152,
-                     schedule="lpt", group_shared: bool = False) -> Plan:
+                     schedule="lpt", group_shared: bool = False, granularity=None,
+                     head_budget=None) -> Plan:
     if isinstance(schedule, str):
         schedule = SCHEDULES[schedule]
     params = _PlanParams()
@@ -216,6 +236,11 @@ def sparse_attn_plan(shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
         hk = np.ascontiguousarray(head_kind, dtype=np.uint8)
         keep.append(hk)
         params.head_kind = hk.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+    for name, arr in (("granularity", granularity), ("head_budget", head_budget)):
+        if arr is not None:
+            a = np.ascontiguousarray(arr, dtype=np.int32)
+            keep.append(a)
+            setattr(params, name, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
     params.k_uniform = k_uniform
     params.k_min = k_min
     params.window_blocks = window_blocks
@@ -278,6 +303,20 @@ def sparse_attn_forward(shape: Shape, plan, q, k, v, idx, cnt, kmax: int, o, lse
 def sparse_attn_pool_kcache(shape: Shape, k, kbar, stream=None):
     _check(_lib.sparse_attn_pool_kcache(ctypes.byref(shape), _ptr(k), _ptr(kbar),
                                         _stream(stream)), "sparse_attn_pool_kcache")
+
+
+def sparse_attn_pool_kcache_plan(shape: Shape, plan: Plan, k, kbar_all, stream=None):
+    """Pooled key caches at every block size of the plan's retrieval heads."""
+    _check(_lib.sparse_attn_pool_kcache_plan(ctypes.byref(shape), plan.handle, _ptr(k),
+                                             _ptr(kbar_all), _stream(stream)),
+           "sparse_attn_pool_kcache_plan")
+
+
+def sparse_attn_score_plan(shape: Shape, plan: Plan, q, kbar_all, scores, stream=None):
+    """Decode scores of each retrieval head at its own block size."""
+    _check(_lib.sparse_attn_score_plan(ctypes.byref(shape), plan.handle, _ptr(q),
+                                       _ptr(kbar_all), _ptr(scores), _stream(stream)),
+           "sparse_attn_score_plan")
 
 
 _noalloc = None

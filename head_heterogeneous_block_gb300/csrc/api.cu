@@ -30,6 +30,7 @@ void free_device(sa_plan* p) {
     if (cur != p->device) cudaSetDevice(p->device);
     cudaFree(p->d_budgets);
     cudaFree(p->d_kinds);
+    cudaFree(p->d_gran);
     cudaFree(p->d_wptr);
     cudaFree(p->d_items);
     cudaFree(p->d_scratch);
@@ -38,6 +39,7 @@ void free_device(sa_plan* p) {
   p->d_scratch = nullptr;
   p->d_budgets = nullptr;
   p->d_kinds = nullptr;
+  p->d_gran = nullptr;
   p->d_wptr = nullptr;
   p->d_items = nullptr;
   p->device = -1;
@@ -50,6 +52,22 @@ sa_status cuda_status(cudaError_t e) {
 }
 
 int64_t nblocks(const sa_shape* s) { return s->seq_len / s->block; }
+
+// Decode: the largest row a plan's selection handles, in blocks.
+int32_t decode_max_row(const sa_plan* p) {
+  int32_t row = p->nb;
+  for (size_t h = 0; h < p->gran.size(); ++h)
+    if (p->kinds[h] != SA_HEAD_STREAMING)
+      row = std::max(row, int32_t(p->shape.seq_len / p->gran[h]));
+  return row;
+}
+
+// Decode: whether any head selects at a size other than B.
+bool has_granularity(const sa_plan* p) {
+  for (int32_t g : p->gran)
+    if (g != p->shape.block) return true;
+  return false;
+}
 
 }  // namespace
 
@@ -64,8 +82,10 @@ sa_status sparse_attn_plan_upload(sa_plan* plan, sa_stream_t stream) {
   const size_t nh = plan->budgets.size();
   const size_t nw = plan->wptr.size();
   const size_t ni = plan->items.size();
+  const size_t ng = plan->gran.size();
   cudaError_t e = cudaMalloc(&plan->d_budgets, nh * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_kinds, nh);
+  if (e == cudaSuccess && ng) e = cudaMalloc(&plan->d_gran, ng * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_wptr, nw * sizeof(int32_t));
   if (e == cudaSuccess && ni) e = cudaMalloc(&plan->d_items, ni * sizeof(int32_t));
   plan->device = dev;
@@ -77,6 +97,9 @@ sa_status sparse_attn_plan_upload(sa_plan* plan, sa_stream_t stream) {
                       cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(plan->d_kinds, plan->kinds.data(), nh, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && ng)
+    e = cudaMemcpyAsync(plan->d_gran, plan->gran.data(), ng * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(plan->d_wptr, plan->wptr.data(), nw * sizeof(int32_t),
                         cudaMemcpyHostToDevice, st);
@@ -147,7 +170,9 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const flo
   if (!plan || !scores || !idx || !cnt) return SA_ERR_INVALID_ARG;
   if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
   if (kmax < plan->kmax) return SA_ERR_SHAPE;
-  if (plan->nb > 2048) return SA_ERR_UNSUPPORTED;
+  const bool decode = shp->mode == SA_MODE_DECODE;
+  const int32_t max_row = decode ? decode_max_row(plan) : plan->nb;
+  if (max_row > (decode ? 4096 : 2048)) return SA_ERR_UNSUPPORTED;
   if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
   sa_k::SelectArgs a;
   a.scores = scores;
@@ -164,6 +189,10 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const flo
   a.rows = a.decode ? shp->batch * shp->num_q_heads
                     : (plan->group_shared ? shp->num_kv_heads : shp->num_q_heads) * plan->nb;
   a.window_blocks = plan->window_blocks;
+  a.gran = decode ? plan->d_gran : nullptr;
+  a.L = int32_t(shp->seq_len);
+  a.stride = decode ? plan->score_stride : 0;
+  a.max_row = max_row;
   return cuda_status(sa_k::launch_select(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -236,6 +265,8 @@ sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const vo
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (shp->mode == SA_MODE_DECODE) {
     if (plan && !same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+    const bool sized = plan && has_granularity(plan);
+    if (sized && plan->device < 0) return SA_ERR_NOT_UPLOADED;
     sa_k::DecodeArgs a;
     a.q = q;
     a.k = k;
@@ -253,6 +284,7 @@ sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const vo
     a.out_f32 = o_dtype == SA_DTYPE_F32;
     a.lse = lse;
     a.dev_status = dev_status;
+    a.gran = sized ? plan->d_gran : nullptr;
     return cuda_status(sa_k::launch_decode_attention(a, st));
   }
   if (!plan) return SA_ERR_INVALID_ARG;
@@ -293,6 +325,49 @@ sa_status sparse_attn_pool_kcache(const sa_shape* shp, const void* k, float* kba
   const int64_t rows = int64_t(shp->batch) * shp->num_kv_heads * nblocks(shp);
   return cuda_status(sa_k::launch_pool(k, kbar, rows, shp->block, shp->head_dim,
                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_pool_kcache_plan(const sa_shape* shp, const sa_plan* plan, const void* k,
+                                       float* kbar_all, sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!plan || shp->mode != SA_MODE_DECODE) return SA_ERR_INVALID_ARG;
+  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+  if (!k || !kbar_all || !aligned16(k) || !aligned16(kbar_all)) return SA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* dst = kbar_all;
+  for (int32_t g : plan->sizes) {
+    const int64_t rows = int64_t(shp->batch) * shp->num_kv_heads * (shp->seq_len / g);
+    cudaError_t e = sa_k::launch_pool(k, dst, rows, g, shp->head_dim, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    dst += rows * shp->head_dim;
+  }
+  return SA_OK;
+}
+
+sa_status sparse_attn_score_plan(const sa_shape* shp, const sa_plan* plan, const void* q,
+                                 const float* kbar_all, float* scores, sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!plan || shp->mode != SA_MODE_DECODE) return SA_ERR_INVALID_ARG;
+  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+  if (!q || !kbar_all || !scores || !aligned16(q) || !aligned16(kbar_all) || !aligned16(scores))
+    return SA_ERR_INVALID_ARG;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int d = shp->head_dim;
+  const int G = shp->num_q_heads / shp->num_kv_heads;
+  const float scale = float(1.0 / std::sqrt(double(d)));
+  const float* src = kbar_all;
+  for (int32_t g : plan->sizes) {
+    const int nbg = int(shp->seq_len / g);
+    cudaError_t e = sa_k::launch_decode_scores(q, src, scores, shp->batch, shp->num_q_heads, G,
+                                               nbg, d, scale, st, plan->score_stride,
+                                               plan->d_kinds, plan->d_gran, g);
+    if (e != cudaSuccess) return cuda_status(e);
+    src += int64_t(shp->batch) * shp->num_kv_heads * nbg * d;
+  }
+  return SA_OK;
 }
 
 }  // extern "C"

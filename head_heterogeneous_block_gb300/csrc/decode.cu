@@ -1,15 +1,19 @@
 // Decode attention over the selected KV blocks (HBM-bound).
 //
-// One CTA per (sequence, query head), four warps.  Each warp takes every
-// fourth selected block.  Lane l owns dimensions [4l, 4l+4) of every key and
-// value row, so each row of the 32-token block is one coalesced 256-byte load
-// across the warp; key and value rows are loaded together before any
-// arithmetic (16 KB in flight per warp and block).  Every lane forms 32
-// partial dot products over its four dimensions; a reduce-scatter over the
-// warp (31 shuffles) leaves the score of token t in lane t, the warp keeps an
-// online softmax, and then accumulates P V in the same dimension layout.  The four partial states are merged by their
+// One CTA per (sequence, query head), four warps.  A head's selected blocks
+// are split into 16-token units (a block of g tokens is g/16 units; the
+// default B = 32 is two), and a step takes 32 rows: the 16 tokens of two
+// consecutive units.  Each warp takes every fourth step.  Lane l owns
+// dimensions [4l, 4l+4) of every key and value row, so each row is one
+// coalesced 256-byte load across the warp; key and value rows are loaded
+// together before any arithmetic (16 KB in flight per warp and step).  Every
+// lane forms 32 partial dot products over its four dimensions; a
+// reduce-scatter over the warp (31 shuffles) leaves the score of row t in
+// lane t, the warp keeps an online softmax, and then accumulates P V in the
+// same dimension layout.  The four partial states are merged by their
 // log-sum-exp.  Streaming and retrieval heads differ only in their block
-// lists ("Riepilogo Tecnico: Fluxion", "Intuizioni Chiave" 2).
+// lists, and retrieval heads may select at their own block size ("Riepilogo
+// Tecnico: Fluxion", "Intuizioni Chiave" 2).
 
 #include <cuda_bf16.h>
 
@@ -24,9 +28,10 @@ namespace {
 constexpr int kD = 128;
 constexpr int kB = 32;
 constexpr int kWarps = 4;
-static_assert(kB == 32 && kD == 4 * 32, "lane t <-> token t, lane l <-> dims [4l, 4l+4)");
+constexpr int kU = 16;       // tokens per unit; a step is two units
+static_assert(kB == 32 && kD == 4 * 32, "lane t <-> row t, lane l <-> dims [4l, 4l+4)");
 
-__global__ void __launch_bounds__(kWarps * 32) decode_attention_kernel(sa_k::DecodeArgs a,
+__global__ void __launch_bounds__(kWarps * 32, 4) decode_attention_kernel(sa_k::DecodeArgs a,
                                                                        float scale_log2) {
   __shared__ float sq[kD];
   __shared__ float sm[kWarps], sl[kWarps];
@@ -35,7 +40,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_attention_kernel(sa_k::Dec
   const int b = row / a.Hq, h = row % a.Hq;
   const int g = h / (a.Hq / a.Hkv);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = a.L / kB;
+  // this head's block size (a multiple of 16) and block count
+  int gsz = a.gran ? a.gran[h] : kB;
+  if (gsz < kU || (gsz % kU) != 0 || a.L % gsz != 0) gsz = kB;
+  const int per = gsz / kU;                   // units per block
+  const int nb = a.L / gsz;
 
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q) + size_t(row) * kD;
   for (int c = threadIdx.x; c < kD; c += kWarps * 32) sq[c] = __bfloat162float(q[c]);
@@ -54,20 +63,30 @@ __global__ void __launch_bounds__(kWarps * 32) decode_attention_kernel(sa_k::Dec
   float m = -INFINITY, l = 0.f;
   float o[4] = {0.f, 0.f, 0.f, 0.f};
   const float q4[4] = {sq[4 * lane], sq[4 * lane + 1], sq[4 * lane + 2], sq[4 * lane + 3]};
-  for (int t = warp; t < n; t += kWarps) {
-    int j = list[t];
+  const int units = n * per;
+  // first token of unit x: unit x % per of block list[x / per]
+  auto unit_start = [&](int x) -> size_t {
+    int j = list[x / per];
     if (j < 0 || j >= nb) {
       if (lane == 0) atomicOr(a.dev_status, SA_DEV_BAD_INDEX);
       j = 0;
     }
-    const uint2* kcol = reinterpret_cast<const uint2*>(K + size_t(j) * kB * kD) + lane;
-    const uint2* vcol = reinterpret_cast<const uint2*>(V + size_t(j) * kB * kD) + lane;
+    return size_t(j) * gsz + size_t(x % per) * kU;
+  };
+  for (int t = warp; 2 * t < units; t += kWarps) {
+    const size_t t0 = unit_start(2 * t);
+    const bool two = 2 * t + 1 < units;       // else rows 16..31 are masked
+    const size_t t1 = two ? unit_start(2 * t + 1) : t0;
+    const uint2* kc0 = reinterpret_cast<const uint2*>(K + t0 * kD) + lane;
+    const uint2* kc1 = reinterpret_cast<const uint2*>(K + t1 * kD) + lane;
+    const uint2* vc0 = reinterpret_cast<const uint2*>(V + t0 * kD) + lane;
+    const uint2* vc1 = reinterpret_cast<const uint2*>(V + t1 * kD) + lane;
     uint2 kv[kB], vv[kB];
 #pragma unroll
-    for (int u = 0; u < kB; ++u) kv[u] = __ldg(kcol + u * (kD / 4));
+    for (int u = 0; u < kB; ++u) kv[u] = __ldg(u < kU ? kc0 + u * (kD / 4) : kc1 + (u - kU) * (kD / 4));
 #pragma unroll
-    for (int u = 0; u < kB; ++u) vv[u] = __ldg(vcol + u * (kD / 4));
-    // partial dot products of token u over this lane's four dimensions
+    for (int u = 0; u < kB; ++u) vv[u] = __ldg(u < kU ? vc0 + u * (kD / 4) : vc1 + (u - kU) * (kD / 4));
+    // partial dot products of row u over this lane's four dimensions
     float part[kB];
 #pragma unroll
     for (int u = 0; u < kB; ++u) {
@@ -76,9 +95,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_attention_kernel(sa_k::Dec
       a = fmaf(__uint_as_float(kv[u].y << 16), q4[2], a);
       part[u] = fmaf(__uint_as_float(kv[u].y & 0xFFFF0000u), q4[3], a);
     }
-    // reduce-scatter: at width w each lane keeps the half of the tokens whose
+    // reduce-scatter: at width w each lane keeps the half of the rows whose
     // bit w matches its own and adds the partner's copy of that half; after
-    // five rounds lane t holds the full dot product of token t
+    // five rounds lane t holds the full dot product of row t
 #pragma unroll
     for (int w = kB / 2; w >= 1; w >>= 1) {
       const bool upper = (lane & w) != 0;
@@ -89,7 +108,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_attention_kernel(sa_k::Dec
         part[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
       }
     }
-    const float s = part[0] * scale_log2;
+    const float s = (two || lane < kU) ? part[0] * scale_log2 : -INFINITY;
     float mb = s;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));

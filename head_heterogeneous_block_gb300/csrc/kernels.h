@@ -17,9 +17,14 @@ cudaError_t launch_prefill_scores(const float* qbar, const float* kbar, float* s
                                   int group, int nb, int d, float scale, cudaStream_t st);
 
 // Decode scores [Bt][Hq][nb] from q [Bt][Hq][d] (bf16) and kbar [Bt][Hkv][nb][d].
+// nb pooled rows per (sequence, KV head) at this pass's block size; score
+// rows of `stride` floats (0: nb).  gran (device [Hq], with kinds) limits the
+// pass to the retrieval heads whose block size is `size`; NULL scores all.
 cudaError_t launch_decode_scores(const void* q, const float* kbar, float* scores, int Bt,
                                  int Hq, int group, int nb, int d, float scale,
-                                 cudaStream_t st);
+                                 cudaStream_t st, int stride = 0,
+                                 const uint8_t* kinds = nullptr,
+                                 const int32_t* gran = nullptr, int size = 0);
 
 struct SelectArgs {
   const float* scores;
@@ -35,6 +40,10 @@ struct SelectArgs {
   int32_t window_blocks;    // decode streaming heads
   int32_t group;            // G = Hq / Hkv
   int32_t group_shared;     // prefill: one row per (KV group, query block)
+  const int32_t* gran;      // decode: [Hq] device block size per head, or NULL
+  int32_t L;                // decode: cache length (rows of L / gran[h] blocks)
+  int32_t stride;           // decode: score row stride (0: nb)
+  int32_t max_row;          // largest row in blocks (picks the kernel width)
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
@@ -91,6 +100,7 @@ struct DecodeArgs {
   int32_t out_f32;
   float* lse;
   int32_t* dev_status;
+  const int32_t* gran;      // [Hq] device block size per head (multiple of 16), or NULL: B
 };
 cudaError_t launch_decode_attention(const DecodeArgs& a, cudaStream_t st);
 

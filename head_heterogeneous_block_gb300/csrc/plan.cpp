@@ -188,7 +188,7 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* p, sa_plan
     plan->k_uniform = p->k_uniform;
     plan->kinds.assign(H, SA_HEAD_RETRIEVAL);
     if (shp->mode == SA_MODE_PREFILL) {
-      if (p->head_kind) { delete plan; return SA_ERR_INVALID_ARG; }
+      if (p->head_kind || p->granularity || p->head_budget) { delete plan; return SA_ERR_INVALID_ARG; }
       if (p->num_workers < 1) { delete plan; return SA_ERR_INVALID_ARG; }
       if (p->group_shared != 0 && p->group_shared != 1) { delete plan; return SA_ERR_INVALID_ARG; }
       plan->budgets = sa_host::maxmin_shift(p->k_uniform, p->demand, H, p->k_min, nb);
@@ -231,15 +231,48 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* p, sa_plan
       }
       plan->window_blocks = p->window_blocks;
       plan->budgets.resize(H);
+      plan->gran.assign(H, shp->block);
+      // per-head selection block sizes and budgets of the retrieval heads
+      for (int32_t h = 0; h < H; ++h) {
+        if (plan->kinds[h] == SA_HEAD_STREAMING) continue;
+        if (p->granularity) {
+          const int32_t g = p->granularity[h];
+          if (g < 16 || g % 16 != 0 || shp->seq_len % g != 0 || shp->seq_len / g > 4096) {
+            delete plan;
+            return SA_ERR_INVALID_ARG;
+          }
+          plan->gran[h] = g;
+        }
+        if (p->head_budget && p->head_budget[h] < p->k_min) {
+          delete plan;
+          return SA_ERR_INVALID_ARG;
+        }
+      }
       // streaming: block 0 plus the last window_blocks blocks
       const int32_t stream_count = (nb - p->window_blocks > 0) ? p->window_blocks + 1 : nb;
       plan->kmax = 0;
       plan->total_blocks = 0;
       for (int32_t h = 0; h < H; ++h) {
-        plan->budgets[h] = plan->kinds[h] == SA_HEAD_STREAMING ? stream_count : p->k_uniform;
+        if (plan->kinds[h] == SA_HEAD_STREAMING) {
+          plan->budgets[h] = stream_count;
+        } else if (p->granularity || p->head_budget) {
+          const int32_t nbh = int32_t(shp->seq_len / plan->gran[h]);
+          plan->budgets[h] = std::min(p->head_budget ? p->head_budget[h] : p->k_uniform, nbh);
+        } else {
+          plan->budgets[h] = p->k_uniform;
+        }
         plan->kmax = std::max(plan->kmax, plan->budgets[h]);
         plan->total_blocks += int64_t(plan->budgets[h]) * shp->batch;
       }
+      for (int32_t h = 0; h < H; ++h)
+        if (plan->kinds[h] != SA_HEAD_STREAMING) plan->sizes.push_back(plan->gran[h]);
+      std::sort(plan->sizes.begin(), plan->sizes.end());
+      plan->sizes.erase(std::unique(plan->sizes.begin(), plan->sizes.end()), plan->sizes.end());
+      if (plan->sizes.size() > 8) {
+        delete plan;
+        return SA_ERR_INVALID_ARG;
+      }
+      plan->score_stride = plan->sizes.empty() ? nb : int32_t(shp->seq_len / plan->sizes[0]);
       plan->num_workers = 0;
       plan->wptr.assign(1, 0);
       plan->makespan = 0;
@@ -263,6 +296,22 @@ sa_status sparse_attn_plan_info(const sa_plan* plan, int32_t* num_workers, int32
   if (kmax) *kmax = plan->kmax;
   if (total_blocks) *total_blocks = plan->total_blocks;
   if (makespan) *makespan = plan->makespan;
+  return SA_OK;
+}
+
+sa_status sparse_attn_plan_decode_layout(const sa_plan* plan, int32_t* num_sizes,
+                                         int32_t* sizes, int64_t* kcache_floats,
+                                         int32_t* score_stride) {
+  if (!plan || plan->shape.mode != SA_MODE_DECODE) return SA_ERR_INVALID_ARG;
+  const sa_shape& s = plan->shape;
+  int64_t floats = 0;
+  for (int32_t g : plan->sizes)
+    floats += int64_t(s.batch) * s.num_kv_heads * (s.seq_len / g) * s.head_dim;
+  if (num_sizes) *num_sizes = int32_t(plan->sizes.size());
+  if (sizes)
+    for (size_t i = 0; i < plan->sizes.size() && i < 8; ++i) sizes[i] = plan->sizes[i];
+  if (kcache_floats) *kcache_floats = floats;
+  if (score_stride) *score_stride = plan->score_stride;
   return SA_OK;
 }
 

@@ -20,6 +20,11 @@ struct sa_plan {
   int64_t makespan = 0;
   std::vector<int32_t> budgets;   // [Hq]
   std::vector<uint8_t> kinds;     // [Hq]
+  // decode: tokens per selection block of each head (streaming heads: B), the
+  // distinct sizes of the retrieval heads (ascending) and the score row stride
+  std::vector<int32_t> gran;      // [Hq]
+  std::vector<int32_t> sizes;
+  int32_t score_stride = 0;
   std::vector<int32_t> wptr;      // [W+1]
   std::vector<int32_t> items;     // [N]
   std::vector<int64_t> loads;     // [W]
@@ -27,6 +32,7 @@ struct sa_plan {
   int device = -1;
   int32_t* d_budgets = nullptr;
   uint8_t* d_kinds = nullptr;
+  int32_t* d_gran = nullptr;      // decode: [Hq]
   int32_t* d_wptr = nullptr;
   int32_t* d_items = nullptr;
   int32_t* d_scratch = nullptr;   // sparse_attn_plan_rebuild: 3N int32

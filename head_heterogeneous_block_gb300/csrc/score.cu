@@ -10,15 +10,21 @@
 //                  64x64 fp32 SIMT tile per CTA over the lower triangle (the
 //                  contraction is small -- d = 128 -- and selection needs fp32
 //                  accuracy, so no reduced-precision tensor path).
-// decode_scores    scores[b,h,j] = q[b,h] . kbar[b,g,j] * scale; a warp takes
-//                  16 pooled key rows (coalesced, all in flight) for all G
-//                  query heads of the group and reduces with a reduce-scatter.
+// decode_scores    scores[b,h,j] = q[b,h] . kbar[b,g,j] * scale; persistent
+//                  CTAs stream 32 KB chunks of pooled keys through a
+//                  three-stage cp.async ring while scoring earlier chunks; a
+//                  warp scores 16 rows for all G query heads of the group
+//                  with tf32 tensor-core MMAs (split in two for fp32-level
+//                  accuracy).  With per-head block sizes, one pass per
+//                  size scores the retrieval heads of that size; a group with
+//                  none of them is skipped without reading its cache.
 
 #include <cuda_bf16.h>
 
 #include <cstdint>
 
 #include "kernels.h"
+#include "sparse_attn.h"
 
 namespace {
 
@@ -118,59 +124,177 @@ __global__ void __launch_bounds__(256) prefill_scores_kernel(const float* __rest
   }
 }
 
-// CTA = (128 pooled rows, kv head g, sequence b); 8 warps of 16 rows.  D = 128.
+// Decode scores, persistent: two CTAs per SM walk chunks of 64 pooled key
+// rows of one (sequence, KV head), c = blockIdx.x, + gridDim.x, ...  Each
+// chunk (32 KB of pooled keys and the group's query rows) is copied into a
+// three-stage shared-memory ring with cp.async while the previous chunks are
+// scored, so the loads of one chunk overlap the arithmetic of the others.
+// The scores of a chunk are a small dense product, [64 rows x 128] x
+// [128 x G heads]: warp w takes rows [16w, 16w+16) and runs it on the tensor
+// cores as m16n8k8 tf32 MMAs (rows x 8 heads per tile, fp32 accumulation).
+// A pooled key x is split into x_hi (x with its 13 low mantissa bits cleared,
+// a tf32 value) and x_lo = x - x_hi (exact in fp32; the MMA reads its top
+// tf32 bits), and both are multiplied by the query (bf16, exact in tf32) into
+// separate accumulators, so the products keep about 20 bits of x -- fp32-level
+// scores.  The k order inside an MMA is
+// permuted (lane t of a quad takes dimensions 16m + 4t .. +4, two k-steps),
+// and a row's 16-byte chunks are stored XOR-swizzled by the row, so every
+// shared-memory read is conflict-free.  D = 128.
 constexpr int kMaxGroup = 16;
+constexpr int kRows = 64;                     // pooled rows per chunk
+constexpr int kStages = 3;
+constexpr int kScoreThreads = 128;
+constexpr int kScoreCtasPerSm = 2;
+constexpr int kMaxKvHeads = 256;              // per-group head masks kept in shared memory
 
-__global__ void __launch_bounds__(256) decode_scores_kernel(const __nv_bfloat16* __restrict__ q,
-                                                            const float* __restrict__ kbar,
-                                                            float* __restrict__ scores, int Hq,
-                                                            int Hkv, int group, int nb,
-                                                            float scale) {
-  // Each warp scores 16 pooled key rows against every query head of the KV
-  // group.  Lane l holds dimensions [4(l%32).. ) of each row -- one coalesced
-  // 512-byte load per row, 16 rows in flight -- and forms partial dot products;
-  // a reduce-scatter over the 16 lanes of each half-warp (15 shuffles) and one
-  // exchange between the halves leave row r's score in lanes r and r + 16.
-  constexpr int D = 128, R = 16;
-  __shared__ float sq[kMaxGroup][D];
-  const int b = blockIdx.z, g = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int e = threadIdx.x; e < group * D; e += 256) {
-    const int hh = e / D, c = e % D;
-    sq[hh][c] = __bfloat162float(q[(size_t(b) * Hq + g * group + hh) * D + c]);
-  }
-  __syncthreads();
-  const float4* kb = reinterpret_cast<const float4*>(kbar + (size_t(b) * Hkv + g) * nb * D);
-  const int j0 = (blockIdx.x * 8 + warp) * R;
-  if (j0 >= nb) return;
-  float4 kv[R];
-#pragma unroll
-  for (int u = 0; u < R; ++u) {
-    const int j = min(j0 + u, nb - 1);        // rows past nb are read (in range) and not stored
-    kv[u] = __ldg(&kb[size_t(j) * (D / 4) + lane]);
-  }
-  for (int hh = 0; hh < group; ++hh) {
-    const float4 q4 = *reinterpret_cast<const float4*>(&sq[hh][lane * 4]);
-    float part[R];
-#pragma unroll
-    for (int u = 0; u < R; ++u)
-      part[u] = fmaf(kv[u].x, q4.x, fmaf(kv[u].y, q4.y, fmaf(kv[u].z, q4.z, kv[u].w * q4.w)));
-#pragma unroll
-    for (int w = R / 2; w >= 1; w >>= 1) {
-      const bool upper = (lane & w) != 0;
-#pragma unroll
-      for (int i = 0; i < w; ++i) {
-        const float send = upper ? part[i] : part[i + w];
-        const float keep = upper ? part[i + w] : part[i];
-        part[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-      }
-    }
-    const float sc = part[0] + __shfl_xor_sync(0xffffffffu, part[0], 16);
-    const int j = j0 + (lane & (R - 1));
-    if (lane < R && j < nb) scores[(size_t(b) * Hq + g * group + hh) * nb + j] = sc * scale;
-  }
+struct ScoreStage {
+  float4 k[kRows][32];                        // 64 rows x 128 floats, chunks swizzled
+  uint2 q[kMaxGroup][32];                     // the group's queries, bf16
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_2() {
+  asm volatile("cp.async.wait_group 2;" ::: "memory");
+}
+// 16-byte chunk c of row r sits at c ^ 4(r mod 8)
+__device__ __forceinline__ int swz(int r, int c) { return c ^ ((r & 7) << 2); }
+
+// x = hi + lo with hi a tf32 value (the 10 leading mantissa bits of x)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xFFFFE000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
 }
 
+// D += A . B for one m16n8k8 tile (A 16x8 row-major, B 8x8 column-major, tf32)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
+    decode_scores_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ kbar,
+                         float* __restrict__ scores, int Bt, int Hq, int Hkv, int group, int nb,
+                         int stride, float scale, const uint8_t* __restrict__ kinds,
+                         const int32_t* __restrict__ gran, int size) {
+  constexpr int D = 128;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  ScoreStage* st = reinterpret_cast<ScoreStage*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, tq = lane & 3;    // MMA fragment coordinates
+  const int per = (nb + kRows - 1) / kRows;   // chunks per (sequence, KV head)
+  const int total = Bt * Hkv * per;
+  // each group's heads this pass scores: all, or the retrieval heads of `size`
+  __shared__ uint32_t gmask[kMaxKvHeads];
+  for (int g = tid; g < Hkv; g += kScoreThreads) {
+    uint32_t m = 0;
+    for (int hh = 0; hh < group; ++hh) {
+      const int h = g * group + hh;
+      if (!gran || (kinds[h] != SA_HEAD_STREAMING && gran[h] == size)) m |= 1u << hh;
+    }
+    gmask[g] = m;
+  }
+  __syncthreads();
+  // the CTA's chunks in order, those of groups with no head to score skipped
+  auto next_chunk = [&](int c) -> int {
+    if (c >= total) return total;
+    for (c += gridDim.x; c < total; c += gridDim.x)
+      if (gmask[(c / per) % Hkv]) return c;
+    return total;
+  };
+  auto issue = [&](int c, int s) {
+    if (c < total) {
+      const int bg = c / per, r0 = (c - bg * per) * kRows;
+      const int rows = min(kRows, nb - r0);
+      const float4* src = reinterpret_cast<const float4*>(kbar + (size_t(bg) * nb + r0) * D);
+      for (int e = tid; e < rows * 32; e += kScoreThreads) {
+        const int r = e >> 5;
+        cp_async16(&st[s].k[r][swz(r, e & 31)], src + e);
+      }
+      const int b = bg / Hkv, g = bg - b * Hkv;
+      const uint2* qs = reinterpret_cast<const uint2*>(q + (size_t(b) * Hq + g * group) * D);
+      for (int e = tid; e < group * 32; e += kScoreThreads)
+        cp_async8(&st[s].q[e >> 5][e & 31], qs + e);
+    }
+    cp_async_commit();                        // empty groups keep the count uniform
+  };
+  // chunk k of this CTA's sequence goes to stage k % 3; cur, nx1 are chunks
+  // k and k + 1 (already issued), nx2 is issued into stage (k + 2) % 3
+  int cur = next_chunk(int(blockIdx.x) - int(gridDim.x));
+  int nx1 = next_chunk(cur);
+  issue(cur, 0);
+  issue(nx1, 1);
+  for (int k = 0; cur < total; ++k) {
+    const int nx2 = next_chunk(nx1);
+    issue(nx2, (k + 2) % kStages);
+    cp_async_wait_2();                        // this thread's copies of chunk k landed
+    __syncthreads();                          // ... and every thread's
+    const ScoreStage& sg = st[k % kStages];
+    const int bg = cur / per, r0 = (cur - bg * per) * kRows;
+    const int b = bg / Hkv, g = bg - b * Hkv;
+    const uint32_t hmask = gmask[g];
+    const int ra = 16 * warp + gq;            // this lane's rows: ra and ra + 8
+    if (r0 + 16 * warp < nb) {
+      for (int n0 = 0; n0 < group; n0 += 8) { // 8 heads per tile
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acl[4] = {0.f, 0.f, 0.f, 0.f};
+        const int hn = n0 + gq;               // the head of this lane's B column
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {         // dimensions 16m .. 16m + 16: two k-steps
+          const float4 xa = sg.k[ra][swz(ra, 4 * m + tq)];
+          const float4 xb = sg.k[ra + 8][swz(ra + 8, 4 * m + tq)];
+          uint2 qb = make_uint2(0u, 0u);
+          if (hn < group) qb = sg.q[hn][4 * m + tq];
+          const uint32_t q0 = qb.x << 16, q1 = qb.x & 0xFFFF0000u;
+          const uint32_t q2 = qb.y << 16, q3 = qb.y & 0xFFFF0000u;
+          uint32_t hi[4], lo[4];
+          // k-step 2m: dimensions +0 (k = t) and +1 (k = t + 4)
+          split_tf32(xa.x, hi[0], lo[0]);
+          split_tf32(xb.x, hi[1], lo[1]);
+          split_tf32(xa.y, hi[2], lo[2]);
+          split_tf32(xb.y, hi[3], lo[3]);
+          mma_tf32(acc, hi, q0, q1);
+          mma_tf32(acl, lo, q0, q1);
+          // k-step 2m + 1: dimensions +2 and +3
+          split_tf32(xa.z, hi[0], lo[0]);
+          split_tf32(xb.z, hi[1], lo[1]);
+          split_tf32(xa.w, hi[2], lo[2]);
+          split_tf32(xb.w, hi[3], lo[3]);
+          mma_tf32(acc, hi, q2, q3);
+          mma_tf32(acl, lo, q2, q3);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += acl[e];
+        // acc: rows ra (0, 1) and ra + 8 (2, 3), heads n0 + 2t and n0 + 2t + 1
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int hh = n0 + 2 * tq + (e & 1);
+          const int j = r0 + ra + ((e & 2) ? 8 : 0);
+          if (hh < group && ((hmask >> hh) & 1u) && j < nb)
+            scores[(size_t(b) * Hq + g * group + hh) * stride + j] = acc[e] * scale;
+        }
+      }
+    }
+    __syncthreads();                          // stage k % 3 is free for chunk k + 3
+    cur = nx1;
+    nx1 = nx2;
+  }
+}
 }  // namespace
 
 namespace sa_k {
@@ -197,12 +321,28 @@ cudaError_t launch_prefill_scores(const float* qbar, const float* kbar, float* s
 }
 
 cudaError_t launch_decode_scores(const void* q, const float* kbar, float* scores, int Bt, int Hq,
-                                 int group, int nb, int d, float scale, cudaStream_t st) {
+                                 int group, int nb, int d, float scale, cudaStream_t st,
+                                 int stride, const uint8_t* kinds, const int32_t* gran,
+                                 int size) {
   if (d != 128 || group > kMaxGroup) return cudaErrorInvalidValue;
-  // 8 warps x 16 rows per CTA
-  const dim3 grid(unsigned((nb + 127) / 128), unsigned(Hq / group), unsigned(Bt));
-  decode_scores_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(q), kbar, scores,
-                                             Hq, Hq / group, group, nb, scale);
+  if (gran && !kinds) return cudaErrorInvalidValue;
+  const int Hkv = Hq / group;
+  if (Hkv > kMaxKvHeads) return cudaErrorInvalidValue;
+  const long long chunks = (long long)Bt * Hkv * ((nb + kRows - 1) / kRows);
+  if (chunks == 0) return cudaSuccess;
+  if (chunks >= (1ll << 30)) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int smem = int(kStages * sizeof(ScoreStage));
+  e = cudaFuncSetAttribute(decode_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long slots = (long long)sms * kScoreCtasPerSm;
+  const int grid = int(chunks < slots ? chunks : slots);
+  decode_scores_kernel<<<grid, kScoreThreads, smem, st>>>(
+      static_cast<const __nv_bfloat16*>(q), kbar, scores, Bt, Hq, Hkv, group, nb,
+      stride > 0 ? stride : nb, scale, kinds, gran, size);
   return cudaGetLastError();
 }
 

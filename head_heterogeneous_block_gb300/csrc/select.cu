@@ -18,6 +18,7 @@
 // scan, only when ties straddle the threshold).  Kept blocks are marked in a
 // bitmap and written in ascending order with warp ballots.
 
+#include <algorithm>
 #include <cstdint>
 
 #include "kernels.h"
@@ -34,20 +35,25 @@ __device__ __forceinline__ uint32_t order_bits(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
-  __shared__ uint32_t bits[kMaxWords];
+// kT threads with kPer candidates each: rows of up to kPer * kT blocks.
+template <int kT, int kPer>
+__global__ void __launch_bounds__(kT) select_kernel(sa_k::SelectArgs a) {
+  __shared__ uint32_t bits[kPer * kT / 32];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t ctl[4];
-  __shared__ uint32_t wsum[kThreads / 32];
+  __shared__ uint32_t wsum[kT / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
 
   int h, i, G = 1;
   const float* srow;
   if (a.decode) {
+    // a retrieval head's row has L / g_h blocks of its own size g_h
     h = row % a.Hq;
-    i = a.nb - 1;
-    srow = a.scores + size_t(row) * a.nb;
+    const int gsz = a.gran ? a.gran[h] : 0;
+    const int nbh = (gsz > 0 && a.kinds[h] != SA_HEAD_STREAMING) ? a.L / gsz : a.nb;
+    i = min(nbh, kPer * kT) - 1;
+    srow = a.scores + size_t(row) * (a.stride > 0 ? a.stride : a.nb);
   } else if (a.group_shared) {
     G = a.group;
     const int g = row / a.nb;
@@ -62,38 +68,38 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
   const size_t head_stride = size_t(a.nb) * a.nb;   // between heads' score rows
   const bool streaming = a.decode && a.kinds[h] == SA_HEAD_STREAMING;
   const int nwords = (i + 1 + 31) / 32;
-  for (int w = tid; w < nwords; w += kThreads) bits[w] = 0u;
+  for (int w = tid; w < nwords; w += kT) bits[w] = 0u;
   __syncthreads();
 
   if (streaming) {
     const int lo = max(1, a.nb - a.window_blocks);
-    for (int j = tid; j <= i; j += kThreads)
+    for (int j = tid; j <= i; j += kT)
       if (j == 0 || j >= lo) atomicOr(&bits[j >> 5], 1u << (j & 31));
   } else {
     const int keep = min(a.budgets[h], i + 1);
     const int rest = keep - ((i == 0) ? 1 : 2);
     const int ncand = max(0, i - 1);          // blocks 1..i-1
     if (rest >= ncand) {
-      for (int j = tid; j <= i; j += kThreads) atomicOr(&bits[j >> 5], 1u << (j & 31));
+      for (int j = tid; j <= i; j += kT) atomicOr(&bits[j >> 5], 1u << (j & 31));
     } else {
       if (tid == 0) {
         atomicOr(&bits[0], 1u);
         atomicOr(&bits[i >> 5], 1u << (i & 31));
       }
       if (rest > 0) {
-        uint32_t u[kPerThread];
+        uint32_t u[kPer];
         if (G == 1) {
           // all of a thread's candidate loads in flight together
 #pragma unroll
-          for (int r = 0; r < kPerThread; ++r) {
-            const int j = 1 + tid + r * kThreads;
+          for (int r = 0; r < kPer; ++r) {
+            const int j = 1 + tid + r * kT;
             u[r] = (j <= i - 1) ? order_bits(srow[j]) : 0u;
           }
         } else {
           // group-shared rows rank by the sum of the group's heads' scores
 #pragma unroll
-          for (int r = 0; r < kPerThread; ++r) {
-            const int j = 1 + tid + r * kThreads;
+          for (int r = 0; r < kPer; ++r) {
+            const int j = 1 + tid + r * kT;
             float sc = 0.f;
             if (j <= i - 1)
               for (int x = 0; x < G; ++x) sc += srow[x * head_stride + j];
@@ -102,12 +108,24 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
         }
         uint32_t prefix = 0, mask = 0, need = uint32_t(rest), eq_total = 0;
         for (int shift = 24; shift >= 0; shift -= 8) {
-          for (int b = tid; b < 256; b += kThreads) hist[b] = 0u;
+          for (int b = tid; b < 256; b += kT) hist[b] = 0u;
           __syncthreads();
+          if (kT > 128 && shift == 24) {
+            // the top byte (sign and high exponent bits) puts most scores in
+            // a few bins: one atomic per bin and warp instead of per lane
 #pragma unroll
-          for (int r = 0; r < kPerThread; ++r) {
-            const int j = 1 + tid + r * kThreads;
-            if (j <= i - 1 && (u[r] & mask) == prefix) atomicAdd(&hist[(u[r] >> shift) & 255u], 1u);
+            for (int r = 0; r < kPer; ++r) {
+              const int j = 1 + tid + r * kT;
+              const uint32_t bin = j <= i - 1 ? (u[r] >> 24) : 256u;
+              const uint32_t same = __match_any_sync(0xffffffffu, bin);
+              if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
+            }
+          } else {
+#pragma unroll
+            for (int r = 0; r < kPer; ++r) {
+              const int j = 1 + tid + r * kT;
+              if (j <= i - 1 && (u[r] & mask) == prefix) atomicAdd(&hist[(u[r] >> shift) & 255u], 1u);
+            }
           }
           __syncthreads();
           if (warp == 0) {
@@ -151,15 +169,15 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
         if (eq_total == need) {
           // every candidate >= T is kept
 #pragma unroll
-          for (int r = 0; r < kPerThread; ++r) {
-            const int j = 1 + tid + r * kThreads;
+          for (int r = 0; r < kPer; ++r) {
+            const int j = 1 + tid + r * kT;
             if (j <= i - 1 && u[r] >= T) atomicOr(&bits[j >> 5], 1u << (j & 31));
           }
         } else {
           // ties straddle the threshold: above T all, equal to T by index
           uint32_t taken = 0;
-          for (int r = 0; r < kPerThread; ++r) {
-            const int j = 1 + tid + r * kThreads;
+          for (int r = 0; r < kPer; ++r) {
+            const int j = 1 + tid + r * kT;
             const bool valid = j <= i - 1;
             const bool eq = valid && u[r] == T;
             const uint32_t m = __ballot_sync(0xffffffffu, eq);
@@ -170,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(sa_k::SelectArgs a) {
             before += __popc(m & ((1u << lane) - 1u));
             if (valid && (u[r] > T || (eq && before < need)))
               atomicOr(&bits[j >> 5], 1u << (j & 31));
-            for (int w = 0; w < kThreads / 32; ++w) taken += wsum[w];
+            for (int w = 0; w < kT / 32; ++w) taken += wsum[w];
             __syncthreads();
           }
         }
@@ -445,8 +463,16 @@ cudaError_t launch_select_topp(const TopPArgs& a, cudaStream_t st) {
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
-  if (a.nb > kPerThread * kThreads) return cudaErrorInvalidValue;
-  select_kernel<<<unsigned(a.rows), kThreads, 0, st>>>(a);
+  // decode launches few rows (sequences x heads): wider CTAs per row
+  const int row = std::max(a.nb, a.max_row);
+  if (!a.decode && row <= 16 * kThreads)
+    select_kernel<kThreads, 16><<<unsigned(a.rows), kThreads, 0, st>>>(a);
+  else if (a.decode && row <= 4 * 512)
+    select_kernel<512, 4><<<unsigned(a.rows), 512, 0, st>>>(a);
+  else if (a.decode && row <= 8 * 512)
+    select_kernel<512, 8><<<unsigned(a.rows), 512, 0, st>>>(a);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

@@ -12,7 +12,8 @@ from __future__ import annotations
 import torch
 
 from . import (Shape, sparse_attn_forward, sparse_attn_plan, sparse_attn_pool_kcache,
-               sparse_attn_score, sparse_attn_score_workspace_size, sparse_attn_select)
+               sparse_attn_pool_kcache_plan, sparse_attn_score, sparse_attn_score_plan,
+               sparse_attn_score_workspace_size, sparse_attn_select)
 
 
 class PrefillLayer:
@@ -60,18 +61,28 @@ class PrefillLayer:
 
 
 class DecodeStep:
+    """One decode step: pooled key cache (built once), scores, selection and
+    attention.  With ``granularity`` (and ``head_budget``) each retrieval head
+    selects ``head_budget[h]`` blocks of ``granularity[h]`` tokens."""
+
     def __init__(self, shape: Shape, budget_blocks: int, head_kind, window_blocks: int,
-                 device="cuda", with_lse: bool = False, out_dtype=torch.bfloat16):
+                 device="cuda", with_lse: bool = False, out_dtype=torch.bfloat16,
+                 granularity=None, head_budget=None):
         dev = torch.device(device)
         self.shape = shape
         self.plan = sparse_attn_plan(shape, budget_blocks, head_kind=head_kind,
-                                     window_blocks=window_blocks, num_workers=1)
+                                     window_blocks=window_blocks, num_workers=1,
+                                     granularity=granularity, head_budget=head_budget)
         self.plan.upload()
         self.kmax = self.plan.info()["kmax"]
+        self.sized = granularity is not None
+        layout = self.plan.decode_layout()
+        self.score_stride = layout["score_stride"]
         Bt, H, Hkv, nb, d = (shape.batch, shape.num_q_heads, shape.num_kv_heads, shape.nb,
                              shape.head_dim)
-        self.kbar = torch.empty(Bt * Hkv * nb * d, dtype=torch.float32, device=dev)
-        self.scores = torch.empty(Bt * H * nb, dtype=torch.float32, device=dev)
+        kfloats = max(1, layout["kcache_floats"]) if self.sized else Bt * Hkv * nb * d
+        self.kbar = torch.empty(kfloats, dtype=torch.float32, device=dev)
+        self.scores = torch.empty(Bt * H * self.score_stride, dtype=torch.float32, device=dev)
         self.idx = torch.empty(Bt * H * self.kmax, dtype=torch.int32, device=dev)
         self.cnt = torch.empty(Bt * H, dtype=torch.int32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -79,11 +90,17 @@ class DecodeStep:
         self.out = torch.empty(Bt, H, d, dtype=out_dtype, device=dev)
 
     def build_cache(self, k, stream=None):
-        sparse_attn_pool_kcache(self.shape, k, self.kbar, stream=stream)
+        if self.sized:
+            sparse_attn_pool_kcache_plan(self.shape, self.plan, k, self.kbar, stream=stream)
+        else:
+            sparse_attn_pool_kcache(self.shape, k, self.kbar, stream=stream)
 
     def __call__(self, q, k, v, out=None, stream=None):
         out = self.out if out is None else out
-        sparse_attn_score(self.shape, q, self.kbar, self.scores, None, 0, stream=stream)
+        if self.sized:
+            sparse_attn_score_plan(self.shape, self.plan, q, self.kbar, self.scores, stream=stream)
+        else:
+            sparse_attn_score(self.shape, q, self.kbar, self.scores, None, 0, stream=stream)
         sparse_attn_select(self.shape, self.plan, self.scores, self.idx, self.cnt, self.kmax,
                            stream=stream)
         sparse_attn_forward(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax, out,

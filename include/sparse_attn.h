@@ -124,6 +124,19 @@ typedef struct sa_plan_params {
                                largest of their budgets.  Must be 0 for decode.
                                (Fluxion, "Intuizioni Chiave": group-level KV
                                access.)                                      */
+  const int32_t* granularity; /* decode: [Hq] tokens per selection block of each
+                               retrieval head: a multiple of 16 that divides L,
+                               with L / g <= 4096, at most 8 distinct sizes;
+                               NULL = B for every head.
+                               Streaming heads' entries are ignored (they keep
+                               blocks of B).  Must be NULL for prefill.
+                               ("Riepilogo Tecnico: Fluxion", "Intuizioni
+                               Chiave" 2: block size and budget chosen per
+                               retrieval head.)                              */
+  const int32_t* head_budget; /* decode: [Hq] blocks each retrieval head keeps,
+                               at its own block size, >= k_min (capped at its
+                               block count); NULL = k_uniform.  Must be NULL
+                               for prefill.                                   */
 } sa_plan_params;
 
 typedef struct sa_plan sa_plan;
@@ -142,12 +155,14 @@ const char* sa_status_string(sa_status status);
  * to the least-loaded worker (ties: lowest worker); LPT_GROUPED walks KV
  * group by KV group, cost descending inside a group; HEAD_ORDER gives worker
  * w the contiguous id range [w*N/W, (w+1)*N/W).
- * Decode: retrieval heads keep k_uniform blocks, streaming heads block 0
- * plus the last window_blocks blocks; no schedule is built.
+ * Decode: retrieval heads keep k_uniform blocks (or head_budget[h] blocks of
+ * granularity[h] tokens), streaming heads block 0 plus the last window_blocks
+ * blocks of B; no schedule is built.
  * On success *out owns a new plan (free with sparse_attn_plan_destroy).
  * Errors: INVALID_ARG (null shp/params/out, bad enum, k_min < 2, k_uniform
- * out of [k_min, max(nb, k_min)], W < 1, negative demand), SHAPE, UNSUPPORTED,
- * NO_MEMORY.  *out is left untouched on error.
+ * out of [k_min, max(nb, k_min)], W < 1, negative demand, a decode-only field
+ * given for prefill, a bad granularity or a head budget < k_min), SHAPE,
+ * UNSUPPORTED, NO_MEMORY.  *out is left untouched on error.
  */
 sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* params,
                            sa_plan** out);
@@ -161,6 +176,21 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* params,
 sa_status sparse_attn_plan_info(const sa_plan* plan, int32_t* num_workers,
                                 int32_t* num_items, int32_t* kmax,
                                 int64_t* total_blocks, int64_t* makespan);
+
+/*
+ * Decode plans: the block sizes their retrieval heads select at.
+ * num_sizes, sizes[0..num_sizes) (ascending, at most 8 entries are written):
+ *   the distinct block sizes of the retrieval heads (B when the plan has no
+ *   granularity; none when every head streams);
+ * kcache_floats: floats of the pooled key caches those sizes need together,
+ *   sum over sizes g of Bt*Hkv*(L/g)*d (see sparse_attn_pool_kcache_plan);
+ * score_stride: the row stride of decode scores, L / sizes[0] (nb when there
+ *   are no retrieval heads).  Any output may be NULL.
+ * Errors: INVALID_ARG (NULL plan, prefill plan).
+ */
+sa_status sparse_attn_plan_decode_layout(const sa_plan* plan, int32_t* num_sizes,
+                                         int32_t* sizes, int64_t* kcache_floats,
+                                         int32_t* score_stride);
 
 /*
  * Copy a plan's contents to host arrays (any may be NULL):
@@ -236,8 +266,11 @@ sa_status sparse_attn_score_noalloc(const sa_shape* shp, const void* q, const vo
 /*
  * Select: for prefill row (h, i) keep min(k_h, i+1) blocks: 0 and i always,
  * then the highest-scoring of 1..i-1, ties to the lower index.  For decode
- * retrieval heads the row is i = nb-1 with k_h = k_uniform; streaming heads
- * get block 0 and the last window_blocks blocks.
+ * retrieval heads the row is i = nb_h - 1 with k_h the head's budget, nb_h =
+ * L / granularity[h] blocks (nb without a granularity) and score rows of the
+ * plan's score_stride floats (nb without a granularity); streaming heads get
+ * block 0 and the last window_blocks blocks of B.  Decode rows of up to 4096
+ * blocks are supported.
  * Group-shared plans (sa_plan_params.group_shared = 1, prefill): one list per
  * (KV group g, row i), chosen as above on the sum over the group's G heads of
  * their scores (the order of their mean) with the group's budget, and written
@@ -245,7 +278,7 @@ sa_status sparse_attn_score_noalloc(const sa_shape* shp, const void* q, const vo
  * Outputs: idx [rows][kmax] int32, each row ascending and padded with -1;
  * cnt [rows] int32; rows = Hq*nb (prefill, row h*nb+i) or Bt*Hq (decode,
  * row b*Hq+h).  kmax must be >= the plan's kmax (sparse_attn_plan_info).
- * Rows of up to 2048 blocks are supported (nb <= 2048), else UNSUPPORTED.
+ * Prefill rows of up to 2048 blocks are supported (nb <= 2048), else UNSUPPORTED.
  * Errors: INVALID_ARG, SHAPE (kmax too small, shape differs from the plan's),
  * UNSUPPORTED, NOT_UPLOADED, CUDA.
  */
@@ -306,7 +339,9 @@ sa_status sparse_attn_plan_device_schedule(const sa_plan* plan, int32_t* wptr,
  *   output row is a convex combination of value rows.
  *   Runs as a persistent kernel: one CTA per plan worker, walking that
  *   worker's items in order (sm_103a: TMA loads, tcgen05 MMAs into TMEM).
- * Decode: o[b,h] over the blocks of row b*Hq+h; plan may be NULL.
+ * Decode: o[b,h] over the blocks of row b*Hq+h, block j of head h covering
+ *   tokens [j*g_h, (j+1)*g_h) with g_h = granularity[h] of the plan (B when
+ *   the plan has none, or when plan is NULL).
  * o_dtype: SA_DTYPE_BF16 (round to nearest even) or SA_DTYPE_F32.
  * lse (nullable): natural-log sum of exponentials per query row, fp32,
  *   [Hq][S] (prefill) or [Bt][Hq] (decode).
@@ -329,6 +364,30 @@ sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan,
  */
 sa_status sparse_attn_pool_kcache(const sa_shape* shp, const void* k,
                                   float* kbar, sa_stream_t stream);
+
+/*
+ * Decode with per-head block sizes: the pooled key caches of every size the
+ * plan's retrieval heads use, one after the other in ascending size, each
+ * fp32 [Bt][Hkv][L/g][d] (the mean of the g keys of each block), into kbar_all
+ * (sparse_attn_plan_decode_layout gives the total floats).  Once per cache.
+ * Errors: INVALID_ARG (NULL, prefill plan), SHAPE (shape differs from the
+ * plan's), UNSUPPORTED, CUDA.
+ */
+sa_status sparse_attn_pool_kcache_plan(const sa_shape* shp, const sa_plan* plan,
+                                       const void* k, float* kbar_all,
+                                       sa_stream_t stream);
+
+/*
+ * Decode with per-head block sizes: scores[b][h][j] = q[b,h] . kbar_g[b,h/G,j]
+ * / sqrt(d) for each retrieval head h at its block size g = granularity[h],
+ * j < L/g, rows of the plan's score_stride floats ([Bt][Hq][score_stride]);
+ * streaming heads' rows are not written.  One pass per block size; a KV group
+ * none of whose heads uses a size does not read that size's cache.
+ * Errors: INVALID_ARG, SHAPE, UNSUPPORTED, CUDA.
+ */
+sa_status sparse_attn_score_plan(const sa_shape* shp, const sa_plan* plan,
+                                 const void* q, const float* kbar_all,
+                                 float* scores, sa_stream_t stream);
 
 #ifdef __cplusplus
 }

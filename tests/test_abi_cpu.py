@@ -281,3 +281,85 @@ def test_topp_and_rebuild_reject_bad_arguments_before_launch(sa):
     assert lib.sparse_attn_plan_rebuild(dplan.handle, P, None) == 1
     assert lib.sparse_attn_plan_rebuild(plan.handle, None, None) == 1
     assert lib.sparse_attn_plan_device_schedule(plan.handle, P, P, None) == 8
+
+
+def test_decode_plan_per_head_block_sizes(sa):
+    shape = sa.Shape.decode(65536, 32, 8, 2, 128, 4)
+    kinds = np.array([0, 1, 0, 0, 0, 0, 1, 0], np.uint8)
+    gran = [16, 8, 64, 128, 16, 32, 999, 64]          # streaming entries are ignored
+    budget = [70, 0, 40, 9000, 2, 64, 0, 31]
+    plan = sa.sparse_attn_plan(shape, 64, head_kind=kinds, window_blocks=16, num_workers=1,
+                               granularity=gran, head_budget=budget)
+    got = plan.get()
+    nbh = [65536 // g for g in (16, 32, 64, 128, 16, 32, 32, 64)]
+    want = [17 if kinds[h] else min(budget[h], nbh[h]) for h in range(8)]
+    assert got["budgets"].tolist() == want
+    assert got["kmax"] == max(want)
+    assert got["total_blocks"] == 4 * sum(want)
+    lay = plan.decode_layout()
+    assert lay["sizes"] == [16, 32, 64, 128]
+    assert lay["score_stride"] == 65536 // 16
+    assert lay["kcache_floats"] == sum(4 * 2 * (65536 // g) * 128 for g in (16, 32, 64, 128))
+    # without sizes: B for every head, scores of nb per row
+    plain = sa.sparse_attn_plan(shape, 64, head_kind=kinds, window_blocks=16, num_workers=1)
+    assert plain.decode_layout() == {"sizes": [32], "kcache_floats": 4 * 2 * 2048 * 128,
+                                     "score_stride": 2048}
+
+
+def test_decode_block_size_argument_errors(sa):
+    dshape = sa.Shape.decode(65536, 32, 4, 2, 128, 2)
+    kinds = np.zeros(4, np.uint8)
+
+    def plan_status(shape, gran=None, budget=None, kinds_=kinds):
+        keep = []
+        p = _params(sa)
+        p.k_uniform, p.num_workers = 8, 1
+        for name, arr, ct in (("granularity", gran, ctypes.c_int32),
+                              ("head_budget", budget, ctypes.c_int32),
+                              ("head_kind", kinds_, ctypes.c_uint8)):
+            if arr is not None:
+                a = np.ascontiguousarray(arr, dtype=np.int32 if ct is ctypes.c_int32 else np.uint8)
+                keep.append(a)
+                setattr(p, name, a.ctypes.data_as(ctypes.POINTER(ct)))
+        return _raw_plan(sa, shape, p)
+
+    assert plan_status(dshape, [16, 32, 64, 128]) == 0
+    assert plan_status(dshape, [8, 32, 32, 32]) == 1          # below 16
+    assert plan_status(dshape, [24, 32, 32, 32]) == 1         # not a multiple of 16
+    assert plan_status(dshape, [48, 32, 32, 32]) == 1         # does not divide L
+    big = sa.Shape.decode(131072, 32, 4, 2, 128, 2)
+    assert plan_status(big, [16, 32, 32, 32]) == 1            # 8192 blocks > 4096
+    assert plan_status(big, [32, 32, 32, 32]) == 0
+    assert plan_status(dshape, None, [8, 1, 8, 8]) == 1       # budget below k_min
+    many = sa.Shape.decode(40320, 32, 16, 2, 128, 1)        # 16 * m divides L for m <= 9
+    sizes = [16 * m for m in (1, 2, 3, 4, 5, 6, 7, 8, 9)] + [16] * 7
+    assert plan_status(many, sizes, None, np.zeros(16, np.uint8)) == 1   # 9 distinct sizes
+    assert plan_status(many, sizes[:8] + [16] * 8, None, np.zeros(16, np.uint8)) == 0
+    pshape = sa.Shape.prefill(4096, 64, 8, 2, 64)
+    p = _params(sa)
+    g = np.full(8, 64, np.int32)
+    p.granularity = g.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    assert _raw_plan(sa, pshape, p) == 1                      # prefill plans take none
+    pplan = sa.sparse_attn_plan(pshape, 9, num_workers=4)
+    with pytest.raises(sa.SparseAttnError):
+        pplan.decode_layout()
+
+
+def test_decode_block_size_calls_reject_bad_arguments_before_launch(sa):
+    lib, P = sa._lib, 8192
+    dshape = sa.Shape.decode(4096, 32, 4, 2, 128, 2)
+    s = ctypes.byref(dshape)
+    plan = sa.sparse_attn_plan(dshape, 8, num_workers=1, granularity=[16, 32, 64, 128])
+    other = sa.Shape.decode(8192, 32, 4, 2, 128, 2)
+    pshape = sa.Shape.prefill(4096, 64, 8, 2, 64)
+    pplan = sa.sparse_attn_plan(pshape, 9, num_workers=4)
+    assert lib.sparse_attn_pool_kcache_plan(s, None, P, P, None) == 1
+    assert lib.sparse_attn_pool_kcache_plan(s, plan.handle, None, P, None) == 1
+    assert lib.sparse_attn_pool_kcache_plan(s, plan.handle, P + 4, P, None) == 1
+    assert lib.sparse_attn_pool_kcache_plan(ctypes.byref(other), plan.handle, P, P, None) == 2
+    assert lib.sparse_attn_pool_kcache_plan(ctypes.byref(pshape), pplan.handle, P, P, None) == 1
+    assert lib.sparse_attn_score_plan(s, plan.handle, P, P, P, None) == 8   # not uploaded
+    assert lib.sparse_attn_score_plan(s, plan.handle, P, None, P, None) == 1
+    assert lib.sparse_attn_score_plan(ctypes.byref(other), plan.handle, P, P, P, None) == 2
+    # a forward with sizes needs the plan on the device
+    assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 8, P, 1, None, P, None) == 8

@@ -95,3 +95,108 @@ def test_decode_full_size(env):
     window = w.window_tokens // w.block
     r = _decode(sa, torch, w, x, kinds, budget, window, "bfloat16")
     _check(w, x, r, kinds, budget, window, bf16_out=True)
+
+
+def _decode_sized(sa, torch, w, x, kinds, gran, budget, window, out_dtype="float32"):
+    from head_heterogeneous_block_gb300.layer import DecodeStep
+    from tests._parity import to_dev
+    shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                            w.batch)
+    step = DecodeStep(shape, 2, kinds, window, with_lse=True,
+                      out_dtype=getattr(torch, out_dtype), granularity=gran, head_budget=budget)
+    t = {n: to_dev(x[n]) for n in "qkv"}
+    step.build_cache(t["k"])
+    out = step(t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    Bt, H = w.batch, w.num_q_heads
+    return {
+        "status": int(step.dev_status.item()),
+        "layout": step.plan.decode_layout(),
+        "kbar": step.kbar.cpu().numpy(),
+        "scores": step.scores.view(Bt, H, step.score_stride).cpu().numpy(),
+        "idx": step.idx.view(Bt, H, step.kmax).cpu().numpy(),
+        "cnt": step.cnt.view(Bt, H).cpu().numpy(),
+        "out": out.float().cpu().numpy(),
+        "lse": step.lse.view(Bt, H).cpu().numpy(),
+    }
+
+
+def _check_sized(w, x, r, kinds, gran, budget, window, bf16_out=False):
+    from oracle import decode as od
+    from oracle import granularity as og
+    from tests import _parity as P
+    from workloads import generate
+    assert r["status"] == 0
+    L, d, Bt, Hkv = w.seq_len, w.head_dim, w.batch, w.num_kv_heads
+    sizes = sorted({gran[h] for h in range(w.num_q_heads) if kinds[h] != 1})
+    assert r["layout"]["sizes"] == sizes
+    assert r["layout"]["score_stride"] == L // sizes[0]
+    block_of = [gran[h] if kinds[h] != 1 else w.block for h in range(w.num_q_heads)]
+    for b in range(Bt):
+        q = generate.bf16_to_f64(x["q"][b:b + 1])
+        k = generate.bf16_to_f32(x["k"][b:b + 1])
+        v = generate.bf16_to_f32(x["v"][b:b + 1])
+        off = 0
+        for g in sizes:
+            n = Bt * Hkv * (L // g) * d
+            cache = r["kbar"][off:off + n].reshape(Bt, Hkv, L // g, d)
+            np.testing.assert_allclose(cache[b], og.pool_cache(k, g)[0], rtol=1e-5, atol=1e-6)
+            off += n
+        sc = og.decode_scores(q, k, kinds, gran)[0]
+        for h in range(w.num_q_heads):
+            n = r["cnt"][b, h]
+            sel = r["idx"][b, h, :n]
+            assert all(t == -1 for t in r["idx"][b, h, n:])
+            if kinds[h] == 1:
+                assert sel.tolist() == od.streaming_blocks(w.nb, window)
+                continue
+            nbh = L // gran[h]
+            np.testing.assert_allclose(r["scores"][b, h, :nbh], sc[h], rtol=1e-4, atol=1e-6)
+            assert n == min(budget[h], nbh)
+            P.check_selection_row(sel, og.select_row(sc[h], min(budget[h], nbh)), sc[h],
+                                  nbh - 1)
+        o, lse = od.decode_attend(q, k, v, r["idx"][b:b + 1], r["cnt"][b:b + 1], block_of)
+        dd = np.abs(r["out"][b] - o[0])
+        if bf16_out:
+            dd = np.maximum(dd - P.half_ulp_bf16(np.maximum(np.abs(o[0]), np.abs(r["out"][b]))),
+                            0)
+        assert dd.max() <= P.MAX_ABS, dd.max()
+        assert dd.sum() / np.abs(o[0]).sum() <= P.MEAN_REL
+        assert np.abs(r["lse"][b] - lse[0]).max() <= P.LSE_ABS
+
+
+@pytest.mark.parametrize("L,Bt,window,sizes", [(4096, 2, 8, (16, 32, 64, 128)),
+                                               (1024, 3, 4, (128, 16)),
+                                               (2048, 1, 16, (64,))])
+def test_decode_per_head_block_sizes(env, L, Bt, window, sizes):
+    # every size a multiple of 16, odd unit counts (a masked half step),
+    # budgets above a head's block count (capped), groups mixing sizes
+    sa, torch = env
+    from workloads import generate, scaled, workload
+    w = scaled(workload(5), L, batch=Bt)
+    x = generate.decode_inputs(w)
+    kinds = generate.head_kinds(w)
+    H = w.num_q_heads
+    gran = [sizes[h % len(sizes)] for h in range(H)]
+    budget = [3 + (5 * h) % 11 for h in range(H)]
+    for out_dtype in ("float32", "bfloat16"):
+        r = _decode_sized(sa, torch, w, x, kinds, gran, budget, window, out_dtype)
+        _check_sized(w, x, r, kinds, gran, budget, window, bf16_out=out_dtype == "bfloat16")
+
+
+def test_decode_per_head_block_sizes_full_size(env):
+    # the 64K decode workload with the block sizes and budgets chosen offline
+    # (rows of up to 4096 blocks)
+    import json
+    import os
+    sa, torch = env
+    from workloads import generate, workload
+    w = workload(5)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "workloads", "demands.json")) as f:
+        prof = json.load(f)["5"]["granularity"]
+    x = generate.decode_inputs(w)
+    kinds = generate.head_kinds(w)
+    window = w.window_tokens // w.block
+    r = _decode_sized(sa, torch, w, x, kinds, prof["gran"], prof["budget"], window, "bfloat16")
+    _check_sized(w, x, r, kinds, prof["gran"], prof["budget"], window, bf16_out=True)
