@@ -164,6 +164,9 @@ __global__ void __launch_bounds__(kT) select_kernel(sa_k::SelectArgs a) {
           prefix |= b << shift;
           mask |= 0xFFu << shift;
           __syncthreads();
+          // the bin holds exactly the candidates still needed: all of them,
+          // and everything above, are kept (u >= prefix, lower bits zero)
+          if (eq_total == need) break;
         }
         const uint32_t T = prefix;
         if (eq_total == need) {
@@ -197,29 +200,43 @@ __global__ void __launch_bounds__(kT) select_kernel(sa_k::SelectArgs a) {
   }
   __syncthreads();
 
-  // Emit ascending block indices, then pad with -1 (warp 0), into the row of
-  // every head that shares the list.
-  if (warp == 0) {
+  // Emit ascending block indices, then pad with -1, into the row of every
+  // head that shares the list.  Warp w takes a contiguous range of the
+  // bitmap's words: counts, a prefix over the warps, then ballots per word.
+  {
+    constexpr int kWarps = kT / 32;
     const size_t orow = a.decode ? size_t(row) : size_t(h) * a.nb + i;
     int32_t* out = a.idx + orow * a.kmax;
-    int written = 0;
-    for (int base = 0; base <= i; base += 32) {
-      const int j = base + lane;
-      const bool on = (j <= i) && ((bits[j >> 5] >> (j & 31)) & 1u);
+    const int nw = (i + 32) / 32;             // words holding blocks 0..i
+    const int wper = (nw + kWarps - 1) / kWarps;
+    const int w0 = min(nw, warp * wper), w1 = min(nw, w0 + wper);
+    uint32_t mine = 0;
+    for (int x = w0 + lane; x < w1; x += 32) mine += __popc(bits[x]);
+    mine = __reduce_add_sync(0xffffffffu, mine);
+    if (lane == 0) wsum[warp] = mine;
+    __syncthreads();
+    int written = 0, total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) written += int(wsum[w]);
+      total += int(wsum[w]);
+    }
+    for (int x = w0; x < w1; ++x) {
+      const bool on = ((bits[x] >> lane) & 1u) != 0;   // bits past i are zero
       const uint32_t m = __ballot_sync(0xffffffffu, on);
       const int pos = written + __popc(m & ((1u << lane) - 1u));
-      if (on && pos < a.kmax) out[pos] = j;
+      if (on && pos < a.kmax) out[pos] = 32 * x + lane;
       written += __popc(m);
     }
-    for (int t = written + lane; t < a.kmax; t += 32) out[t] = -1;
-    if (lane == 0) a.cnt[orow] = min(written, a.kmax);
-    // the other heads of a group-shared row get copies of the list (written
-    // above by the warp's lanes: order those writes before the reads)
-    __syncwarp();
-    for (int x = 1; x < G; ++x) {
-      int32_t* dst = a.idx + (orow + size_t(x) * a.nb) * a.kmax;
-      for (int t = lane; t < a.kmax; t += 32) dst[t] = out[t];
-      if (lane == 0) a.cnt[orow + size_t(x) * a.nb] = min(written, a.kmax);
+    for (int t = total + tid; t < a.kmax; t += kT) out[t] = -1;
+    if (tid == 0) a.cnt[orow] = min(total, a.kmax);
+    if (G > 1) {
+      // the other heads of a group-shared row get copies of the list
+      __syncthreads();
+      for (int x = 1; x < G; ++x) {
+        int32_t* dst = a.idx + (orow + size_t(x) * a.nb) * a.kmax;
+        for (int t = tid; t < a.kmax; t += kT) dst[t] = out[t];
+        if (tid == 0) a.cnt[orow + size_t(x) * a.nb] = min(total, a.kmax);
+      }
     }
   }
 }
