@@ -200,3 +200,53 @@ def test_decode_per_head_block_sizes_full_size(env):
     window = w.window_tokens // w.block
     r = _decode_sized(sa, torch, w, x, kinds, prof["gran"], prof["budget"], window, "bfloat16")
     _check_sized(w, x, r, kinds, prof["gran"], prof["budget"], window, bf16_out=True)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (16, 2), (32, 2)])
+def test_decode_group_sizes(env, Hq, Hkv):
+    # groups of 1, 8 and 16 query heads: one or two 8-head tensor-core tiles
+    # in the scores, with the default and with per-head block sizes
+    sa, torch = env
+    from workloads import generate, scaled, workload
+    w = scaled(workload(5), 2048, num_q_heads=Hq, num_kv_heads=Hkv, batch=2)
+    x = generate.decode_inputs(w)
+    kinds = generate.head_kinds(w)
+    r = _decode(sa, torch, w, x, kinds, 9, 4, "float32")
+    _check(w, x, r, kinds, 9, 4)
+    gran = [(16, 32, 64)[h % 3] for h in range(Hq)]
+    budget = [4 + h % 7 for h in range(Hq)]
+    if all(k == 1 for k in kinds):
+        return
+    r = _decode_sized(sa, torch, w, x, kinds, gran, budget, 4, "float32")
+    _check_sized(w, x, r, kinds, gran, budget, 4)
+
+
+def test_decode_all_streaming_with_block_sizes(env):
+    # no retrieval head: no pooled cache, no score pass; streaming lists only
+    sa, torch = env
+    from workloads import generate, scaled, workload
+    w = scaled(workload(5), 1024, num_q_heads=8, num_kv_heads=2, batch=2)
+    x = generate.decode_inputs(w)
+    kinds = np.ones(8, np.uint8)
+    from head_heterogeneous_block_gb300.layer import DecodeStep
+    from oracle import decode as od
+    from tests import _parity as P
+    from tests._parity import to_dev
+    shape = sa.Shape.decode(w.seq_len, w.block, 8, 2, w.head_dim, 2)
+    step = DecodeStep(shape, 2, kinds, 4, with_lse=True, out_dtype=torch.float32,
+                      granularity=[16] * 8, head_budget=[4] * 8)
+    assert step.plan.decode_layout()["sizes"] == []
+    t = {n: to_dev(x[n]) for n in "qkv"}
+    step.build_cache(t["k"])
+    out = step(t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+    idx = step.idx.view(2, 8, step.kmax).cpu().numpy()
+    cnt = step.cnt.view(2, 8).cpu().numpy()
+    for b in range(2):
+        for h in range(8):
+            assert idx[b, h, :cnt[b, h]].tolist() == od.streaming_blocks(w.nb, 4)
+    from workloads import generate as gen
+    o, _ = od.decode_attend(gen.bf16_to_f64(x["q"]), gen.bf16_to_f32(x["k"]),
+                            gen.bf16_to_f32(x["v"]), idx, cnt, w.block)
+    assert np.abs(out.cpu().numpy() - o).max() <= P.MAX_ABS
