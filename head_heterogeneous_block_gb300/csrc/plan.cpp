@@ -83,10 +83,11 @@ void build_schedule(const std::vector<int32_t>& budgets, int32_t nb, int32_t gro
                     std::vector<int32_t>& items, std::vector<int64_t>& loads) {
   const int32_t heads = int32_t(budgets.size());
   const int64_t n = int64_t(heads) * nb;
-  auto cost = [&](int32_t id) -> int32_t {
-    const int32_t h = id / nb, i = id % nb;
-    return std::min(budgets[h], i + 1);
-  };
+  // item (h, i) has id h*nb + i and costs min(k_h, i+1) blocks
+  std::vector<int32_t> item_cost(n);
+  for (int32_t h = 0; h < heads; ++h)
+    for (int32_t i = 0; i < nb; ++i) item_cost[int64_t(h) * nb + i] = std::min(budgets[h], i + 1);
+  auto cost = [&](int32_t id) -> int32_t { return item_cost[id]; };
   wptr.assign(workers + 1, 0);
   items.resize(n);
   loads.assign(workers, 0);
@@ -104,39 +105,113 @@ void build_schedule(const std::vector<int32_t>& budgets, int32_t nb, int32_t gro
   }
 
   // Walk order: cost descending, ties by id; LPT_GROUPED first by KV group.
+  // Costs are integers in [0, nb], so a stable counting sort over the key
+  // (group, nb - cost) -- the group part only for LPT_GROUPED -- walking the
+  // ids in ascending order gives exactly that order in linear time.
   std::vector<int32_t> order(n);
-  for (int64_t id = 0; id < n; ++id) order[id] = int32_t(id);
-  if (policy == SA_SCHED_LPT_GROUPED) {
-    std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
-      const int32_t ga = (a / nb) / group, gb = (b / nb) / group;
-      if (ga != gb) return ga < gb;
-      const int32_t ca = cost(a), cb = cost(b);
-      if (ca != cb) return ca > cb;
-      return a < b;
-    });
-  } else {
-    std::sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
-      const int32_t ca = cost(a), cb = cost(b);
-      if (ca != cb) return ca > cb;
-      return a < b;
-    });
+  {
+    const int32_t ngroups = policy == SA_SCHED_LPT_GROUPED ? (heads + group - 1) / group : 1;
+    const int64_t nkeys = int64_t(ngroups) * (nb + 1);
+    std::vector<int64_t> start(nkeys + 1, 0);
+    std::vector<int64_t> keys(n);
+    for (int32_t h = 0; h < heads; ++h) {
+      const int64_t base = policy == SA_SCHED_LPT_GROUPED ? int64_t(h / group) * (nb + 1) : 0;
+      for (int32_t i = 0; i < nb; ++i) {
+        const int64_t id = int64_t(h) * nb + i;
+        keys[id] = base + (nb - std::max(0, std::min(item_cost[id], nb)));
+      }
+    }
+    for (int64_t id = 0; id < n; ++id) ++start[keys[id] + 1];
+    for (int64_t k = 0; k < nkeys; ++k) start[k + 1] += start[k];
+    for (int64_t id = 0; id < n; ++id) order[start[keys[id]]++] = int32_t(id);
   }
 
-  // Least-loaded worker first; equal loads go to the lower worker id.
-  using Slot = std::pair<int64_t, int32_t>;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int32_t w = 0; w < workers; ++w) heap.push({0, w});
+  // Least-loaded worker first; equal loads go to the lower worker id.  The
+  // walk is a sequence of runs of equal cost c, and a run of r items is
+  // placed at once: its choices are the r smallest pairs (value, worker)
+  // among the sequences L_w + m*c (m >= 0) -- every step takes the smallest
+  // head of those sequences and moves that worker's head up by c.  A binary
+  // search finds the value V of the r-th pair; worker w takes its pairs below
+  // V, plus one at V if it is among the first workers (by id) with a pair
+  // there.  A pair's value is q*c + (L_w mod c) at level q = L_w / c + m, so
+  // the pairs in (value, worker) order are the levels in turn, each over the
+  // workers ordered by (L_w mod c, w): the k-th item of the run goes to the
+  // worker of the k-th pair.
   std::vector<int32_t> owner(n);
   std::vector<int32_t> count(workers, 0);
-  for (int64_t r = 0; r < n; ++r) {
-    Slot s = heap.top();
-    heap.pop();
-    owner[r] = s.second;
-    ++count[s.second];
-    s.first += cost(order[r]);
-    loads[s.second] = s.first;
-    heap.push(s);
+  std::vector<int64_t> L(workers, 0), take(workers, 0), Lq(workers), Lr(workers);
+  std::vector<int32_t> act;
+  act.reserve(workers);
+  int64_t placed = 0;                         // sum of the loads
+  for (int64_t r0 = 0; r0 < n;) {
+    const int64_t c = cost(order[r0]);
+    int64_t r1 = r0;
+    while (r1 < n && cost(order[r1]) == c) ++r1;
+    const int64_t r = r1 - r0;
+    if (c <= 0) {
+      // zero cost: every item goes to the least-loaded worker
+      int32_t w0 = 0;
+      for (int32_t w = 1; w < workers; ++w)
+        if (L[w] < L[w0]) w0 = w;
+      for (int64_t k = r0; k < r1; ++k) owner[k] = w0;
+      count[w0] += int32_t(r);
+      r0 = r1;
+      continue;
+    }
+    // L_w = Lq_w * c + Lr_w; worker w has max(0, Vq - Lq_w + [Vr > Lr_w]) pairs
+    // below V = Vq * c + Vr
+    for (int32_t w = 0; w < workers; ++w) {
+      Lq[w] = L[w] / c;
+      Lr[w] = L[w] - Lq[w] * c;
+    }
+    auto below = [&](int64_t V) {
+      const int64_t Vq = V / c, Vr = V - Vq * c;
+      int64_t t = 0;
+      for (int32_t w = 0; w < workers; ++w)
+        t += std::max<int64_t>(0, Vq - Lq[w] + (Vr > Lr[w] ? 1 : 0));
+      return t;
+    };
+    int64_t mn = L[0];
+    for (int32_t w = 1; w < workers; ++w) mn = std::min(mn, L[w]);
+    // below(lo) = 0 < r <= below(hi), since below(V) >= sum_w (V - L_w) / c
+    int64_t lo = mn, hi = std::min(mn + r * c, (placed + r * c + workers - 1) / workers);
+    while (hi - lo > 1) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (below(mid) < r) lo = mid;
+      else hi = mid;
+    }
+    const int64_t V = lo;                     // the value of the r-th pair
+    int64_t extra = r - below(V);             // pairs taken at exactly V
+    act.clear();
+    const int64_t Vq = V / c, Vr = V - Vq * c;
+    for (int32_t w = 0; w < workers; ++w) {
+      int64_t t = std::max<int64_t>(0, Vq - Lq[w] + (Vr > Lr[w] ? 1 : 0));
+      if (extra > 0 && Vr == Lr[w] && Vq >= Lq[w]) {
+        ++t;
+        --extra;
+      }
+      take[w] = t;
+      if (t) act.push_back(w);
+    }
+    std::stable_sort(act.begin(), act.end(),
+                     [&](int32_t x, int32_t y) { return Lr[x] < Lr[y]; });
+    int64_t qlo = INT64_MAX, qhi = 0;
+    for (int32_t w : act) {
+      qlo = std::min(qlo, Lq[w]);
+      qhi = std::max(qhi, Lq[w] + take[w] - 1);
+    }
+    int64_t pos = r0;
+    for (int64_t q = qlo; q <= qhi && pos < r1; ++q)
+      for (int32_t w : act)
+        if (Lq[w] <= q && q < Lq[w] + take[w] && pos < r1) owner[pos++] = w;
+    for (int32_t w : act) {
+      L[w] += take[w] * c;
+      count[w] += int32_t(take[w]);
+    }
+    placed += r * c;
+    r0 = r1;
   }
+  for (int32_t w = 0; w < workers; ++w) loads[w] = L[w];
   // CSR by worker, each list in assignment order.
   for (int32_t w = 0; w < workers; ++w) wptr[w + 1] = wptr[w] + count[w];
   std::vector<int32_t> fill(wptr.begin(), wptr.end() - 1);
