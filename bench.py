@@ -182,7 +182,15 @@ def run_ours(args):
     t0 = time.perf_counter()
     layer = PrefillLayer(shape, prof["k_uniform"], demand=prof["demand"], k_min=prof["k_min"],
                          num_workers=sms, schedule=args.schedule, device=dev)
-    plan_ms = (time.perf_counter() - t0) * 1e3
+    setup_ms = (time.perf_counter() - t0) * 1e3
+    # the host plan alone (Max-Min budgets and the schedule), best of five
+    plan_ms = float("inf")
+    for _ in range(5):
+        t0 = time.perf_counter()
+        p = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=prof["demand"],
+                                k_min=prof["k_min"], num_workers=sms, schedule=args.schedule)
+        plan_ms = min(plan_ms, (time.perf_counter() - t0) * 1e3)
+        p.close()
     x = generate.prefill_inputs(w)
     host = {n: torch.from_numpy(x[n].view(np.int16)).view(torch.bfloat16).pin_memory()
             for n in "qkv"}
@@ -355,27 +363,31 @@ def run_ours(args):
                 "device_status": int(layer.dev_status.item()), **res}
         del tidx, tcnt, swptr, sitems
 
-    # ---- end to end through the public API with host buffers
-    out_host = torch.empty((w.num_q_heads, w.seq_len, w.head_dim), dtype=torch.bfloat16,
-                           pin_memory=True)
+    # ---- end to end through the public API with host buffers: every step
+    # copies its Q, K and V from pinned host memory and reads its output
+    # back; HostPipeline overlaps one step's copies with another's compute.
+    # The host plan is rebuilt before every step to charge its cost too.
+    from head_heterogeneous_block_gb300.layer import HostPipeline
+    out_host = [torch.empty((w.num_q_heads, w.seq_len, w.head_dim), dtype=torch.bfloat16,
+                            pin_memory=True) for _ in range(2)]
     h2d = sum(host[n].numel() * host[n].element_size() for n in "qkv")
-    d2h = out_host.numel() * out_host.element_size()
-    e2e_steps = max(2, min(args.steps, 5))
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    e2e_steps = 8
+    pipe = HostPipeline(layer, device=dev)
+
+    def replan(_s):
+        p = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=prof["demand"],
+                                k_min=prof["k_min"], num_workers=sms, schedule=args.schedule)
+        p.close()
+
+    steps_in = [(host["q"], host["k"], host["v"], out_host[s % 2]) for s in range(e2e_steps)]
+    pipe.run(steps_in[:2], stream=stream)          # warm-up
     torch.cuda.synchronize(dev)
     t1 = time.perf_counter()
-    for _ in range(e2e_steps):
-        plan_e2e = sa.sparse_attn_plan(shape, prof["k_uniform"], demand=prof["demand"],
-                                       k_min=prof["k_min"], num_workers=sms,
-                                       schedule=args.schedule)
-        plan_e2e.close()
-        dq = host["q"].to(dev, non_blocking=True)
-        dk = host["k"].to(dev, non_blocking=True)
-        dv = host["v"].to(dev, non_blocking=True)
-        o = layer(dq, dk, dv, stream=stream)
-        out_host.copy_(o, non_blocking=True)
-        torch.cuda.synchronize(dev)
+    pipe.run(steps_in, stream=stream, before_step=replan)
     e2e_s = (time.perf_counter() - t1) / e2e_steps
     e2e_value = flops / e2e_s / 1e12
+    del pipe
 
     # ---- decode step (workload 5), reported beside the prefill line
     decode = None
@@ -400,6 +412,7 @@ def run_ours(args):
         "forward_ms": round(fwd_ms, 4),
         "stages": stages,
         "plan_host_ms": round(plan_ms, 3),
+        "layer_setup_ms": round(setup_ms, 3),
         "roofline": {"bound": "tensor", "kernel": "prefill_attention_kernel<128,128>",
                      "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
@@ -411,7 +424,8 @@ def run_ours(args):
         "output_aware_demands": output_aware,
         "topp": topp,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_s * 1e3, 3),
+                "overlap": "double-buffered: copies of one step overlap another's compute"},
         "gpu_launches": 5 * args.steps,
         "clocks": clk,
         "device_status": status,

@@ -106,3 +106,66 @@ class DecodeStep:
         sparse_attn_forward(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax, out,
                             self.lse, self.dev_status, stream=stream)
         return out
+
+
+class HostPipeline:
+    """A PrefillLayer over a sequence of host-resident (pinned) steps, with
+    each step's host-to-device copies and the previous step's device-to-host
+    read overlapped with compute.
+
+    Two device buffer sets alternate.  Step s copies its Q, K and V into set
+    s % 2 on a copy-in stream once the compute of step s - 2 (the last reader
+    of that set) is done; the layer runs on the compute stream once the
+    copies are in and the read-back of step s - 2's output is done; the
+    output is copied to the step's host buffer on a copy-out stream.  Every
+    step still moves all of its inputs and its result across the link; only
+    the order in time changes.
+    """
+
+    def __init__(self, layer: "PrefillLayer", device="cuda"):
+        dev = torch.device(device)
+        s = layer.shape
+        H, Hkv, S, d = s.num_q_heads, s.num_kv_heads, s.seq_len, s.head_dim
+        self.layer = layer
+        self.bufs = [{"q": torch.empty(H, S, d, dtype=torch.bfloat16, device=dev),
+                      "k": torch.empty(Hkv, S, d, dtype=torch.bfloat16, device=dev),
+                      "v": torch.empty(Hkv, S, d, dtype=torch.bfloat16, device=dev),
+                      "o": torch.empty_like(layer.out)} for _ in range(2)]
+        self.copy_in = torch.cuda.Stream(dev)
+        self.copy_out = torch.cuda.Stream(dev)
+        self.dev = dev
+
+    def run(self, steps, stream=None, before_step=None):
+        """steps: iterable of (q, k, v, o) pinned host tensors; o receives the
+        step's output.  before_step(s), if given, runs on the host before
+        step s is issued.  Returns once every output is on the host."""
+        comp = torch.cuda.current_stream(self.dev) if stream is None else stream
+        done = [None, None]       # compute of the last step that used each set
+        read = [None, None]       # read-back of the last output of each set
+        for s, (qh, kh, vh, oh) in enumerate(steps):
+            if before_step is not None:
+                before_step(s)
+            b = s % 2
+            buf = self.bufs[b]
+            with torch.cuda.stream(self.copy_in):
+                if done[b] is not None:
+                    self.copy_in.wait_event(done[b])
+                buf["q"].copy_(qh, non_blocking=True)
+                buf["k"].copy_(kh, non_blocking=True)
+                buf["v"].copy_(vh, non_blocking=True)
+                copied = torch.cuda.Event()
+                copied.record(self.copy_in)
+            comp.wait_event(copied)
+            if read[b] is not None:
+                comp.wait_event(read[b])
+            self.layer(buf["q"], buf["k"], buf["v"], out=buf["o"], stream=comp)
+            done[b] = torch.cuda.Event()
+            done[b].record(comp)
+            with torch.cuda.stream(self.copy_out):
+                self.copy_out.wait_event(done[b])
+                oh.copy_(buf["o"], non_blocking=True)
+                read[b] = torch.cuda.Event()
+                read[b].record(self.copy_out)
+        self.copy_out.synchronize()
+        self.copy_in.synchronize()
+        comp.synchronize()

@@ -272,3 +272,29 @@ def test_prefill_largest_rows(env):
     items = P.sample_items(r["budgets"], w.nb, 24, seed=2048)
     P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group,
                       bf16_out=True)
+
+
+def test_host_pipeline_matches_the_layer_step_by_step(env):
+    # overlapped host copies change only when data moves, never the result:
+    # each step's output equals the layer run on that step's inputs alone
+    sa, torch = env
+    from head_heterogeneous_block_gb300.layer import HostPipeline, PrefillLayer
+    from workloads import generate, scaled, workload
+    w = scaled(workload(2), 4096, 8, 2)
+    shape = sa.Shape.prefill(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim)
+    layer = PrefillLayer(shape, 9)
+    steps, want = [], []
+    for seed in (11, 12, 13, 14, 15):
+        x = generate.prefill_inputs(w, seed=seed)
+        host = {n: torch.from_numpy(x[n].view(np.int16)).view(torch.bfloat16).pin_memory()
+                for n in "qkv"}
+        o = torch.empty(w.num_q_heads, w.seq_len, w.head_dim, dtype=torch.bfloat16,
+                        pin_memory=True)
+        steps.append((host["q"], host["k"], host["v"], o))
+        ref = layer(*(host[n].cuda() for n in "qkv")).cpu()
+        torch.cuda.synchronize()
+        want.append(ref)
+    HostPipeline(layer).run(steps)
+    for (_, _, _, o), ref in zip(steps, want):
+        assert torch.equal(o, ref)
+    assert int(layer.dev_status.item()) == 0
