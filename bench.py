@@ -372,7 +372,7 @@ def run_ours(args):
                             pin_memory=True) for _ in range(2)]
     h2d = sum(host[n].numel() * host[n].element_size() for n in "qkv")
     d2h = out_host[0].numel() * out_host[0].element_size()
-    e2e_steps = 8
+    e2e_steps = 16
     pipe = HostPipeline(layer, device=dev)
 
     def replan(_s):
