@@ -7,9 +7,9 @@
 // pool_kernel      HBM-bound: every block of B rows x d bf16 is read once with
 //                  16-byte loads, summed in fp32 and scaled by 1/B.
 // prefill_scores   S[h,i,j] = qbar[h,i] . kbar[g,j] * scale for j <= i; a
-//                  64x64 fp32 SIMT tile per CTA over the lower triangle (the
-//                  contraction is small -- d = 128 -- and selection needs fp32
-//                  accuracy, so no reduced-precision tensor path).
+//                  64x64 tile per CTA over the lower triangle on the tensor
+//                  cores (tf32 MMAs on both operands split in two, products
+//                  hi*hi + hi*lo + lo*hi: selection needs fp32-level scores).
 // decode_scores    scores[b,h,j] = q[b,h] . kbar[b,g,j] * scale; persistent
 //                  CTAs stream 32 KB chunks of pooled keys through a
 //                  three-stage cp.async ring while scoring earlier chunks; a
@@ -66,62 +66,133 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4* __restrict__ x,
   }
 }
 
-// 64x64 output tile per CTA, 256 threads, each 4x4 outputs; d in chunks of 32.
-constexpr int kT = 64, kKc = 32;
+// ---------------------------------------------------------------- tf32 MMA helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_2() {
+  asm volatile("cp.async.wait_group 2;" ::: "memory");
+}
+// 16-byte chunk c of a row of kC chunks sits at c ^ 4(r mod kC/4): the rows
+// a quarter-warp reads together land on different banks
+template <int kC>
+__device__ __forceinline__ int swz(int r, int c) { return c ^ ((r & (kC / 4 - 1)) << 2); }
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
+// x = hi + lo with hi a tf32 value (the 10 leading mantissa bits of x)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xFFFFE000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+// D += A . B for one m16n8k8 tile (A 16x8 row-major, B 8x8 column-major, tf32)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Prefill scores on the tensor cores: one 64x64 tile of (query block i, key
+// block j), j <= i, per CTA over the lower triangle.  The tile's pooled query
+// and key rows (fp32) are copied into XOR-swizzled shared memory with
+// cp.async; warp w takes tile rows 16(w%4) .. +16 and columns 32(w/4) .. +32
+// as four m16n8k8 tf32 MMA tiles.  Both operands are fp32: each is split into
+// a tf32 part and the rest, and the products hi*hi + hi*lo + lo*hi keep
+// fp32-level scores (selection needs them; a single tf32 or bf16 product
+// would not).  The k order inside an MMA is permuted as in the decode kernel.
+constexpr int kT = 64;
+
+template <int D>
 __global__ void __launch_bounds__(256) prefill_scores_kernel(const float* __restrict__ qbar,
                                                              const float* __restrict__ kbar,
                                                              float* __restrict__ scores, int nb,
-                                                             int d, int group, float scale,
-                                                             int tiles) {
+                                                             int group, float scale) {
+  constexpr int kC = D / 4;                   // 16-byte chunks per row
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float4 (*sa)[kC] = reinterpret_cast<float4 (*)[kC]>(smem_raw);
+  float4 (*sb)[kC] = reinterpret_cast<float4 (*)[kC]>(smem_raw + kT * kC * sizeof(float4));
   // blockIdx.x enumerates lower-triangle tile pairs (ti >= tj); blockIdx.y = head
   int t = blockIdx.x, ti = 0;
   while (t > ti) {
     t -= ti + 1;
     ++ti;
   }
-  const int tj = t;
-  const int h = blockIdx.y;
-  const float* qh = qbar + size_t(h) * nb * d;
-  const float* kg = kbar + size_t(h / group) * nb * d;
-  __shared__ float sq[kKc][kT + 4];
-  __shared__ float sk[kKc][kT + 4];
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4] = {};
-  for (int c0 = 0; c0 < d; c0 += kKc) {
-    for (int e = threadIdx.x; e < kT * kKc; e += 256) {
-      const int r = e / kKc, c = e % kKc;
-      const int qi = ti * kT + r, kj = tj * kT + r;
-      sq[c][r] = (qi < nb) ? qh[size_t(qi) * d + c0 + c] : 0.f;
-      sk[c][r] = (kj < nb) ? kg[size_t(kj) * d + c0 + c] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int c = 0; c < kKc; ++c) {
-      float a[4], b[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        a[u] = sq[c][ty * 4 + u];
-        b[u] = sk[c][tx * 4 + u];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(a[u], b[w], acc[u][w]);
-    }
-    __syncthreads();
+  const int tj = t, h = blockIdx.y;
+  const int i0 = ti * kT, j0 = tj * kT;
+  const float4* qh = reinterpret_cast<const float4*>(qbar + size_t(h) * nb * D);
+  const float4* kg = reinterpret_cast<const float4*>(kbar + size_t(h / group) * nb * D);
+  for (int e = threadIdx.x; e < kT * kC; e += 256) {
+    const int r = e / kC, c = e - r * kC;
+    if (i0 + r < nb) cp_async16(&sa[r][swz<kC>(r, c)], qh + size_t(i0 + r) * kC + c);
+    if (j0 + r < nb) cp_async16(&sb[r][swz<kC>(r, c)], kg + size_t(j0 + r) * kC + c);
   }
-  (void)tiles;
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+  // rows past nb hold stale data; they only reach outputs that are not stored
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int ra = 16 * (warp & 3) + gq;        // this lane's tile rows: ra, ra + 8
+  const int cb = 32 * (warp >> 2);            // the warp's tile columns: cb .. cb + 32
+  float acc[4][4];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int i = ti * kT + ty * 4 + u;
-    if (i >= nb) continue;
+  for (int n = 0; n < 4; ++n)
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const int j = tj * kT + tx * 4 + w;
-      if (j <= i) scores[(size_t(h) * nb + i) * nb + j] = acc[u][w] * scale;
+    for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m) {          // dimensions 16m .. 16m + 16: two k-steps
+    const float4 xa = sa[ra][swz<kC>(ra, 4 * m + tq)];
+    const float4 xb = sa[ra + 8][swz<kC>(ra + 8, 4 * m + tq)];
+    uint32_t ah0[4], al0[4], ah1[4], al1[4];
+    split_tf32(xa.x, ah0[0], al0[0]);
+    split_tf32(xb.x, ah0[1], al0[1]);
+    split_tf32(xa.y, ah0[2], al0[2]);
+    split_tf32(xb.y, ah0[3], al0[3]);
+    split_tf32(xa.z, ah1[0], al1[0]);
+    split_tf32(xb.z, ah1[1], al1[1]);
+    split_tf32(xa.w, ah1[2], al1[2]);
+    split_tf32(xb.w, ah1[3], al1[3]);
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const int rn = cb + 8 * n + gq;         // the key block of this lane's B column
+      const float4 y = sb[rn][swz<kC>(rn, 4 * m + tq)];
+      uint32_t bh0, bl0, bh1, bl1, bh2, bl2, bh3, bl3;
+      split_tf32(y.x, bh0, bl0);
+      split_tf32(y.y, bh1, bl1);
+      split_tf32(y.z, bh2, bl2);
+      split_tf32(y.w, bh3, bl3);
+      mma_tf32(acc[n], ah0, bh0, bh1);
+      mma_tf32(acc[n], ah0, bl0, bl1);
+      mma_tf32(acc[n], al0, bh0, bh1);
+      mma_tf32(acc[n], ah1, bh2, bh3);
+      mma_tf32(acc[n], ah1, bl2, bl3);
+      mma_tf32(acc[n], al1, bh2, bh3);
     }
   }
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = i0 + ra + ((e & 2) ? 8 : 0);
+      const int j = j0 + cb + 8 * n + 2 * tq + (e & 1);
+      if (i < nb && j <= i) scores[(size_t(h) * nb + i) * nb + j] = acc[n][e] * scale;
+    }
 }
 
 // Decode scores, persistent: two CTAs per SM walk chunks of 64 pooled key
@@ -151,42 +222,6 @@ struct ScoreStage {
   float4 k[kRows][32];                        // 64 rows x 128 floats, chunks swizzled
   uint2 q[kMaxGroup][32];                     // the group's queries, bf16
 };
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_2() {
-  asm volatile("cp.async.wait_group 2;" ::: "memory");
-}
-// 16-byte chunk c of row r sits at c ^ 4(r mod 8)
-__device__ __forceinline__ int swz(int r, int c) { return c ^ ((r & 7) << 2); }
-
-// x = hi + lo with hi a tf32 value (the 10 leading mantissa bits of x)
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = __float_as_uint(x) & 0xFFFFE000u;
-  lo = __float_as_uint(x - __uint_as_float(hi));
-}
-
-// D += A . B for one m16n8k8 tile (A 16x8 row-major, B 8x8 column-major, tf32)
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
     decode_scores_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ kbar,
@@ -225,7 +260,7 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
       const float4* src = reinterpret_cast<const float4*>(kbar + (size_t(bg) * nb + r0) * D);
       for (int e = tid; e < rows * 32; e += kScoreThreads) {
         const int r = e >> 5;
-        cp_async16(&st[s].k[r][swz(r, e & 31)], src + e);
+        cp_async16(&st[s].k[r][swz<32>(r, e & 31)], src + e);
       }
       const int b = bg / Hkv, g = bg - b * Hkv;
       const uint2* qs = reinterpret_cast<const uint2*>(q + (size_t(b) * Hq + g * group) * D);
@@ -256,8 +291,8 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
         const int hn = n0 + gq;               // the head of this lane's B column
 #pragma unroll
         for (int m = 0; m < 8; ++m) {         // dimensions 16m .. 16m + 16: two k-steps
-          const float4 xa = sg.k[ra][swz(ra, 4 * m + tq)];
-          const float4 xb = sg.k[ra + 8][swz(ra + 8, 4 * m + tq)];
+          const float4 xa = sg.k[ra][swz<32>(ra, 4 * m + tq)];
+          const float4 xb = sg.k[ra + 8][swz<32>(ra + 8, 4 * m + tq)];
           uint2 qb = make_uint2(0u, 0u);
           if (hn < group) qb = sg.q[hn][4 * m + tq];
           const uint32_t q0 = qb.x << 16, q1 = qb.x & 0xFFFF0000u;
@@ -316,7 +351,22 @@ cudaError_t launch_prefill_scores(const float* qbar, const float* kbar, float* s
                                   int group, int nb, int d, float scale, cudaStream_t st) {
   const int tiles = (nb + kT - 1) / kT;
   const dim3 grid(unsigned(tiles * (tiles + 1) / 2), unsigned(Hq));
-  prefill_scores_kernel<<<grid, 256, 0, st>>>(qbar, kbar, scores, nb, d, group, scale, tiles);
+  const int smem = 2 * kT * d * int(sizeof(float));
+  cudaError_t e;
+  if (d == 128) {
+    e = cudaFuncSetAttribute(prefill_scores_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      prefill_scores_kernel<128><<<grid, 256, smem, st>>>(qbar, kbar, scores, nb, group, scale);
+  } else if (d == 64) {
+    e = cudaFuncSetAttribute(prefill_scores_kernel<64>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      prefill_scores_kernel<64><<<grid, 256, smem, st>>>(qbar, kbar, scores, nb, group, scale);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
