@@ -523,6 +523,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_col = C::kO + grp * C::kOCols;
     uint32_t kb = 0, qi = 0, xn = 0;   // xn: uses of the exchange buffer so far
     bool ok = true;
+    // The epilogue of an item (O / l out to memory, O released) runs after the
+    // next item's first block: by then that item's last P.V has finished, so
+    // the wait on it costs nothing, and the next item's first P.V waits for
+    // the release as before.  The last item's epilogue runs after the loop.
+    bool pend = false;
+    ItemInfo pit{};
+    float pl = 0.f, pm = 0.f;
+    uint32_t pq = 0;
+    auto epilogue = [&]() -> bool {
+      // exchange the partial sums (the same double buffer), then O / l for
+      // this group's columns.  o_last has exactly one phase per item, waited
+      // on every time.
+      float* xb = &sh->xch[xn & 1][0][0];
+      xb[grp * 128 + row] = pl;
+      mbar_arrive(&sh->xch_bar);
+      if (!mbar_wait(&sh->o_last, pq & 1, abort) || !mbar_wait(&sh->xch_bar, xn & 1, abort))
+        return false;
+      ++xn;
+      tc_fence_after();
+      const float lt = (xb[row] + xb[128 + row]) + (xb[256 + row] + xb[384 + row]);
+      const float inv_l = 1.f / lt;
+      const bool store = row < p.B;
+      const size_t orow = size_t(pit.h) * p.S + size_t(pit.i) * p.B + size_t(row);
+      const int col = grp * C::kOCols;
+      uint32_t r[C::kOCols];
+      if constexpr (C::kOCols == 32) {
+        tmem_ld32(lanes + o_col, r);
+        tmem_ld_wait(r);
+      } else {
+        tmem_ld16(lanes + o_col, r);
+        tmem_ld_wait(r);
+      }
+      if (store) {
+        if (p.out_f32) {
+          uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + orow * D + col);
+#pragma unroll
+          for (int x = 0; x < C::kOCols / 4; ++x)
+            d4[x] = make_uint4(__float_as_uint(__uint_as_float(r[4 * x]) * inv_l),
+                               __float_as_uint(__uint_as_float(r[4 * x + 1]) * inv_l),
+                               __float_as_uint(__uint_as_float(r[4 * x + 2]) * inv_l),
+                               __float_as_uint(__uint_as_float(r[4 * x + 3]) * inv_l));
+        } else {
+          uint32_t ob[C::kOCols / 2];
+#pragma unroll
+          for (int x = 0; x < C::kOCols / 2; ++x)
+            ob[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
+                                __uint_as_float(r[2 * x + 1]) * inv_l);
+          uint4* d4 =
+              reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
+#pragma unroll
+          for (int x = 0; x < C::kOCols / 8; ++x)
+            d4[x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
+        }
+      }
+      if (p.lse && store && grp == 0)
+        p.lse[orow] = (pm + log2f(lt)) * 0.6931471805599453f;
+      tc_fence_before();
+      mbar_arrive(&sh->o_free);
+      return true;
+    };
     for (;;) {
       const int slot = qi % kNI;
       if (!mbar_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
@@ -685,61 +745,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&sh->p_full[sb]);
         ++kb;
-      }
-      if (!ok) break;
-      // ---- epilogue: exchange the partial sums (the same double buffer), then
-      // O / l for this group's columns.  o_last has exactly one phase per
-      // item, waited on every time.
-      float* xb = &sh->xch[xn & 1][0][0];
-      xb[grp * 128 + row] = l;
-      mbar_arrive(&sh->xch_bar);
-      if (!mbar_wait(&sh->o_last, qi & 1, abort) || !mbar_wait(&sh->xch_bar, xn & 1, abort)) {
-        ok = false;
-        break;
-      }
-      ++xn;
-      tc_fence_after();
-      const float lt = (xb[row] + xb[128 + row]) + (xb[256 + row] + xb[384 + row]);
-      const float inv_l = 1.f / lt;
-      const bool store = row < p.B;
-      const size_t orow = size_t(it.h) * p.S + size_t(it.i) * p.B + size_t(row);
-      const int col = grp * C::kOCols;
-      uint32_t r[C::kOCols];
-      if constexpr (C::kOCols == 32) {
-        tmem_ld32(lanes + o_col, r);
-        tmem_ld_wait(r);
-      } else {
-        tmem_ld16(lanes + o_col, r);
-        tmem_ld_wait(r);
-      }
-      if (store) {
-        if (p.out_f32) {
-          uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + orow * D + col);
-#pragma unroll
-          for (int x = 0; x < C::kOCols / 4; ++x)
-            d4[x] = make_uint4(__float_as_uint(__uint_as_float(r[4 * x]) * inv_l),
-                               __float_as_uint(__uint_as_float(r[4 * x + 1]) * inv_l),
-                               __float_as_uint(__uint_as_float(r[4 * x + 2]) * inv_l),
-                               __float_as_uint(__uint_as_float(r[4 * x + 3]) * inv_l));
-        } else {
-          uint32_t ob[C::kOCols / 2];
-#pragma unroll
-          for (int x = 0; x < C::kOCols / 2; ++x)
-            ob[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
-                                __uint_as_float(r[2 * x + 1]) * inv_l);
-          uint4* d4 =
-              reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
-#pragma unroll
-          for (int x = 0; x < C::kOCols / 8; ++x)
-            d4[x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
+        if (t == 0 && pend) {
+          if (!epilogue()) {
+            ok = false;
+            break;
+          }
+          pend = false;
         }
       }
-      if (p.lse && store && grp == 0)
-        p.lse[orow] = (m_used + log2f(lt)) * 0.6931471805599453f;
-      tc_fence_before();
-      mbar_arrive(&sh->o_free);
+      if (!ok) break;
+      pend = true;
+      pit = it;
+      pl = l;
+      pm = m_used;
+      pq = qi;
       ++qi;
     }
+    if (ok && pend) ok = epilogue();
     if (!ok) raise_abort(sh, p);
   }
 
