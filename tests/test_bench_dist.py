@@ -61,3 +61,37 @@ def test_single_process_is_identity():
 
     assert bench.max_over_ranks(3.5, torch.device("cpu")) == 3.5
     assert bench.job_value(1e12, 1, 4, 2000.0) == pytest.approx(2.0)
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the reference arm times the oracle on the host: one JSON line with the
+    # main arm's metric, unit and config, the host baseline and a zero-copy e2e
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0"], env=env, capture_output=True,
+                         text=True, timeout=600, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    import bench
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is True and line["value"] > 0
+    assert line["config"]["workload"] == "llama31_8b_prefill_128k"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    import subprocess
+    import sys
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0
+    assert r.stdout.strip() == ""
