@@ -363,3 +363,23 @@ def test_decode_block_size_calls_reject_bad_arguments_before_launch(sa):
     assert lib.sparse_attn_score_plan(ctypes.byref(other), plan.handle, P, P, P, None) == 2
     # a forward with sizes needs the plan on the device
     assert lib.sparse_attn_forward(s, plan.handle, P, P, P, P, P, 8, P, 1, None, P, None) == 8
+
+
+@pytest.mark.parametrize("policy", ["lpt", "lpt_grouped"])
+@pytest.mark.parametrize("Hq,Hkv,nb,W,k_u,demand", [
+    (2, 1, 3, 50, 2, None),              # more workers than items
+    (4, 2, 37, 1, 9, [1, 30, 5, 37]),    # one worker takes everything, in walk order
+    (2, 2, 1, 3, 2, None),               # one block per sequence: every cost is 1
+    (8, 2, 64, 256, 20, [2, 64, 3, 60, 5, 40, 2, 64]),   # many workers, very unequal budgets
+    (16, 4, 200, 152, 31, None),         # long runs of equal cost
+])
+def test_plan_lpt_edge_cases_match_oracle(sa, policy, Hq, Hkv, nb, W, k_u, demand):
+    shape = sa.Shape.prefill(nb * 64, 64, Hq, Hkv, 64)
+    plan = sa.sparse_attn_plan(shape, k_u, demand=demand, k_min=2, num_workers=W,
+                               schedule=policy)
+    got = plan.get()
+    k, wptr, items, loads = _oracle_plan(Hq, k_u, demand, 2, nb, W, policy, Hq // Hkv)
+    assert got["budgets"].tolist() == k
+    assert got["wptr"].tolist() == wptr
+    assert got["items"].tolist() == items
+    assert got["loads"].tolist() == loads
