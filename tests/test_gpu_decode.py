@@ -64,11 +64,9 @@ def _check(w, x, r, kinds, budget, window, bf16_out=False):
                                   generate.bf16_to_f32(x["k"][b:b + 1]),
                                   generate.bf16_to_f32(x["v"][b:b + 1]),
                                   r["idx"][b:b + 1], r["cnt"][b:b + 1], w.block)
-        d = np.abs(r["out"][b] - o[0])
-        if bf16_out:
-            d = np.maximum(d - P.half_ulp_bf16(np.maximum(np.abs(o[0]), np.abs(r["out"][b]))), 0)
-        assert d.max() <= P.MAX_ABS, d.max()
-        assert d.sum() / np.abs(o[0]).sum() <= P.MEAN_REL
+        d_max, d_rel = P.output_errors(r["out"][b], o[0], bf16_out)
+        assert d_max.max() <= P.MAX_ABS, d_max.max()
+        assert d_rel.sum() / np.abs(o[0]).sum() <= P.MEAN_REL
         assert np.abs(r["lse"][b] - lse[0]).max() <= P.LSE_ABS
 
 
@@ -93,8 +91,10 @@ def test_decode_full_size(env):
     kinds = generate.head_kinds(w)
     budget = w.budget_tokens // w.block
     window = w.window_tokens // w.block
-    r = _decode(sa, torch, w, x, kinds, budget, window, "bfloat16")
-    _check(w, x, r, kinds, budget, window, bf16_out=True)
+    # fp32 output at the plain tolerance, then bf16 output as well
+    for out_dtype in ("float32", "bfloat16"):
+        r = _decode(sa, torch, w, x, kinds, budget, window, out_dtype)
+        _check(w, x, r, kinds, budget, window, bf16_out=out_dtype == "bfloat16")
 
 
 def _decode_sized(sa, torch, w, x, kinds, gran, budget, window, out_dtype="float32"):
@@ -156,12 +156,9 @@ def _check_sized(w, x, r, kinds, gran, budget, window, bf16_out=False):
             P.check_selection_row(sel, og.select_row(sc[h], min(budget[h], nbh)), sc[h],
                                   nbh - 1)
         o, lse = od.decode_attend(q, k, v, r["idx"][b:b + 1], r["cnt"][b:b + 1], block_of)
-        dd = np.abs(r["out"][b] - o[0])
-        if bf16_out:
-            dd = np.maximum(dd - P.half_ulp_bf16(np.maximum(np.abs(o[0]), np.abs(r["out"][b]))),
-                            0)
-        assert dd.max() <= P.MAX_ABS, dd.max()
-        assert dd.sum() / np.abs(o[0]).sum() <= P.MEAN_REL
+        d_max, d_rel = P.output_errors(r["out"][b], o[0], bf16_out)
+        assert d_max.max() <= P.MAX_ABS, d_max.max()
+        assert d_rel.sum() / np.abs(o[0]).sum() <= P.MEAN_REL
         assert np.abs(r["lse"][b] - lse[0]).max() <= P.LSE_ABS
 
 
@@ -198,8 +195,11 @@ def test_decode_per_head_block_sizes_full_size(env):
     x = generate.decode_inputs(w)
     kinds = generate.head_kinds(w)
     window = w.window_tokens // w.block
-    r = _decode_sized(sa, torch, w, x, kinds, prof["gran"], prof["budget"], window, "bfloat16")
-    _check_sized(w, x, r, kinds, prof["gran"], prof["budget"], window, bf16_out=True)
+    for out_dtype in ("float32", "bfloat16"):
+        r = _decode_sized(sa, torch, w, x, kinds, prof["gran"], prof["budget"], window,
+                          out_dtype)
+        _check_sized(w, x, r, kinds, prof["gran"], prof["budget"], window,
+                     bf16_out=out_dtype == "bfloat16")
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (16, 2), (32, 2)])

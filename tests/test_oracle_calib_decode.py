@@ -41,13 +41,28 @@ def test_coverage_count_brute_force(seed):
     assert got == best
 
 
-def test_uniform_attention_needs_about_ninety_percent():
-    B, nb, d = 8, 16, 4
-    S = B * nb
-    q = np.zeros((S, d))
-    k = np.random.default_rng(1).standard_normal((S, d))
-    rho = calib.head_density(q, k, B)
-    assert 0.80 < rho < 0.95
+@pytest.mark.parametrize("B,nb", [(8, 16), (4, 9), (16, 5)])
+def test_uniform_attention_density_closed_form(B, nb):
+    # q = 0 gives every visible key the same weight: query t puts 1/(t+1) on
+    # each key u <= t.  Block j < i then holds (1/B) sum_t B/(t+1), the
+    # diagonal block (1/B) sum_t (t - iB + 1)/(t+1).  The count for row i is
+    # the fewest of these, largest first, reaching 0.9; the density is the
+    # counts' sum over the causal block total.
+    d = 4
+    q = np.zeros((B * nb, d))
+    k = np.random.default_rng(1).standard_normal((B * nb, d))
+    need = 0
+    for i in range(nb):
+        ts = range(i * B, (i + 1) * B)
+        off = sum(B / (t + 1) for t in ts) / B
+        diag = sum((t - i * B + 1) / (t + 1) for t in ts) / B
+        masses = sorted([off] * i + [diag], reverse=True)
+        acc, c = 0.0, 0
+        while c < len(masses) and acc < 0.9 - 1e-12:
+            acc += masses[c]
+            c += 1
+        need += c
+    assert calib.head_density(q, k, B) == pytest.approx(need / (nb * (nb + 1) / 2), abs=1e-15)
 
 
 def test_peaked_head_needs_fewer_blocks():
