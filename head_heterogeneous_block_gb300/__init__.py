@@ -21,6 +21,7 @@ __all__ = [
     "sparse_attn_score_workspace_size", "sparse_attn_select", "sparse_attn_forward",
     "sparse_attn_pool_kcache", "sa_status_string", "library_path",
     "sparse_attn_select_topp", "sparse_attn_pool_kcache_plan", "sparse_attn_score_plan",
+    "sparse_attn_set_wait_limit",
 ]
 
 SA_OK = 0
@@ -104,6 +105,7 @@ def _load():
                                                           ctypes.POINTER(I32)]),
         "sparse_attn_pool_kcache_plan": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P]),
         "sparse_attn_score_plan": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P]),
+        "sparse_attn_set_wait_limit": (ctypes.c_int, [ctypes.c_uint64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -317,6 +319,13 @@ def sparse_attn_score_plan(shape: Shape, plan: Plan, q, kbar_all, scores, stream
     _check(_lib.sparse_attn_score_plan(ctypes.byref(shape), plan.handle, _ptr(q),
                                        _ptr(kbar_all), _ptr(scores), _stream(stream)),
            "sparse_attn_score_plan")
+
+
+def sparse_attn_set_wait_limit(ns: int):
+    """Limit, in ns, of every wait inside the prefill forward kernel for later
+    launches (0: the 4 s default).  A wait that runs out sets SA_DEV_TIMEOUT in
+    the launch's status word; the kernel cleans up and returns."""
+    _check(_lib.sparse_attn_set_wait_limit(int(ns)), "sparse_attn_set_wait_limit")
 
 
 _noalloc = None

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -45,11 +46,10 @@ void free_device(sa_plan* p) {
   p->device = -1;
 }
 
-sa_status cuda_status(cudaError_t e) {
-  if (e == cudaSuccess) return SA_OK;
-  if (e == cudaErrorMemoryAllocation) return SA_ERR_NO_MEMORY;
-  return SA_ERR_CUDA;
-}
+using sa_k::cuda_status;
+
+// Operational wait limit of the prefill forward, in ns (0: the kernel default).
+std::atomic<uint64_t> g_wait_ns{0};
 
 int64_t nblocks(const sa_shape* s) { return s->seq_len / s->block; }
 
@@ -153,14 +153,9 @@ sa_status sparse_attn_score(const sa_shape* shp, const void* q, const void* k, f
   size_t need = 0;
   sparse_attn_score_workspace_size(shp, &need);
   if (!ws || ws_bytes < need || !aligned16(ws)) return SA_ERR_INVALID_ARG;
-  float* qbar = static_cast<float*>(ws);
-  float* kbar = qbar + size_t(shp->num_q_heads) * nb * d;
-  cudaError_t e = sa_k::launch_pool(q, qbar, int64_t(shp->num_q_heads) * nb, shp->block, d, st);
-  if (e == cudaSuccess)
-    e = sa_k::launch_pool(k, kbar, int64_t(shp->num_kv_heads) * nb, shp->block, d, st);
-  if (e == cudaSuccess)
-    e = sa_k::launch_prefill_scores(qbar, kbar, scores, shp->num_q_heads, G, nb, d, scale, st);
-  return cuda_status(e);
+  return cuda_status(sa_k::launch_prefill_index(q, k, scores, static_cast<float*>(ws),
+                                                shp->num_q_heads, shp->num_kv_heads, nb,
+                                                shp->block, d, st));
 }
 
 sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const float* scores,
@@ -310,10 +305,16 @@ sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const vo
   a.out_f32 = o_dtype == SA_DTYPE_F32;
   a.lse = lse;
   a.dev_status = dev_status;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   bool encode_failed = false;
   cudaError_t e = sa_k::launch_prefill_attention(a, st, &encode_failed);
   if (encode_failed) return SA_ERR_CUDA;
   return cuda_status(e);
+}
+
+sa_status sparse_attn_set_wait_limit(uint64_t ns) {
+  g_wait_ns.store(ns, std::memory_order_relaxed);
+  return SA_OK;
 }
 
 sa_status sparse_attn_pool_kcache(const sa_shape* shp, const void* k, float* kbar,

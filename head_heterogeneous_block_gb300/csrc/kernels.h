@@ -6,7 +6,16 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "sparse_attn.h"
+
 namespace sa_k {
+
+// A CUDA error as the ABI's status: allocation failures keep their own code.
+inline sa_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SA_OK;
+  if (e == cudaErrorMemoryAllocation) return SA_ERR_NO_MEMORY;
+  return SA_ERR_CUDA;
+}
 
 // Mean of each block of `block` rows: x [rows*block][d] bf16 -> out [rows][d] fp32.
 cudaError_t launch_pool(const void* x, float* out, int64_t rows, int block, int d,
@@ -15,6 +24,12 @@ cudaError_t launch_pool(const void* x, float* out, int64_t rows, int block, int 
 // Prefill block scores for j <= i (scores [Hq][nb][nb], upper part untouched).
 cudaError_t launch_prefill_scores(const float* qbar, const float* kbar, float* scores, int Hq,
                                   int group, int nb, int d, float scale, cudaStream_t st);
+
+// The whole prefill Index step: pool Q into ws, pool K after it, then score
+// every block pair j <= i with scale 1/sqrt(d).  ws holds (Hq + Hkv) * nb * d
+// floats: the pooled queries first, then the pooled keys.
+cudaError_t launch_prefill_index(const void* q, const void* k, float* scores, float* ws, int Hq,
+                                 int Hkv, int nb, int block, int d, cudaStream_t st);
 
 // Decode scores [Bt][Hq][nb] from q [Bt][Hq][d] (bf16) and kbar [Bt][Hkv][nb][d].
 // nb pooled rows per (sequence, KV head) at this pass's block size; score
@@ -83,6 +98,7 @@ struct PrefillArgs {
   int32_t out_f32;          // 1: o is fp32, 0: bf16
   float* lse;
   int32_t* dev_status;
+  uint64_t wait_ns;         // limit of each operational wait (0: the 4 s default)
 };
 // Returns cudaSuccess, or an error; *encode_failed is set when a TMA
 // descriptor could not be built.

@@ -115,6 +115,7 @@ struct Params {
   int32_t out_f32;
   float* lse;
   int32_t* dev_status;
+  uint64_t wait_ns;   // limit of every operational wait; drains keep kWaitLimitNs
 };
 
 __device__ __forceinline__ void raise_abort(Shared* sh, const Params& p) {
@@ -236,12 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // publish the item's metadata for the MMA, V-producer and softmax warps
         const int slot = qi % kNI;
         if (qi >= uint32_t(kNI) &&
-            !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort))
+            !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort, p.wait_ns))
           ok = false;
         if (ok) {
           sh->info[slot] = ItemInfo{h, i, n, jlast == i ? 1 : 0};
           mbar_arrive(&sh->info_full[slot]);
-          if (qi >= 1 && !mbar_wait(&sh->q_empty[0], (qi - 1) & 1, abort)) ok = false;
+          if (qi >= 1 && !mbar_wait(&sh->q_empty[0], (qi - 1) & 1, abort, p.wait_ns)) ok = false;
           if (ok) {
             mbar_arrive_expect_tx(&sh->q_full[0], C::kQBytes);
 #pragma unroll
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int ks = kiss % C::kNK;
           if (kiss >= uint32_t(C::kNK) &&
-              !mbar_wait(&sh->k_empty[ks], ((kiss / C::kNK) - 1) & 1, abort))
+              !mbar_wait(&sh->k_empty[ks], ((kiss / C::kNK) - 1) & 1, abort, p.wait_ns))
             ok = false;
           if (ok) {
             mbar_arrive_expect_tx(&sh->k_full[ks], C::kKVBytes);
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // end marker for the consumers
         const int slot = qi % kNI;
         if (qi >= uint32_t(kNI) &&
-            !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort))
+            !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort, p.wait_ns))
           ok = false;
         if (ok) {
           sh->info[slot] = ItemInfo{0, 0, 0, 0};
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (;;) {
       const int slot = qi % kNI;
-      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const int vs = viss % C::kNV;
           if (viss >= uint32_t(C::kNV) &&
-              !mbar_wait(&sh->v_empty[vs], ((viss / C::kNV) - 1) & 1, abort))
+              !mbar_wait(&sh->v_empty[vs], ((viss / C::kNV) - 1) & 1, abort, p.wait_ns))
             ok = false;
           if (ok) {
             mbar_arrive_expect_tx(&sh->v_full[vs], C::kKVBytes);
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (;;) {
       const int slot = qi % kNI;
-      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->info_empty[slot]);
       if (n == 0) break;
-      if (!warp_wait(&sh->q_full[0], qi & 1, abort)) {
+      if (!warp_wait(&sh->q_full[0], qi & 1, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -390,11 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           par = phase ^ 1u;
         }
         const uint32_t have = __ballot_sync(0xffffffffu, mbar_test(bar, par));
-        if (!(have & 1u) && !warp_wait(&sh->k_full[stage], phase, abort)) {
+        if (!(have & 1u) && !warp_wait(&sh->k_full[stage], phase, abort, p.wait_ns)) {
           ok = false;
           break;
         }
-        if (reuse && !(have & 2u) && !warp_wait(&sh->pv_done[stage], phase ^ 1u, abort)) {
+        if (reuse && !(have & 2u) && !warp_wait(&sh->pv_done[stage], phase ^ 1u, abort, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (;;) {
       const int slot = qi % kNI;
-      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+      if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -463,15 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           par = (qi - 1) & 1;
         }
         const uint32_t have = __ballot_sync(0xffffffffu, mbar_test(bar, par));
-        if (!(have & 1u) && !warp_wait(&sh->p_full[stage], phase, abort)) {
+        if (!(have & 1u) && !warp_wait(&sh->p_full[stage], phase, abort, p.wait_ns)) {
           ok = false;
           break;
         }
-        if (!(have & 2u) && !warp_wait(&sh->v_full[vstage], vphase, abort)) {
+        if (!(have & 2u) && !warp_wait(&sh->v_full[vstage], vphase, abort, p.wait_ns)) {
           ok = false;
           break;
         }
-        if (need_o && !(have & 4u) && !warp_wait(&sh->o_free, (qi - 1) & 1, abort)) {
+        if (need_o && !(have & 4u) && !warp_wait(&sh->o_free, (qi - 1) & 1, abort, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -538,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* xb = &sh->xch[xn & 1][0][0];
       xb[grp * 128 + row] = pl;
       mbar_arrive(&sh->xch_bar);
-      if (!mbar_wait(&sh->o_last, pq & 1, abort) || !mbar_wait(&sh->xch_bar, xn & 1, abort))
+      if (!wait_all(&sh->o_last, pq & 1, abort, p.wait_ns) || !wait_all(&sh->xch_bar, xn & 1, abort, p.wait_ns))
         return false;
       ++xn;
       tc_fence_after();
@@ -585,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (;;) {
       const int slot = qi % kNI;
-      if (!mbar_wait(&sh->info_full[slot], (qi / kNI) & 1, abort)) {
+      if (!wait_all(&sh->info_full[slot], (qi / kNI) & 1, abort, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int t = 0; t < it.n; ++t) {
         const int sb = kb % C::kNS;
-        if (!mbar_wait(&sh->s_full[sb], (kb / C::kNS) & 1, abort)) {
+        if (!wait_all(&sh->s_full[sb], (kb / C::kNS) & 1, abort, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -639,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh->xch_bar);
         if (t == 0) {
           // first block of the item: the row maximum must be known first
-          if (!mbar_wait(&sh->xch_bar, xn & 1, abort)) {
+          if (!wait_all(&sh->xch_bar, xn & 1, abort, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -673,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (t > 0) {
-          if (!mbar_wait(&sh->xch_bar, xn & 1, abort)) {
+          if (!wait_all(&sh->xch_bar, xn & 1, abort, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -686,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // was reused only after P.V of block kb-3 completed, and P.V of
             // block kb+2 cannot have run.
             const uint32_t pb = kb - 1;
-            if (!mbar_wait(&sh->pv_done[pb % C::kNS], (pb / C::kNS) & 1, abort)) {
+            if (!wait_all(&sh->pv_done[pb % C::kNS], (pb / C::kNS) & 1, abort, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -763,6 +764,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && pend) ok = epilogue();
     if (!ok) raise_abort(sh, p);
+    // a role that gave up may have left a tensor-memory access in flight; all
+    // of them end before the allocation is freed below
+    tmem_ld_wait();
+    tmem_st_wait();
+    tc_fence_before();
   }
 
   __syncthreads();
@@ -837,6 +843,7 @@ cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_fai
   p.out_f32 = a.out_f32;
   p.lse = a.lse;
   p.dev_status = a.dev_status;
+  p.wait_ns = a.wait_ns ? a.wait_ns : kWaitLimitNs;
   auto kern = prefill_attention_kernel<D, BK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;

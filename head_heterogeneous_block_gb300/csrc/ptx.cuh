@@ -1,8 +1,9 @@
 // Inline-PTX building blocks for sm_103a: mbarriers, TMA tile loads, and the
 // tcgen05 tensor-core path (TMEM allocation, MMA issue/commit, TMEM load and
-// store).  Every wait here is bounded: it gives up after kWaitLimitNs of
-// global time (or when another role raised the CTA's abort flag) and reports
-// failure to the caller instead of spinning forever.
+// store).  Every wait here is bounded: it gives up after a limit of global
+// time (kWaitLimitNs unless the caller passes its own), or when another role
+// raised the CTA's abort flag, and reports failure to the caller instead of
+// spinning forever.
 #pragma once
 
 #include <cstdint>
@@ -10,7 +11,7 @@
 
 namespace sa_dev {
 
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per wait
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per wait (the default)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -71,14 +72,18 @@ __device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, 
 }
 
 // Wait until the phase with the given parity has completed.  Returns false if
-// the wait gave up (time limit, or *abort set by another role).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// the wait gave up (time limit, or *abort set by another role).  The hardware
+// suspend between polls is capped by the limit, so a short limit is honoured
+// at about its own scale.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
+  const uint32_t hint = limit_ns < 20000u ? uint32_t(limit_ns) : 20000u;
   for (;;) {
-    if (mbar_test_sleep(bar, parity, 20000u)) return true;
+    if (mbar_test_sleep(bar, parity, hint)) return true;
     if (abort && *abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -94,10 +99,18 @@ __device__ __forceinline__ bool elect_one() {
 
 // Lane 0 waits (bounded), the warp learns the outcome; __shfl_sync also
 // orders the other lanes' later shared-memory reads after the wait.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort);
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, limit_ns);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Every lane waits; the warp gives up together if any lane gave up, so that
+// no lane goes on alone into a warp-collective (.sync.aligned) instruction.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         uint64_t limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit_ns));
 }
 
 // ---------------------------------------------------------------- TMA

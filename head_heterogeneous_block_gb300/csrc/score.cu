@@ -21,6 +21,7 @@
 
 #include <cuda_bf16.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "kernels.h"
@@ -368,6 +369,18 @@ cudaError_t launch_prefill_scores(const float* qbar, const float* kbar, float* s
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_index(const void* q, const void* k, float* scores, float* ws, int Hq,
+                                 int Hkv, int nb, int block, int d, cudaStream_t st) {
+  float* qbar = ws;
+  float* kbar = qbar + size_t(Hq) * nb * d;
+  cudaError_t e = launch_pool(q, qbar, int64_t(Hq) * nb, block, d, st);
+  if (e == cudaSuccess) e = launch_pool(k, kbar, int64_t(Hkv) * nb, block, d, st);
+  if (e == cudaSuccess)
+    e = launch_prefill_scores(qbar, kbar, scores, Hq, Hq / Hkv, nb, d,
+                              float(1.0 / std::sqrt(double(d))), st);
+  return e;
 }
 
 cudaError_t launch_decode_scores(const void* q, const float* kbar, float* scores, int Bt, int Hq,

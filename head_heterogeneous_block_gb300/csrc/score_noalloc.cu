@@ -7,9 +7,17 @@
 // by their own pool allocator and hand plugins only the input and output
 // buffers, and callers running with a fixed memory budget set at start-up.
 // For them this entry point keeps the pooled vectors in one fixed area of
-// device memory that is part of this library's module: every device that
-// loads the library holds those kNoAllocScratchBytes until the process exits,
-// and the call itself allocates nothing.
+// device memory that is part of this file's module.  CUDA loads modules
+// lazily by default, so a device reserves those kNoAllocScratchBytes at the
+// first call on it (at library load when modules load eagerly) and keeps them
+// until the process exits; the call itself allocates nothing.
+//
+// The first call on a device looks the area's address up, with that device
+// current, and may load the module: make it before any stream capture.  The
+// address is kept for the life of the process, so after cudaDeviceReset (or
+// any other teardown of the device's primary context) this entry point must
+// not be called again in that process: the module is reloaded elsewhere and
+// the kept address would be stale.
 //
 // The area is shared by every call on a device and keeps whatever the last
 // call left in it.  Nothing in it needs to start at zero: each call
@@ -20,7 +28,6 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
-#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -76,17 +83,9 @@ extern "C" sa_status sparse_attn_score_noalloc(const sa_shape* shp, const void* 
   void* ws = nullptr;
   s = scratch_address(&ws);
   if (s != SA_OK) return s;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int nb = int(shp->seq_len / shp->block);
-  const int d = shp->head_dim;
-  const int G = shp->num_q_heads / shp->num_kv_heads;
-  float* qbar = static_cast<float*>(ws);
-  float* kbar = qbar + size_t(shp->num_q_heads) * nb * d;
-  cudaError_t e = sa_k::launch_pool(q, qbar, int64_t(shp->num_q_heads) * nb, shp->block, d, st);
-  if (e == cudaSuccess)
-    e = sa_k::launch_pool(k, kbar, int64_t(shp->num_kv_heads) * nb, shp->block, d, st);
-  if (e == cudaSuccess)
-    e = sa_k::launch_prefill_scores(qbar, kbar, scores, shp->num_q_heads, G, nb, d,
-                                    float(1.0 / std::sqrt(double(d))), st);
-  return e == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+  // the same stages as sparse_attn_score, with the area as the workspace
+  return sa_k::cuda_status(sa_k::launch_prefill_index(
+      q, k, scores, static_cast<float*>(ws), shp->num_q_heads, shp->num_kv_heads,
+      int(shp->seq_len / shp->block), shp->block, shp->head_dim,
+      reinterpret_cast<cudaStream_t>(stream)));
 }

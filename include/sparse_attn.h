@@ -244,16 +244,20 @@ sa_status sparse_attn_score(const sa_shape* shp, const void* q, const void* k,
  * through their own pool and hand a plugin only its inputs and outputs, and
  * callers held to a memory budget fixed at start-up.  It computes exactly what
  * sparse_attn_score computes, but keeps the pooled queries and keys in a
- * fixed 32 MiB area of device memory that belongs to this library (every
- * device that loads the library holds it until the process exits); the call
- * allocates nothing and takes no workspace.  The pages have no counterpart of
+ * fixed 32 MiB area of device memory that belongs to this library; the call
+ * allocates nothing and takes no workspace.  A device reserves the area at the
+ * first call on it (at library load when CUDA loads modules eagerly) and keeps
+ * it until the process exits.  The pages have no counterpart of
  * this entry point; it exists for deployment only.
  *  - Limit: prefill shapes with (Hq + Hkv) * nb * d * 4 bytes <= 32 MiB (the
  *    Llama-3.1-8B 128K shape needs 20 MiB); larger ones return
  *    SA_ERR_UNSUPPORTED.  Decode shapes need no scratch and behave as
  *    sparse_attn_score.
  *  - The first call on each device looks up the area's device address with
- *    that device current; make that first call before any stream capture.
+ *    that device current, and may load the module that holds it; make that
+ *    first call before any stream capture.  The address is kept for the life
+ *    of the process: do not call this entry point again after cudaDeviceReset
+ *    or any other teardown of the device's primary context.
  *  - All calls on a device share the area.  Each call rewrites every pooled
  *    vector it reads, so nothing has to be cleared, but calls whose execution
  *    overlaps on the GPU (other streams, other host threads) race on it:
@@ -329,6 +333,21 @@ sa_status sparse_attn_plan_rebuild(sa_plan* plan, const int32_t* cnt, sa_stream_
  */
 sa_status sparse_attn_plan_device_schedule(const sa_plan* plan, int32_t* wptr,
                                            int32_t* items, sa_stream_t stream);
+
+/*
+ * Watchdog limit of the prefill forward kernel: every wait of one role on
+ * another (a copy landing, a tensor-core result, a softmax step) gives up
+ * after `ns` nanoseconds of GPU global time, for launches made after this
+ * call by any thread of the process.  0 restores the default, 4 s.
+ * A CTA whose wait runs out ORs SA_DEV_TIMEOUT into dev_status, stops every
+ * role of the CTA, lets the copies and tensor-core operations it already
+ * issued complete (those waits keep the 4 s limit), frees its tensor memory
+ * and exits: the launch ends with invalid output but the context stays
+ * usable.  Callers that would rather see an error than a stalled stream set
+ * a limit near their own deadline; short limits also let a test take this
+ * path on purpose.  Returns SA_OK.
+ */
+sa_status sparse_attn_set_wait_limit(uint64_t ns);
 
 /*
  * Attention over the selected blocks.
