@@ -32,6 +32,7 @@ SCHEDULES = {"lpt": SA_SCHED_LPT, "lpt_grouped": SA_SCHED_LPT_GROUPED,
 SA_HEAD_RETRIEVAL, SA_HEAD_STREAMING = 0, 1
 SA_DTYPE_BF16, SA_DTYPE_F32 = 0, 1
 SA_DEV_BAD_INDEX, SA_DEV_BAD_COUNT, SA_DEV_TIMEOUT, SA_DEV_BAD_ITEM, SA_DEV_BAD_LAUNCH = 1, 2, 4, 8, 16
+SA_DEV_RANGE = 32
 
 
 class Shape(ctypes.Structure):

@@ -83,7 +83,12 @@ constexpr int kThreads = 128 + kSoftmaxThreads;
 
 struct ItemInfo {
   int32_t h, i, n, diag_last;   // n == 0: end of this worker's list
+  int32_t pos;                  // position in this worker's list
 };
+
+// Items of a worker's list whose rows the exact pass recomputes, one bit per
+// list position (lists longer than this report SA_DEV_RANGE instead).
+constexpr int kRedoWords = 1024;
 
 struct Shared {
   uint64_t q_full[1], q_empty[1];
@@ -91,13 +96,14 @@ struct Shared {
   uint64_t v_full[3], v_empty[3];
   uint64_t s_full[3];     // S of block b is in TMEM buffer b % 3
   uint64_t p_full[3];     // P of block b written (every softmax group)
-  uint64_t pv_done[3];    // P.V of block b complete (waited only before an O rescale)
+  uint64_t pv_done[3];    // P.V of block b complete (its S buffer may be rewritten)
   uint64_t o_last;        // one phase per item, after its last P.V (epilogue)
   uint64_t o_free;        // one phase per item: every group finished the epilogue
   uint64_t xch_bar;       // exchange between the softmax groups
   uint64_t drain_qk, drain_pv;
   uint64_t info_full[kNI], info_empty[kNI];
   ItemInfo info[kNI];
+  uint32_t redo[kRedoWords];
   float xch[2][4][128];   // [use parity][group][row]: partial row max per block, or
                           // partial sum per item; use u goes to buffer u & 1
   uint32_t tmem_base;
@@ -105,6 +111,9 @@ struct Shared {
 };
 
 struct Params {
+  const __nv_bfloat16* q;   // [Hq*S][D], [Hkv*S][D], [Hkv*S][D]: read only by exact_row
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
   const int32_t* idx;
   const int32_t* cnt;
   const int32_t* wptr;
@@ -133,6 +142,62 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t issued, int 
 // A block index as both producers use it: out-of-range entries become block 0.
 __device__ __forceinline__ int32_t clamp_block(int32_t j, int32_t i) {
   return (j < 0 || j > i) ? 0 : j;
+}
+
+// Exact attention of one query row of item (h, i) over the item's selected
+// blocks, for output columns [col0, col0 + NC): two passes in fp32 on the
+// CUDA cores, the row's maximum first, then the weights, their sum and the
+// weighted values.  It serves only rows whose sum left the range of the
+// tensor-core pass (a later block scoring far above the item's first block,
+// or values so large that O overflowed), so it favours plainness over speed.
+template <int D, int BK, int NC>
+__device__ __noinline__ void exact_row(const Params& p, int32_t h, int32_t i, int32_t n,
+                                       int row, int col0, bool write_lse) {
+  const size_t orow = size_t(h) * p.S + size_t(i) * p.B + size_t(row);
+  const __nv_bfloat16* q = p.q + orow * D;
+  const size_t kv0 = size_t(h / p.G) * p.S;
+  const int32_t* list = p.idx + (size_t(h) * p.nb + i) * size_t(p.kmax);
+  const float c = p.scale_log2;
+  float m = -INFINITY;
+  for (int t = 0; t < n; ++t) {
+    const int32_t j = clamp_block(list[t], i);
+    const int keys = j == i ? row + 1 : BK;   // causal inside the diagonal block
+    for (int u = 0; u < keys; ++u) {
+      const __nv_bfloat16* kr = p.k + (kv0 + size_t(j) * BK + u) * D;
+      float sc = 0.f;
+#pragma unroll 8
+      for (int x = 0; x < D; ++x) sc = fmaf(__bfloat162float(q[x]), __bfloat162float(kr[x]), sc);
+      m = fmaxf(m, sc * c);
+    }
+  }
+  float l = 0.f, acc[NC];
+#pragma unroll
+  for (int x = 0; x < NC; ++x) acc[x] = 0.f;
+  for (int t = 0; t < n; ++t) {
+    const int32_t j = clamp_block(list[t], i);
+    const int keys = j == i ? row + 1 : BK;
+    for (int u = 0; u < keys; ++u) {
+      const size_t key = kv0 + size_t(j) * BK + u;
+      const __nv_bfloat16* kr = p.k + key * D;
+      float sc = 0.f;
+#pragma unroll 8
+      for (int x = 0; x < D; ++x) sc = fmaf(__bfloat162float(q[x]), __bfloat162float(kr[x]), sc);
+      const float w = ex2(sc * c - m);
+      l += w;
+      const __nv_bfloat16* vr = p.v + key * D + col0;
+#pragma unroll
+      for (int x = 0; x < NC; ++x) acc[x] = fmaf(w, __bfloat162float(vr[x]), acc[x]);
+    }
+  }
+  const float inv_l = 1.f / l;
+  if (p.out_f32) {
+    float* o = static_cast<float*>(p.o) + orow * D + col0;
+    for (int x = 0; x < NC; ++x) o[x] = acc[x] * inv_l;
+  } else {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.o) + orow * D + col0;
+    for (int x = 0; x < NC; ++x) o[x] = __float2bfloat16_rn(acc[x] * inv_l);
+  }
+  if (write_lse && p.lse) p.lse[orow] = (m + log2f(l)) * 0.6931471805599453f;
 }
 
 template <int D, int BK>
@@ -181,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh->abort = 0;
     fence_mbar_init();
   }
+  for (int x = threadIdx.x; x < kRedoWords; x += kThreads) sh->redo[x] = 0;
   if (warp == 1) {
     tmem_alloc(&sh->tmem_base, C::kTmemCols);
     tmem_relinquish();
@@ -240,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort, p.wait_ns))
           ok = false;
         if (ok) {
-          sh->info[slot] = ItemInfo{h, i, n, jlast == i ? 1 : 0};
+          sh->info[slot] = ItemInfo{h, i, n, jlast == i ? 1 : 0, pos - begin};
           mbar_arrive(&sh->info_full[slot]);
           if (qi >= 1 && !mbar_wait(&sh->q_empty[0], (qi - 1) & 1, abort, p.wait_ns)) ok = false;
           if (ok) {
@@ -300,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait(&sh->info_empty[slot], ((qi / kNI) - 1) & 1, abort, p.wait_ns))
           ok = false;
         if (ok) {
-          sh->info[slot] = ItemInfo{0, 0, 0, 0};
+          sh->info[slot] = ItemInfo{0, 0, 0, 0, 0};
           mbar_arrive(&sh->info_full[slot]);
         }
       }
@@ -556,7 +622,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(lanes + o_col, r);
         tmem_ld_wait(r);
       }
-      if (store) {
+      // the range the tensor-core pass keeps: every weight below 2^100 (so
+      // neither P nor l can overflow) and O finite; beyond it the row's
+      // columns are recomputed exactly
+      float osum = 0.f;
+#pragma unroll
+      for (int x = 0; x < C::kOCols; ++x) osum += __uint_as_float(r[x]);
+      const bool in_range = lt <= 0x1p100f && fabsf(osum) <= 3.0e38f;
+      if (store && !in_range) {
+        // the whole item is recomputed after the list (the bit is set by
+        // every thread that finds a row out of range; one is enough)
+        if (pit.pos < 32 * kRedoWords)
+          atomicOr(&sh->redo[pit.pos >> 5], 1u << (pit.pos & 31));
+        else
+          atomicOr(p.dev_status, SA_DEV_RANGE);
+      } else if (store) {
         if (p.out_f32) {
           uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + orow * D + col);
 #pragma unroll
@@ -577,9 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = 0; x < C::kOCols / 8; ++x)
             d4[x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
         }
+        if (p.lse && grp == 0) p.lse[orow] = (pm + log2f(lt)) * 0.6931471805599453f;
       }
-      if (p.lse && store && grp == 0)
-        p.lse[orow] = (pm + log2f(lt)) * 0.6931471805599453f;
       tc_fence_before();
       mbar_arrive(&sh->o_free);
       return true;
@@ -623,33 +702,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = 0; x < C::kCols; ++x)
             if (grp * C::kCols + x > row) s[x] = -INFINITY;
         }
-        // partial row maximum over four independent chains
-        float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-        for (int x = 4; x + 8 <= C::kCols; x += 8)
-#pragma unroll
-          for (int a = 0; a < 4; ++a) mx[a] = max3(mx[a], s[x + a], s[x + 4 + a]);
-#pragma unroll
-        for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], s[C::kCols - 4 + a]);
-        const float mine = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
-        // Exchange with the other groups.  Use xn writes buffer xn & 1: every
-        // thread read use xn-2 before it posted use xn-1, and this thread saw
-        // use xn-1 complete, so that buffer is free.
-        float* xb = &sh->xch[xn & 1][0][0];
-        xb[grp * 128 + row] = mine;
-        mbar_arrive(&sh->xch_bar);
         if (t == 0) {
-          // first block of the item: the row maximum must be known first
+          // first block of the item: its row maximum, exchanged between the
+          // groups, is the reference every block of the item uses.  Use xn
+          // writes buffer xn & 1: every thread read use xn-2 before it posted
+          // use xn-1, and this thread saw use xn-1 complete, so that buffer
+          // is free.
+          float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+          for (int x = 4; x + 8 <= C::kCols; x += 8)
+#pragma unroll
+            for (int a = 0; a < 4; ++a) mx[a] = max3(mx[a], s[x + a], s[x + 4 + a]);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) mx[a] = fmaxf(mx[a], s[C::kCols - 4 + a]);
+          float* xb = &sh->xch[xn & 1][0][0];
+          xb[grp * 128 + row] = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
+          mbar_arrive(&sh->xch_bar);
           if (!wait_all(&sh->xch_bar, xn & 1, abort, p.wait_ns)) {
             ok = false;
             break;
           }
           m_used = max3(fmaxf(xb[row], xb[128 + row]), xb[256 + row], xb[384 + row]) * c;
+          ++xn;
         }
-        // P = 2^(s*c - m) in bf16 with the running maximum m_used, written
-        // over this group's S columns.  When the exchange shows that the
-        // block raised a row's maximum by more than 2^8 (rare), that row's P
-        // and sum are scaled down after O is.
+        // P = 2^(s*c - m) in bf16 with the item's reference maximum m_used,
+        // written over this group's S columns.  Later blocks may score above
+        // it: their weights exceed 1 but stay exact in bf16 and fp32, the
+        // reference cancels in O / l, and no group has to wait for another.
+        // A row whose sum leaves the range checked at the end of the item is
+        // recomputed exactly.
         float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
         {
           uint32_t pk[C::kCols / 2];
@@ -673,74 +754,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st8(lanes + scol, pk);
           }
         }
-        if (t > 0) {
-          if (!wait_all(&sh->xch_bar, xn & 1, abort, p.wait_ns)) {
-            ok = false;
-            break;
-          }
-          const float m_blk =
-              max3(fmaxf(xb[row], xb[128 + row]), xb[256 + row], xb[384 + row]) * c;
-          const bool need = m_blk > m_used + 8.0f;
-          if (__any_sync(0xffffffffu, need)) {
-            // O still receives P V of the previous block: let it finish first.
-            // pv_done[(kb-1) % 3] is unambiguous here: this block's S buffer
-            // was reused only after P.V of block kb-3 completed, and P.V of
-            // block kb+2 cannot have run.
-            const uint32_t pb = kb - 1;
-            if (!wait_all(&sh->pv_done[pb % C::kNS], (pb / C::kNS) & 1, abort, p.wait_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            float alpha = 1.f;
-            if (need) {
-              alpha = ex2(m_used - m_blk);
-              m_used = m_blk;
-              l *= alpha;
-            }
-            if constexpr (C::kOCols == 32) {
-              uint32_t r[32];
-              tmem_ld32(lanes + o_col, r);
-              tmem_ld_wait(r);
-#pragma unroll
-              for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-              tmem_st32(lanes + o_col, r);
-            } else {
-              uint32_t r[16];
-              tmem_ld16(lanes + o_col, r);
-              tmem_ld_wait(r);
-#pragma unroll
-              for (int x = 0; x < 16; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-              tmem_st16(lanes + o_col, r);
-            }
-            tmem_st_wait();
-            // this row's P (already in TMEM) is scaled the same way; rows
-            // that keep their maximum scale by 1
-            float t0 = 0.f, t1 = 0.f;
-            uint32_t r[16];
-            tmem_ld16(lanes + scol, r);      // kCols / 2 <= 16 words used
-            tmem_ld_wait(r);
-#pragma unroll
-            for (int x = 0; x < C::kCols / 2; ++x) {
-              r[x] = pack_bf16x2(__uint_as_float(r[x] << 16) * alpha,
-                                 __uint_as_float(r[x] & 0xFFFF0000u) * alpha);
-              t0 += __uint_as_float(r[x] << 16);
-              t1 += __uint_as_float(r[x] & 0xFFFF0000u);
-            }
-            if constexpr (C::kCols == 32) {
-              tmem_st16(lanes + scol, r);
-            } else {
-              uint32_t w[8];
-#pragma unroll
-              for (int x = 0; x < 8; ++x) w[x] = r[x];
-              tmem_st8(lanes + scol, w);
-            }
-            sum0 = t0;
-            sum1 = t1;
-            sum2 = sum3 = 0.f;
-          }
-        }
-        ++xn;
         tmem_st_wait();
         l += (sum0 + sum1) + (sum2 + sum3);
         tc_fence_before();
@@ -764,6 +777,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && pend) ok = epilogue();
     if (!ok) raise_abort(sh, p);
+    // every epilogue of the list has set its bits: recompute the marked items,
+    // one (row, column group) per thread
+    asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
+    if (ok && row < p.B) {
+      const int32_t begin = p.wptr[blockIdx.x];
+      for (int w = 0; w < kRedoWords; ++w) {
+        uint32_t bits = sh->redo[w];
+        while (bits) {
+          const int32_t pos = begin + 32 * w + __ffs(bits) - 1;
+          bits &= bits - 1;
+          const int32_t item = p.items[pos];
+          const int32_t h = item / p.nb, i = item - h * p.nb;
+          const int32_t n = max(1, min(p.cnt[item], min(p.kmax, i + 1)));
+          exact_row<D, BK, C::kOCols>(p, h, i, n, row, grp * C::kOCols, grp == 0);
+        }
+      }
+    }
     // a role that gave up may have left a tensor-memory access in flight; all
     // of them end before the allocation is freed below
     tmem_ld_wait();
@@ -827,6 +857,9 @@ cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_fai
     return cudaErrorInvalidValue;
   }
   Params p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.k = static_cast<const __nv_bfloat16*>(a.k);
+  p.v = static_cast<const __nv_bfloat16*>(a.v);
   p.idx = a.idx;
   p.cnt = a.cnt;
   p.wptr = a.wptr;

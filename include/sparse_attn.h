@@ -88,8 +88,12 @@ enum {
   SA_DEV_BAD_COUNT = 2,      /* a block count outside [1, min(kmax,i+1)]     */
   SA_DEV_TIMEOUT = 4,        /* a bounded wait gave up; outputs are invalid  */
   SA_DEV_BAD_ITEM = 8,       /* a schedule entry outside the item range      */
-  SA_DEV_BAD_LAUNCH = 16     /* the kernel found its shared memory misaligned
+  SA_DEV_BAD_LAUNCH = 16,    /* the kernel found its shared memory misaligned
                                 and did nothing; outputs are not written     */
+  SA_DEV_RANGE = 32          /* rows beyond the tensor-core pass's range
+                                (weights above 2^100 or O overflowed) could
+                                not all be recomputed exactly: a worker list
+                                longer than 32768 items; outputs invalid     */
 };
 
 typedef struct sa_shape {

@@ -160,6 +160,34 @@ def test_corrupt_indices_are_flagged_not_dereferenced(env):
     assert torch.isfinite(layer.out.float()).all()
 
 
+@pytest.mark.parametrize("factor,exact", [(3.0, False), (30.0, True)])
+def test_later_blocks_scoring_far_above_the_first(env, factor, exact):
+    """The forward takes each row's maximum from the item's first block and
+    keeps it; a later block that scores higher only makes the weights exceed
+    1.  A key planted along one query (k = factor * q) makes later blocks
+    score about factor * |q|^2 / sqrt(d) above the rest: with factor 3 the
+    weights reach ~2^50 and stay on the tensor-core pass; with factor 30 they
+    overflow, and every affected item is recomputed exactly.  Both must match
+    the oracle at the plain tolerance, output and log-sum-exp."""
+    sa, torch = env
+    from tests import _parity as P
+    from workloads import generate, scaled, workload
+    w = scaled(workload(2), 4096, 8, 2)
+    x = generate.prefill_inputs(w)
+    h, i, r, j, u = 1, 20, 5, 10, 7          # query row (h, 128 i + r); key 128 j + u
+    q_row = generate.bf16_to_f32(x["q"][h, i * w.block + r])
+    k = x["k"].copy()
+    k[h // w.group, j * w.block + u] = generate.bf16_bits(q_row * factor)
+    x = dict(x, k=k)
+    rr = _run(sa, torch, w, x, {"k_uniform": w.nb}, workers=16)
+    assert rr["status"] == 0
+    assert rr["idx"][h, i, j] == j
+    P.check_attention(rr["out"], rr["lse"], x, rr["idx"], rr["cnt"], w.block,
+                      range(w.num_q_heads * w.nb), w.group)
+    s_jump = float(q_row @ generate.bf16_to_f32(k[h // w.group, j * w.block + u]))
+    assert (s_jump / np.sqrt(w.head_dim) / np.log(2) > 100) == exact
+
+
 def test_wait_timeout_is_reported_and_the_context_stays_usable(env):
     """The forward's watchdog: with every wait limited to 100 ns (far below
     the latency of the first copy from memory), waits run out on every CTA.
