@@ -58,8 +58,8 @@ struct Cfg {
   static constexpr int kKVPanel = BK * 128;       // bytes of one K/V panel
   static constexpr int kQBytes = kM * D * 2;
   static constexpr int kKVBytes = BK * D * 2;
-  static constexpr int kNQ = 1;                   // Q stages
-  static constexpr int kNK = 3;                   // K stages
+  static constexpr int kNQ = 2;                   // Q stages (the next item's loads early)
+  static constexpr int kNK = 2;                   // K stages
   static constexpr int kNV = 2;                   // V stages (a V load has ~2 block periods)
   static constexpr int kNS = 3;                   // S buffers in tensor memory
   static constexpr int kGroups = 4;               // softmax column groups
@@ -91,7 +91,7 @@ struct ItemInfo {
 constexpr int kRedoWords = 1024;
 
 struct Shared {
-  uint64_t q_full[1], q_empty[1];
+  uint64_t q_full[2], q_empty[2];
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[3], v_empty[3];
   uint64_t s_full[3];     // S of block b is in TMEM buffer b % 3
@@ -100,6 +100,7 @@ struct Shared {
   uint64_t o_last;        // one phase per item, after its last P.V (epilogue)
   uint64_t o_free;        // one phase per item: every group finished the epilogue
   uint64_t xch_bar;       // exchange between the softmax groups
+  uint64_t stage_bar;     // one phase per item: the output tile is staged
   uint64_t drain_qk, drain_pv;
   uint64_t info_full[kNI], info_empty[kNI];
   ItemInfo info[kNI];
@@ -204,7 +205,8 @@ template <int D, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tq,
                              const __grid_constant__ CUtensorMap tk,
-                             const __grid_constant__ CUtensorMap tv, const Params p) {
+                             const __grid_constant__ CUtensorMap tv,
+                             const __grid_constant__ CUtensorMap to, const Params p) {
   using C = Cfg<D, BK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // The data stages need 1024-byte alignment; the launch reserves no slack
@@ -223,8 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(&sh->q_full[0], 1);
-    mbar_init(&sh->q_empty[0], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh->q_full[s], 1);
+      // the item's last Q.K^T (commit) and its output tile leaving the stage
+      mbar_init(&sh->q_empty[s], 2);
+    }
     for (int s = 0; s < 3; ++s) {
       mbar_init(&sh->k_full[s], 1);
       mbar_init(&sh->k_empty[s], 1);
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh->o_last, 1);
     mbar_init(&sh->o_free, kSoftmaxThreads);
     mbar_init(&sh->xch_bar, kSoftmaxThreads);
+    mbar_init(&sh->stage_bar, kSoftmaxThreads);
     mbar_init(&sh->drain_qk, 1);
     mbar_init(&sh->drain_pv, 1);
     sh->abort = 0;
@@ -308,13 +314,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           sh->info[slot] = ItemInfo{h, i, n, jlast == i ? 1 : 0, pos - begin};
           mbar_arrive(&sh->info_full[slot]);
-          if (qi >= 1 && !mbar_wait(&sh->q_empty[0], (qi - 1) & 1, abort, p.wait_ns)) ok = false;
+          const int qs = qi % C::kNQ;
+          if (qi >= uint32_t(C::kNQ) &&
+              !mbar_wait(&sh->q_empty[qs], ((qi / C::kNQ) - 1) & 1, abort, p.wait_ns))
+            ok = false;
           if (ok) {
-            mbar_arrive_expect_tx(&sh->q_full[0], C::kQBytes);
+            mbar_arrive_expect_tx(&sh->q_full[qs], C::kQBytes);
 #pragma unroll
             for (int s = 0; s < C::kPanels; ++s)
-              tma_load_2d(sQ + s * C::kQPanel, &tq, &sh->q_full[0], s * 64, h * p.S + i * p.B,
-                          pol_q);
+              tma_load_2d(sQ + qs * C::kQBytes + s * C::kQPanel, &tq, &sh->q_full[qs], s * 64,
+                          h * p.S + i * p.B, pol_q);
+            // the next item's queries, into L2 while this item runs
+            if (pos + 1 < end && item_next >= 0 && item_next < p.num_items) {
+              const int32_t h2 = item_next / p.nb, i2 = item_next - h2 * p.nb;
+#pragma unroll
+              for (int s = 0; s < C::kPanels; ++s)
+                tma_prefetch_2d(&tq, s * 64, h2 * p.S + i2 * p.B);
+            }
           }
         }
       }
@@ -429,8 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier phases a step needs are tested together (one non-blocking test
     // per lane, one ballot) and only the missing ones are waited on.
     constexpr uint32_t idesc_qk = idesc_bf16(128, BK, 0, 0);  // Q, K both K-major
-    static_assert(C::kNK == 3 && C::kNS == 3, "shared ring indexing");
-    uint32_t qi = 0, kb = 0, stage = 0, phase = 0;
+    static_assert(C::kNS == 3, "S ring indexing");
+    uint32_t qi = 0, kb = 0, stage = 0, phase = 0;   // S ring
+    uint32_t kst = 0, kph = 0;                       // K ring
     bool ok = true;
     for (;;) {
       const int slot = qi % kNI;
@@ -442,22 +459,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->info_empty[slot]);
       if (n == 0) break;
-      if (!warp_wait(&sh->q_full[0], qi & 1, abort, p.wait_ns)) {
+      const int qs = qi % C::kNQ;
+      if (!warp_wait(&sh->q_full[qs], (qi / C::kNQ) & 1, abort, p.wait_ns)) {
         ok = false;
         break;
       }
-      const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t qdesc = smem_desc_sw128(smem_u32(sQ + qs * C::kQBytes), 16, 1024);
       for (int t = 0; t < n; ++t) {
         // lane 0: K of this block; lane 1: P.V of block kb-3 (same S buffer)
         const bool reuse = kb >= 3;
-        uint64_t* bar = &sh->k_full[stage];
-        uint32_t par = phase;
+        uint64_t* bar = &sh->k_full[kst];
+        uint32_t par = kph;
         if (lane == 1 && reuse) {
           bar = &sh->pv_done[stage];
           par = phase ^ 1u;
         }
         const uint32_t have = __ballot_sync(0xffffffffu, mbar_test(bar, par));
-        if (!(have & 1u) && !warp_wait(&sh->k_full[stage], phase, abort, p.wait_ns)) {
+        if (!(have & 1u) && !warp_wait(&sh->k_full[kst], kph, abort, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -466,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t kdesc = smem_desc_sw128(smem_u32(sK + stage * C::kKVBytes), 16, 1024);
+        const uint64_t kdesc = smem_desc_sw128(smem_u32(sK + kst * C::kKVBytes), 16, 1024);
         const uint32_t s_tmem = tmem + stage * BK;
         if (elect_one()) {
 #pragma unroll
@@ -479,14 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kk > 0 ? 1u : 0u);
           }
           mma_commit(&sh->s_full[stage]);
-          mma_commit(&sh->k_empty[stage]);
-          if (t == n - 1) mma_commit(&sh->q_empty[0]);
+          mma_commit(&sh->k_empty[kst]);
+          if (t == n - 1) mma_commit(&sh->q_empty[qs]);
         }
         __syncwarp();
         ++kb;
         if (++stage == 3) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (++kst == C::kNK) {
+          kst = 0;
+          kph ^= 1u;
         }
       }
       if (!ok) break;
@@ -622,6 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(lanes + o_col, r);
         tmem_ld_wait(r);
       }
+      // O is in registers: the next item's first P.V may overwrite it
+      tc_fence_before();
+      mbar_arrive(&sh->o_free);
       // the range the tensor-core pass keeps: every weight below 2^100 (so
       // neither P nor l can overflow) and O finite; beyond it the row's
       // columns are recomputed exactly
@@ -636,8 +661,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicOr(&sh->redo[pit.pos >> 5], 1u << (pit.pos & 31));
         else
           atomicOr(p.dev_status, SA_DEV_RANGE);
-      } else if (store) {
-        if (p.out_f32) {
+      }
+      if (store && in_range && p.lse && grp == 0)
+        p.lse[orow] = (pm + log2f(lt)) * 0.6931471805599453f;
+      if (p.out_f32) {
+        if (store && in_range) {
           uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(p.o) + orow * D + col);
 #pragma unroll
           for (int x = 0; x < C::kOCols / 4; ++x)
@@ -645,23 +673,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                                __float_as_uint(__uint_as_float(r[4 * x + 1]) * inv_l),
                                __float_as_uint(__uint_as_float(r[4 * x + 2]) * inv_l),
                                __float_as_uint(__uint_as_float(r[4 * x + 3]) * inv_l));
-        } else {
-          uint32_t ob[C::kOCols / 2];
-#pragma unroll
-          for (int x = 0; x < C::kOCols / 2; ++x)
-            ob[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
-                                __uint_as_float(r[2 * x + 1]) * inv_l);
-          uint4* d4 =
-              reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow * D + col);
-#pragma unroll
-          for (int x = 0; x < C::kOCols / 8; ++x)
-            d4[x] = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
         }
-        if (p.lse && grp == 0) p.lse[orow] = (pm + log2f(lt)) * 0.6931471805599453f;
+        // the item's Q stage needs no staging: release it at once
+        if (warp == 4 && lane == 0) mbar_arrive(&sh->q_empty[pq % C::kNQ]);
+        return true;
       }
-      tc_fence_before();
-      mbar_arrive(&sh->o_free);
-      return true;
+      // bf16: the tile is staged in the finished item's Q stage (its last
+      // Q.K^T is complete, and the producer reloads it only after the store
+      // below has read it), laid out as the 128-byte-swizzled boxes a TMA
+      // store reads, then written with one store per 64-column panel: rows
+      // reach memory whole instead of as 32 scattered pieces per warp store
+      uint8_t* stg = sQ + (pq % C::kNQ) * C::kQBytes;
+      if (store) {
+        uint32_t ob[C::kOCols / 2];
+#pragma unroll
+        for (int x = 0; x < C::kOCols / 2; ++x)
+          ob[x] = in_range ? pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
+                                         __uint_as_float(r[2 * x + 1]) * inv_l)
+                           : 0u;   // rewritten by the exact pass
+#pragma unroll
+        for (int x = 0; x < C::kOCols / 8; ++x) {
+          const int c16 = (col + 8 * x) / 8;           // 16-byte chunk of the row
+          const int panel = c16 / 8, chunk = c16 % 8;
+          uint4* dst = reinterpret_cast<uint4*>(stg + panel * C::kQPanel + row * 128 +
+                                                ((chunk ^ (row & 7)) << 4));
+          *dst = make_uint4(ob[4 * x], ob[4 * x + 1], ob[4 * x + 2], ob[4 * x + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sh->stage_bar);
+      bool sent = true;
+      if (warp == 4 && lane == 0) {
+        sent = mbar_wait(&sh->stage_bar, pq & 1, abort, p.wait_ns);
+        if (sent) {
+#pragma unroll
+          for (int s = 0; s < C::kPanels; ++s)
+            tma_store_2d(&to, stg + s * C::kQPanel, s * 64, pit.h * p.S + pit.i * p.B);
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(&sh->q_empty[pq % C::kNQ]);
+        }
+      }
+      return __all_sync(0xffffffffu, sent);   // the warp gives up together
     };
     for (;;) {
       const int slot = qi % kNI;
@@ -777,6 +830,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && pend) ok = epilogue();
     if (!ok) raise_abort(sh, p);
+    // the output tiles' stores complete before any exact rewrite and exit
+    if (warp == 4 && lane == 0) bulk_wait_all();
     // every epilogue of the list has set its bits: recompute the marked items,
     // one (row, column group) per thread
     asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
@@ -849,10 +904,13 @@ cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_fai
   // data stages + the small shared block; the kernel checks the alignment
   constexpr int kSmem = C::kData + int(sizeof(Shared));
   static_assert(kSmem <= 232448, "shared memory budget");
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
+  // the bf16 output is written by TMA in boxes of one query block; fp32 output
+  // is stored directly (the map is then unused)
   if (!make_map(&tq, a.q, uint64_t(a.Hq) * a.S, D, C::kM) ||
       !make_map(&tk, a.k, uint64_t(a.Hkv) * a.S, D, BK) ||
-      !make_map(&tv, a.v, uint64_t(a.Hkv) * a.S, D, BK)) {
+      !make_map(&tv, a.v, uint64_t(a.Hkv) * a.S, D, BK) ||
+      !make_map(&to, a.out_f32 ? a.q : a.o, uint64_t(a.Hq) * a.S, D, a.B)) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
@@ -881,7 +939,7 @@ cudaError_t launch(const sa_k::PrefillArgs& a, cudaStream_t st, bool* encode_fai
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   if (a.num_workers == 0) return cudaSuccess;
-  kern<<<a.num_workers, kThreads, kSmem, st>>>(tq, tk, tv, p);
+  kern<<<a.num_workers, kThreads, kSmem, st>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
