@@ -401,13 +401,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, per-head query scales; calibrated budgets)",
-        "config": {"workload": w.name, "seq_len": w.seq_len, "block": w.block,
-                   "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
-                   "head_dim": w.head_dim, "mean_density": round(
-                       layer.total_blocks / (w.num_q_heads * w.nb * (w.nb + 1) / 2), 5),
-                   "selected_blocks": layer.total_blocks, "schedule": args.schedule,
-                   "workers": sms, "l2": "inputs larger than L2 (no flush)",
-                   "parallelism": f"replicas{ws}"},
+        "config": workload_config(w, layer.total_blocks, ws),
+        "launch": {"schedule": args.schedule, "workers": sms},
         "ms_per_layer": round(ms_step, 4),
         "forward_ms": round(fwd_ms, 4),
         "stages": stages,
@@ -580,11 +575,55 @@ def bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush):
             "device_status": status}
 
 
+def _sample_in_subprocess(steps: int, cores: int):
+    """reference_sample in a child process restricted to `cores` host cores
+    (CPU affinity and BLAS thread counts), so that numpy's thread pools start
+    with that width."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    code = ("import json, os, sys; sys.path.insert(0, %r); "
+            "os.sched_setaffinity(0, sorted(os.sched_getaffinity(0))[:%d]) "
+            "if hasattr(os, 'sched_setaffinity') else None; "
+            "import bench; print(json.dumps(bench.reference_sample(%d)))" % (ROOT, cores, steps))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-400:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _layer_flops():
+    """Algorithmic work of one headline layer (attention over every selected
+    block plus block scoring), from the oracle's plan."""
+    from oracle import plan as op
+    from workloads import workload
+
+    w = workload(WORKLOAD)
+    prof = _profile(WORKLOAD)
+    budgets = op.maxmin_shift(prof["k_uniform"], prof["demand"], prof["k_min"], w.nb)
+    blocks = sum(op.kept_blocks(k, w.nb) for k in budgets)
+    return _attention_flops(blocks, w.block, w.head_dim) + _score_flops(w), blocks
+
+
 def cpu_baseline(args, sample_seconds: float):
-    """The oracle, as it stands, on the host cores over a bounded sample."""
-    s = reference_sample(max(1, int(sample_seconds // 4)))
-    return {"value": s["value"], "unit": UNIT, "cores": s["cores"], "kind": "oracle",
-            "sample": s["sample"]}
+    """The oracle, as it stands, on the host cores over a bounded sample: on
+    all cores and on one, each extrapolated to the full layer."""
+    all_cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    steps = max(1, int(sample_seconds // 4))
+    full = _sample_in_subprocess(steps, all_cores)
+    one = _sample_in_subprocess(max(1, steps // 2), 1)
+    layer_flops, _ = _layer_flops()
+    return {"value": full["value"], "unit": UNIT, "cores": full["cores"], "kind": "oracle",
+            "sample": full["sample"],
+            "one_core": {"value": one["value"], "unit": UNIT, "cores": one["cores"],
+                         "sample": one["sample"]},
+            "extrapolation": {
+                "layer_tflop": round(layer_flops / 1e12, 4),
+                "all_cores_s_per_layer": round(layer_flops / (full["value"] * 1e12), 1),
+                "one_core_s_per_layer": round(layer_flops / (one["value"] * 1e12), 1),
+                "how": "the layer's algorithmic work (selected-block attention plus block "
+                       "scoring) over the sample's throughput; attention dominates both"}}
 
 
 def reference_sample(steps: int):
@@ -626,29 +665,40 @@ def reference_sample(steps: int):
                       f"{w.name}; fp64 numpy (BLAS threads)"}
 
 
+def workload_config(w, total_blocks: int, ws: int) -> dict:
+    """The workload as both arms name it in their JSON line."""
+    return {"workload": w.name, "seq_len": w.seq_len, "block": w.block,
+            "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "mean_density": round(total_blocks / (w.num_q_heads * w.nb * (w.nb + 1) / 2), 5),
+            "selected_blocks": total_blocks,
+            "budgets": "calibrated per head, Max-Min shifted (workloads/demands.json)",
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas{ws}"}
+
+
 def run_reference(args):
     ws, rank, local = _dist()
     if rank != 0:
         return
     from workloads import workload
     w = workload(WORKLOAD)
-    per = []
     for _ in range(args.warmup):
         reference_sample(1)
     t0 = time.perf_counter()
     res = [reference_sample(1) for _ in range(args.steps)]
     total = time.perf_counter() - t0
     value = statistics.mean(r["value"] for r in res)
+    layer_flops, blocks = _layer_flops()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) bf16)", "impl": "reference",
-        "config": {"workload": w.name, "seq_len": w.seq_len, "block": w.block,
-                   "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
-                   "head_dim": w.head_dim, "parallelism": "host cores"},
+        "data": "synthetic (seeded N(0,1) bf16, per-head query scales; calibrated budgets)",
+        "impl": "reference",
+        "config": workload_config(w, blocks, ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
-                         "cores": res[0]["cores"], "sample": res[0]["sample"]},
+                         "cores": res[0]["cores"], "sample": res[0]["sample"],
+                         "extrapolation": {"layer_tflop": round(layer_flops / 1e12, 4),
+                                           "s_per_layer": round(layer_flops / (value * 1e12), 1)}},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

@@ -81,7 +81,13 @@ def test_reference_arm_prints_the_contract_line():
     assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
     assert line["higher_is_better"] is True and line["value"] > 0
     assert line["config"]["workload"] == "llama31_8b_prefill_128k"
+    # the same config the GPU arm prints: the workload and its plan's blocks
+    from workloads import workload
+    layer_flops, blocks = bench._layer_flops()
+    assert line["config"] == bench.workload_config(workload(bench.WORKLOAD), blocks, 1)
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["extrapolation"]["s_per_layer"] == pytest.approx(
+        layer_flops / (line["value"] * 1e12), rel=1e-2)
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
@@ -95,3 +101,16 @@ def test_reference_arm_other_ranks_exit_quietly():
                        text=True, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_cpu_baseline_reports_one_core_and_all_cores():
+    # the oracle timed twice on the host, on every core and on one, each
+    # figure extrapolated to the whole layer
+    import bench
+    b = bench.cpu_baseline(None, sample_seconds=4.0)
+    assert b["kind"] == "oracle" and b["value"] > 0 and b["one_core"]["value"] > 0
+    assert b["one_core"]["cores"] == 1 and b["cores"] >= 1
+    ext = b["extrapolation"]
+    assert ext["one_core_s_per_layer"] == pytest.approx(
+        ext["layer_tflop"] / b["one_core"]["value"], rel=1e-2)
+    assert ext["all_cores_s_per_layer"] == pytest.approx(ext["layer_tflop"] / b["value"], rel=1e-2)
