@@ -21,7 +21,7 @@ __all__ = [
     "sparse_attn_score_workspace_size", "sparse_attn_select", "sparse_attn_forward",
     "sparse_attn_pool_kcache", "sa_status_string", "library_path",
     "sparse_attn_select_topp", "sparse_attn_pool_kcache_plan", "sparse_attn_score_plan",
-    "sparse_attn_set_wait_limit",
+    "sparse_attn_set_wait_limit", "sparse_attn_select_kind", "sparse_attn_forward_kind",
 ]
 
 SA_OK = 0
@@ -107,6 +107,10 @@ def _load():
         "sparse_attn_pool_kcache_plan": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P]),
         "sparse_attn_score_plan": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P]),
         "sparse_attn_set_wait_limit": (ctypes.c_int, [ctypes.c_uint64]),
+        "sparse_attn_select_kind": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, I32, I32,
+                                                   P]),
+        "sparse_attn_forward_kind": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P, P,
+                                                    I32, P, I32, P, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -276,6 +280,14 @@ def sparse_attn_select(shape: Shape, plan: Plan, scores, idx, cnt, kmax: int, st
                                    _ptr(cnt), kmax, _stream(stream)), "sparse_attn_select")
 
 
+def sparse_attn_select_kind(shape: Shape, plan: Plan, scores, idx, cnt, kmax: int, head_kind: int,
+                            stream=None):
+    """Decode: the selection of the heads of one kind only."""
+    _check(_lib.sparse_attn_select_kind(ctypes.byref(shape), plan.handle, _ptr(scores), _ptr(idx),
+                                        _ptr(cnt), kmax, int(head_kind), _stream(stream)),
+           "sparse_attn_select_kind")
+
+
 def sparse_attn_select_topp(shape: Shape, plan: Plan, scores, p: float, idx, cnt, kmax: int,
                             stream=None):
     _check(_lib.sparse_attn_select_topp(ctypes.byref(shape), plan.handle, _ptr(scores),
@@ -301,6 +313,16 @@ def sparse_attn_forward(shape: Shape, plan, q, k, v, idx, cnt, kmax: int, o, lse
                                     _out_dtype(o, o_dtype), _ptr(lse), _ptr(dev_status),
                                     _stream(stream)),
            "sparse_attn_forward")
+
+
+def sparse_attn_forward_kind(shape: Shape, plan: Plan, q, k, v, idx, cnt, kmax: int, o, lse,
+                             dev_status, head_kind: int, stream=None, o_dtype=None):
+    """Decode: the attention of the heads of one kind only."""
+    _check(_lib.sparse_attn_forward_kind(ctypes.byref(shape), plan.handle, _ptr(q), _ptr(k),
+                                         _ptr(v), _ptr(idx), _ptr(cnt), kmax, _ptr(o),
+                                         _out_dtype(o, o_dtype), _ptr(lse), _ptr(dev_status),
+                                         int(head_kind), _stream(stream)),
+           "sparse_attn_forward_kind")
 
 
 def sparse_attn_pool_kcache(shape: Shape, k, kbar, stream=None):

@@ -9,6 +9,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <vector>
 
 #include "kernels.h"
 #include "plan_impl.h"
@@ -35,9 +36,11 @@ void free_device(sa_plan* p) {
     cudaFree(p->d_wptr);
     cudaFree(p->d_items);
     cudaFree(p->d_scratch);
+    cudaFree(p->d_kind_heads);
     if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
   }
   p->d_scratch = nullptr;
+  p->d_kind_heads = nullptr;
   p->d_budgets = nullptr;
   p->d_kinds = nullptr;
   p->d_gran = nullptr;
@@ -71,6 +74,116 @@ bool has_granularity(const sa_plan* p) {
 
 }  // namespace
 
+namespace {
+
+// Selection over every row, or (decode) over the rows of the heads in
+// `heads` (nh of them); scores may then be NULL when all of them stream.
+sa_status select_rows(const sa_shape* shp, const sa_plan* plan, const float* scores,
+                      int32_t* idx, int32_t* cnt, int32_t kmax, const int32_t* heads,
+                      int32_t nh, bool need_scores, sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!plan || (need_scores && !scores) || !idx || !cnt) return SA_ERR_INVALID_ARG;
+  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+  if (kmax < plan->kmax) return SA_ERR_SHAPE;
+  const bool decode = shp->mode == SA_MODE_DECODE;
+  const int32_t max_row = decode ? decode_max_row(plan) : plan->nb;
+  if (max_row > (decode ? 4096 : 2048)) return SA_ERR_UNSUPPORTED;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  sa_k::SelectArgs a;
+  a.scores = scores;
+  a.budgets = plan->d_budgets;
+  a.kinds = plan->d_kinds;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.kmax = kmax;
+  a.nb = plan->nb;
+  a.Hq = shp->num_q_heads;
+  a.decode = shp->mode == SA_MODE_DECODE;
+  a.group = plan->group;
+  a.group_shared = plan->group_shared;
+  a.rows = a.decode ? shp->batch * shp->num_q_heads
+                    : (plan->group_shared ? shp->num_kv_heads : shp->num_q_heads) * plan->nb;
+  a.window_blocks = plan->window_blocks;
+  a.gran = decode ? plan->d_gran : nullptr;
+  a.L = int32_t(shp->seq_len);
+  a.stride = decode ? plan->score_stride : 0;
+  a.max_row = max_row;
+  a.heads = heads;
+  a.nh = nh;
+  if (heads) a.rows = shp->batch * nh;
+  return cuda_status(sa_k::launch_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Attention over every row, or (decode) over the rows of the heads in `heads`.
+sa_status forward_rows(const sa_shape* shp, const sa_plan* plan, const void* q, const void* k,
+                       const void* v, const int32_t* idx, const int32_t* cnt, int32_t kmax,
+                       void* o, int32_t o_dtype, float* lse, int32_t* dev_status,
+                       const int32_t* heads, int32_t nh, sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!q || !k || !v || !idx || !cnt || !o || !dev_status || kmax < 1) return SA_ERR_INVALID_ARG;
+  if (o_dtype != SA_DTYPE_BF16 && o_dtype != SA_DTYPE_F32) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (shp->mode == SA_MODE_DECODE) {
+    if (plan && !same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+    const bool sized = plan && has_granularity(plan);
+    if (sized && plan->device < 0) return SA_ERR_NOT_UPLOADED;
+    sa_k::DecodeArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.idx = idx;
+    a.cnt = cnt;
+    a.kmax = kmax;
+    a.Bt = shp->batch;
+    a.Hq = shp->num_q_heads;
+    a.Hkv = shp->num_kv_heads;
+    a.L = int(shp->seq_len);
+    a.B = shp->block;
+    a.d = shp->head_dim;
+    a.o = o;
+    a.out_f32 = o_dtype == SA_DTYPE_F32;
+    a.lse = lse;
+    a.dev_status = dev_status;
+    a.gran = sized ? plan->d_gran : nullptr;
+    a.heads = heads;
+    a.nh = nh;
+    return cuda_status(sa_k::launch_decode_attention(a, st));
+  }
+  if (!plan) return SA_ERR_INVALID_ARG;
+  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  sa_k::PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.kmax = kmax;
+  a.wptr = plan->d_wptr;
+  a.items = plan->d_items;
+  a.num_workers = plan->num_workers;
+  a.num_items = shp->num_q_heads * plan->nb;
+  a.S = int(shp->seq_len);
+  a.B = shp->block;
+  a.d = shp->head_dim;
+  a.Hq = shp->num_q_heads;
+  a.Hkv = shp->num_kv_heads;
+  a.o = o;
+  a.out_f32 = o_dtype == SA_DTYPE_F32;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  bool encode_failed = false;
+  cudaError_t e = sa_k::launch_prefill_attention(a, st, &encode_failed);
+  if (encode_failed) return SA_ERR_CUDA;
+  return cuda_status(e);
+}
+
+}  // namespace
+
 extern "C" {
 
 sa_status sparse_attn_plan_upload(sa_plan* plan, sa_stream_t stream) {
@@ -83,11 +196,22 @@ sa_status sparse_attn_plan_upload(sa_plan* plan, sa_stream_t stream) {
   const size_t nw = plan->wptr.size();
   const size_t ni = plan->items.size();
   const size_t ng = plan->gran.size();
+  // decode: head indices by kind, streaming heads first
+  std::vector<int32_t> kind_heads;
+  if (plan->shape.mode == SA_MODE_DECODE) {
+    for (size_t h = 0; h < plan->kinds.size(); ++h)
+      if (plan->kinds[h] == SA_HEAD_STREAMING) kind_heads.push_back(int32_t(h));
+    plan->n_streaming = int32_t(kind_heads.size());
+    for (size_t h = 0; h < plan->kinds.size(); ++h)
+      if (plan->kinds[h] != SA_HEAD_STREAMING) kind_heads.push_back(int32_t(h));
+  }
   cudaError_t e = cudaMalloc(&plan->d_budgets, nh * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_kinds, nh);
   if (e == cudaSuccess && ng) e = cudaMalloc(&plan->d_gran, ng * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMalloc(&plan->d_wptr, nw * sizeof(int32_t));
   if (e == cudaSuccess && ni) e = cudaMalloc(&plan->d_items, ni * sizeof(int32_t));
+  if (e == cudaSuccess && !kind_heads.empty())
+    e = cudaMalloc(&plan->d_kind_heads, kind_heads.size() * sizeof(int32_t));
   plan->device = dev;
   if (e != cudaSuccess) {
     free_device(plan);
@@ -106,6 +230,9 @@ sa_status sparse_attn_plan_upload(sa_plan* plan, sa_stream_t stream) {
   if (e == cudaSuccess && ni)
     e = cudaMemcpyAsync(plan->d_items, plan->items.data(), ni * sizeof(int32_t),
                         cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && !kind_heads.empty())
+    e = cudaMemcpyAsync(plan->d_kind_heads, kind_heads.data(),
+                        kind_heads.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {
     free_device(plan);
@@ -160,35 +287,21 @@ sa_status sparse_attn_score(const sa_shape* shp, const void* q, const void* k, f
 
 sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan, const float* scores,
                              int32_t* idx, int32_t* cnt, int32_t kmax, sa_stream_t stream) {
-  sa_status s = sa_host::check_supported(shp);
-  if (s != SA_OK) return s;
-  if (!plan || !scores || !idx || !cnt) return SA_ERR_INVALID_ARG;
-  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
-  if (kmax < plan->kmax) return SA_ERR_SHAPE;
-  const bool decode = shp->mode == SA_MODE_DECODE;
-  const int32_t max_row = decode ? decode_max_row(plan) : plan->nb;
-  if (max_row > (decode ? 4096 : 2048)) return SA_ERR_UNSUPPORTED;
+  return select_rows(shp, plan, scores, idx, cnt, kmax, nullptr, 0, true, stream);
+}
+
+sa_status sparse_attn_select_kind(const sa_shape* shp, const sa_plan* plan, const float* scores,
+                                  int32_t* idx, int32_t* cnt, int32_t kmax, int32_t head_kind,
+                                  sa_stream_t stream) {
+  if (!shp || !plan || shp->mode != SA_MODE_DECODE) return SA_ERR_INVALID_ARG;
+  if (head_kind != SA_HEAD_STREAMING && head_kind != SA_HEAD_RETRIEVAL) return SA_ERR_INVALID_ARG;
   if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
-  sa_k::SelectArgs a;
-  a.scores = scores;
-  a.budgets = plan->d_budgets;
-  a.kinds = plan->d_kinds;
-  a.idx = idx;
-  a.cnt = cnt;
-  a.kmax = kmax;
-  a.nb = plan->nb;
-  a.Hq = shp->num_q_heads;
-  a.decode = shp->mode == SA_MODE_DECODE;
-  a.group = plan->group;
-  a.group_shared = plan->group_shared;
-  a.rows = a.decode ? shp->batch * shp->num_q_heads
-                    : (plan->group_shared ? shp->num_kv_heads : shp->num_q_heads) * plan->nb;
-  a.window_blocks = plan->window_blocks;
-  a.gran = decode ? plan->d_gran : nullptr;
-  a.L = int32_t(shp->seq_len);
-  a.stride = decode ? plan->score_stride : 0;
-  a.max_row = max_row;
-  return cuda_status(sa_k::launch_select(a, reinterpret_cast<cudaStream_t>(stream)));
+  const bool streaming = head_kind == SA_HEAD_STREAMING;
+  const int32_t nh = streaming ? plan->n_streaming
+                               : int32_t(plan->kinds.size()) - plan->n_streaming;
+  if (nh == 0) return SA_OK;
+  const int32_t* heads = plan->d_kind_heads + (streaming ? 0 : plan->n_streaming);
+  return select_rows(shp, plan, scores, idx, cnt, kmax, heads, nh, !streaming, stream);
 }
 
 sa_status sparse_attn_select_topp(const sa_shape* shp, const sa_plan* plan, const float* scores,
@@ -250,66 +363,26 @@ sa_status sparse_attn_plan_device_schedule(const sa_plan* plan, int32_t* wptr, i
 sa_status sparse_attn_forward(const sa_shape* shp, const sa_plan* plan, const void* q,
                               const void* k, const void* v, const int32_t* idx,
                               const int32_t* cnt, int32_t kmax, void* o, int32_t o_dtype,
-                              float* lse,
-                              int32_t* dev_status, sa_stream_t stream) {
-  sa_status s = sa_host::check_supported(shp);
-  if (s != SA_OK) return s;
-  if (!q || !k || !v || !idx || !cnt || !o || !dev_status || kmax < 1) return SA_ERR_INVALID_ARG;
-  if (o_dtype != SA_DTYPE_BF16 && o_dtype != SA_DTYPE_F32) return SA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SA_ERR_INVALID_ARG;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (shp->mode == SA_MODE_DECODE) {
-    if (plan && !same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
-    const bool sized = plan && has_granularity(plan);
-    if (sized && plan->device < 0) return SA_ERR_NOT_UPLOADED;
-    sa_k::DecodeArgs a;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.idx = idx;
-    a.cnt = cnt;
-    a.kmax = kmax;
-    a.Bt = shp->batch;
-    a.Hq = shp->num_q_heads;
-    a.Hkv = shp->num_kv_heads;
-    a.L = int(shp->seq_len);
-    a.B = shp->block;
-    a.d = shp->head_dim;
-    a.o = o;
-    a.out_f32 = o_dtype == SA_DTYPE_F32;
-    a.lse = lse;
-    a.dev_status = dev_status;
-    a.gran = sized ? plan->d_gran : nullptr;
-    return cuda_status(sa_k::launch_decode_attention(a, st));
-  }
-  if (!plan) return SA_ERR_INVALID_ARG;
-  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+                              float* lse, int32_t* dev_status, sa_stream_t stream) {
+  return forward_rows(shp, plan, q, k, v, idx, cnt, kmax, o, o_dtype, lse, dev_status, nullptr, 0,
+                      stream);
+}
+
+sa_status sparse_attn_forward_kind(const sa_shape* shp, const sa_plan* plan, const void* q,
+                                   const void* k, const void* v, const int32_t* idx,
+                                   const int32_t* cnt, int32_t kmax, void* o, int32_t o_dtype,
+                                   float* lse, int32_t* dev_status, int32_t head_kind,
+                                   sa_stream_t stream) {
+  if (!shp || !plan || shp->mode != SA_MODE_DECODE) return SA_ERR_INVALID_ARG;
+  if (head_kind != SA_HEAD_STREAMING && head_kind != SA_HEAD_RETRIEVAL) return SA_ERR_INVALID_ARG;
   if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
-  sa_k::PrefillArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.idx = idx;
-  a.cnt = cnt;
-  a.kmax = kmax;
-  a.wptr = plan->d_wptr;
-  a.items = plan->d_items;
-  a.num_workers = plan->num_workers;
-  a.num_items = shp->num_q_heads * plan->nb;
-  a.S = int(shp->seq_len);
-  a.B = shp->block;
-  a.d = shp->head_dim;
-  a.Hq = shp->num_q_heads;
-  a.Hkv = shp->num_kv_heads;
-  a.o = o;
-  a.out_f32 = o_dtype == SA_DTYPE_F32;
-  a.lse = lse;
-  a.dev_status = dev_status;
-  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
-  bool encode_failed = false;
-  cudaError_t e = sa_k::launch_prefill_attention(a, st, &encode_failed);
-  if (encode_failed) return SA_ERR_CUDA;
-  return cuda_status(e);
+  const bool streaming = head_kind == SA_HEAD_STREAMING;
+  const int32_t nh = streaming ? plan->n_streaming
+                               : int32_t(plan->kinds.size()) - plan->n_streaming;
+  if (nh == 0) return SA_OK;
+  const int32_t* heads = plan->d_kind_heads + (streaming ? 0 : plan->n_streaming);
+  return forward_rows(shp, plan, q, k, v, idx, cnt, kmax, o, o_dtype, lse, dev_status, heads, nh,
+                      stream);
 }
 
 sa_status sparse_attn_set_wait_limit(uint64_t ns) {

@@ -36,7 +36,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_attention_kernel(sa_k::
   __shared__ float sq[kD];
   __shared__ float sm[kWarps], sl[kWarps];
   __shared__ float so[kWarps][kD];
-  const int row = blockIdx.x;
+  // rows may be restricted to a list of heads (one kind of head)
+  const int row = a.heads ? (int(blockIdx.x) / a.nh) * a.Hq + a.heads[blockIdx.x % a.nh]
+                          : int(blockIdx.x);
   const int b = row / a.Hq, h = row % a.Hq;
   const int g = h / (a.Hq / a.Hkv);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -173,7 +175,8 @@ namespace sa_k {
 
 cudaError_t launch_decode_attention(const DecodeArgs& a, cudaStream_t st) {
   if (a.d != kD || a.B != kB) return cudaErrorInvalidValue;
-  const int rows = a.Bt * a.Hq;
+  if (a.heads && a.nh <= 0) return cudaErrorInvalidValue;
+  const int rows = a.Bt * (a.heads ? a.nh : a.Hq);
   if (rows == 0) return cudaSuccess;
   const float scale_log2 = float(1.4426950408889634 / 11.313708498984761);  // log2(e)/sqrt(128)
   decode_attention_kernel<<<rows, kWarps * 32, 0, st>>>(a, scale_log2);

@@ -59,6 +59,8 @@ struct SelectArgs {
   int32_t L;                // decode: cache length (rows of L / gran[h] blocks)
   int32_t stride;           // decode: score row stride (0: nb)
   int32_t max_row;          // largest row in blocks (picks the kernel width)
+  const int32_t* heads;     // decode: NULL (every head), or the nh heads to run: the
+  int32_t nh;               //   grid is Bt * nh rows, row = b * Hq + heads[x % nh]
 };
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st);
 
@@ -117,6 +119,8 @@ struct DecodeArgs {
   float* lse;
   int32_t* dev_status;
   const int32_t* gran;      // [Hq] device block size per head (multiple of 16), or NULL: B
+  const int32_t* heads;     // NULL (every head), or the nh heads to run, as for select
+  int32_t nh;
 };
 cudaError_t launch_decode_attention(const DecodeArgs& a, cudaStream_t st);
 

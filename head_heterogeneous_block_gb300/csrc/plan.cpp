@@ -266,15 +266,23 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* p, sa_plan
       if (p->head_kind || p->granularity || p->head_budget) { delete plan; return SA_ERR_INVALID_ARG; }
       if (p->num_workers < 1) { delete plan; return SA_ERR_INVALID_ARG; }
       if (p->group_shared != 0 && p->group_shared != 1) { delete plan; return SA_ERR_INVALID_ARG; }
-      plan->budgets = sa_host::maxmin_shift(p->k_uniform, p->demand, H, p->k_min, nb);
       plan->group_shared = p->group_shared;
-      if (p->group_shared) {
-        // a shared list gets the largest of its heads' budgets
-        for (int32_t g = 0; g < shp->num_kv_heads; ++g) {
-          int32_t k = 0;
-          for (int32_t x = 0; x < plan->group; ++x) k = std::max(k, plan->budgets[g * plan->group + x]);
-          for (int32_t x = 0; x < plan->group; ++x) plan->budgets[g * plan->group + x] = k;
+      if (!p->group_shared) {
+        plan->budgets = sa_host::maxmin_shift(p->k_uniform, p->demand, H, p->k_min, nb);
+      } else {
+        // one list per KV group: the budget is shifted between groups, each
+        // demanding what its most demanding head demands (the totals stay
+        // Hkv * k_uniform per group and Hq * k_uniform per head)
+        const int32_t Hkv = shp->num_kv_heads, G = plan->group;
+        std::vector<int32_t> g_demand;
+        if (p->demand) {
+          g_demand.assign(Hkv, 0);
+          for (int32_t h = 0; h < H; ++h) g_demand[h / G] = std::max(g_demand[h / G], p->demand[h]);
         }
+        const std::vector<int32_t> k_g = sa_host::maxmin_shift(
+            p->k_uniform, p->demand ? g_demand.data() : nullptr, Hkv, p->k_min, nb);
+        plan->budgets.resize(H);
+        for (int32_t h = 0; h < H; ++h) plan->budgets[h] = k_g[h / G];
       }
       plan->num_workers = p->num_workers;
       sa_host::build_schedule(plan->budgets, nb, plan->group, p->num_workers, p->schedule,

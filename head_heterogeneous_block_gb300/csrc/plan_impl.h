@@ -36,6 +36,10 @@ struct sa_plan {
   int32_t* d_wptr = nullptr;
   int32_t* d_items = nullptr;
   int32_t* d_scratch = nullptr;   // sparse_attn_plan_rebuild: 3N int32
+  // decode: head indices by kind, streaming heads first ([Hq]), and how many
+  // are streaming (sparse_attn_select_kind / sparse_attn_forward_kind)
+  int32_t* d_kind_heads = nullptr;
+  int32_t n_streaming = 0;
 };
 
 namespace sa_host {

@@ -324,13 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < C::kPanels; ++s)
               tma_load_2d(sQ + qs * C::kQBytes + s * C::kQPanel, &tq, &sh->q_full[qs], s * 64,
                           h * p.S + i * p.B, pol_q);
-            // the next item's queries, into L2 while this item runs
-            if (pos + 1 < end && item_next >= 0 && item_next < p.num_items) {
-              const int32_t h2 = item_next / p.nb, i2 = item_next - h2 * p.nb;
-#pragma unroll
-              for (int s = 0; s < C::kPanels; ++s)
-                tma_prefetch_2d(&tq, s * 64, h2 * p.S + i2 * p.B);
-            }
+
           }
         }
       }

@@ -43,7 +43,9 @@ __global__ void __launch_bounds__(kT) select_kernel(sa_k::SelectArgs a) {
   __shared__ uint32_t ctl[4];
   __shared__ uint32_t wsum[kT / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x;
+  // decode rows may be restricted to a list of heads (one kind of head)
+  const int row = a.heads ? (int(blockIdx.x) / a.nh) * a.Hq + a.heads[blockIdx.x % a.nh]
+                          : int(blockIdx.x);
 
   int h, i, G = 1;
   const float* srow;
@@ -480,6 +482,7 @@ cudaError_t launch_select_topp(const TopPArgs& a, cudaStream_t st) {
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
+  if (a.heads && (!a.decode || a.nh <= 0)) return cudaErrorInvalidValue;
   // decode launches few rows (sequences x heads): wider CTAs per row
   const int row = std::max(a.nb, a.max_row);
   if (!a.decode && row <= 16 * kThreads)

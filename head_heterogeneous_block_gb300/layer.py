@@ -11,9 +11,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (Shape, sparse_attn_forward, sparse_attn_plan, sparse_attn_pool_kcache,
+from . import (SA_HEAD_RETRIEVAL, SA_HEAD_STREAMING, Shape, sparse_attn_forward,
+               sparse_attn_forward_kind, sparse_attn_plan, sparse_attn_pool_kcache,
                sparse_attn_pool_kcache_plan, sparse_attn_score, sparse_attn_score_plan,
-               sparse_attn_score_workspace_size, sparse_attn_select)
+               sparse_attn_score_workspace_size, sparse_attn_select, sparse_attn_select_kind)
 
 
 class PrefillLayer:
@@ -63,13 +64,21 @@ class PrefillLayer:
 class DecodeStep:
     """One decode step: pooled key cache (built once), scores, selection and
     attention.  With ``granularity`` (and ``head_budget``) each retrieval head
-    selects ``head_budget[h]`` blocks of ``granularity[h]`` tokens."""
+    selects ``head_budget[h]`` blocks of ``granularity[h]`` tokens.
+
+    With ``overlap`` the streaming heads, whose block lists do not depend on
+    the scores, are selected and attended on a side stream while the
+    retrieval heads score, select and attend on the caller's stream; the
+    step ends when both are done.  The kernels and results are the same."""
 
     def __init__(self, shape: Shape, budget_blocks: int, head_kind, window_blocks: int,
                  device="cuda", with_lse: bool = False, out_dtype=torch.bfloat16,
-                 granularity=None, head_budget=None):
+                 granularity=None, head_budget=None, overlap: bool = False):
         dev = torch.device(device)
         self.shape = shape
+        self.overlap = overlap
+        if overlap:
+            self.side = torch.cuda.Stream(device=dev)
         self.plan = sparse_attn_plan(shape, budget_blocks, head_kind=head_kind,
                                      window_blocks=window_blocks, num_workers=1,
                                      granularity=granularity, head_budget=head_budget)
@@ -97,14 +106,37 @@ class DecodeStep:
 
     def __call__(self, q, k, v, out=None, stream=None):
         out = self.out if out is None else out
-        if self.sized:
-            sparse_attn_score_plan(self.shape, self.plan, q, self.kbar, self.scores, stream=stream)
-        else:
-            sparse_attn_score(self.shape, q, self.kbar, self.scores, None, 0, stream=stream)
+        if self.overlap:
+            return self._overlapped(q, k, v, out, stream)
+        self._score(q, stream)
         sparse_attn_select(self.shape, self.plan, self.scores, self.idx, self.cnt, self.kmax,
                            stream=stream)
         sparse_attn_forward(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax, out,
                             self.lse, self.dev_status, stream=stream)
+        return out
+
+    def _score(self, q, stream):
+        if self.sized:
+            sparse_attn_score_plan(self.shape, self.plan, q, self.kbar, self.scores, stream=stream)
+        else:
+            sparse_attn_score(self.shape, q, self.kbar, self.scores, None, 0, stream=stream)
+
+    def _overlapped(self, q, k, v, out, stream):
+        main = torch.cuda.current_stream() if stream is None else stream
+        self.side.wait_stream(main)
+        # streaming heads: fixed lists, attended beside the scoring
+        sparse_attn_select_kind(self.shape, self.plan, None, self.idx, self.cnt, self.kmax,
+                                SA_HEAD_STREAMING, stream=self.side)
+        sparse_attn_forward_kind(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax,
+                                 out, self.lse, self.dev_status, SA_HEAD_STREAMING,
+                                 stream=self.side)
+        # retrieval heads: scores, top-k, attention
+        self._score(q, main)
+        sparse_attn_select_kind(self.shape, self.plan, self.scores, self.idx, self.cnt,
+                                self.kmax, SA_HEAD_RETRIEVAL, stream=main)
+        sparse_attn_forward_kind(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax,
+                                 out, self.lse, self.dev_status, SA_HEAD_RETRIEVAL, stream=main)
+        main.wait_stream(self.side)
         return out
 
 

@@ -295,6 +295,23 @@ sa_status sparse_attn_select(const sa_shape* shp, const sa_plan* plan,
                              int32_t kmax, sa_stream_t stream);
 
 /*
+ * Decode plans only: sparse_attn_select restricted to the rows of the heads
+ * of one kind, head_kind = SA_HEAD_STREAMING or SA_HEAD_RETRIEVAL (rows b*Hq+h
+ * of the other heads are left as they are).  Streaming heads keep block 0 and
+ * the last window blocks whatever the scores say, so their lists can be made
+ * (and attended, sparse_attn_forward_kind) on one stream while the retrieval
+ * heads score and select on another: Fluxion's split into streaming and
+ * retrieval heads ("Riepilogo Tecnico: Fluxion", "Intuizioni Chiave" 1) lets
+ * the two kinds proceed independently.  scores may be NULL for
+ * SA_HEAD_STREAMING.  A kind with no head returns SA_OK and launches nothing.
+ * Errors: as sparse_attn_select, plus INVALID_ARG for a prefill plan or an
+ * unknown kind.
+ */
+sa_status sparse_attn_select_kind(const sa_shape* shp, const sa_plan* plan,
+                                  const float* scores, int32_t* idx, int32_t* cnt,
+                                  int32_t kmax, int32_t head_kind, sa_stream_t stream);
+
+/*
  * Top-p selection, the data-dependent alternative the S-HPLB pages compare
  * against (Italian summary, "Sparsita' Eterogenea": an adaptive top-p budget
  * fixes accuracy but makes every head's work different).  Prefill only.
@@ -337,6 +354,21 @@ sa_status sparse_attn_plan_rebuild(sa_plan* plan, const int32_t* cnt, sa_stream_
  */
 sa_status sparse_attn_plan_device_schedule(const sa_plan* plan, int32_t* wptr,
                                            int32_t* items, sa_stream_t stream);
+
+/*
+ * Decode plans only: sparse_attn_forward restricted to the rows (b, h) of the
+ * heads of one kind (see sparse_attn_select_kind); the other rows of o and lse
+ * are not written.  The plan is required and must be uploaded.  A kind with no
+ * head returns SA_OK and launches nothing.
+ * Errors: as sparse_attn_forward, plus INVALID_ARG for a prefill plan or an
+ * unknown kind.
+ */
+sa_status sparse_attn_forward_kind(const sa_shape* shp, const sa_plan* plan,
+                                   const void* q, const void* k, const void* v,
+                                   const int32_t* idx, const int32_t* cnt, int32_t kmax,
+                                   void* o, int32_t o_dtype, float* lse,
+                                   int32_t* dev_status, int32_t head_kind,
+                                   sa_stream_t stream);
 
 /*
  * Watchdog limit of the prefill forward kernel: every wait of one role on

@@ -81,20 +81,23 @@ def maxmin_shift(k_uniform: int, demand: list[int], k_min: int, nb: int) -> list
     return k
 
 
-def group_budgets(budgets: list[int], group: int) -> list[int]:
+def group_budgets(k_uniform: int, demand: list[int], group: int, k_min: int,
+                  nb: int) -> list[int]:
     """Budgets when the G query heads of a KV group share one block list.
 
     Fluxion models access at the level of the GQA group ("Riepilogo Tecnico:
-    Fluxion", "Intuizioni Chiave": one KV block fetched serves every query head
-    of its group).  Reading: the shared list of a group gets the largest of its
-    heads' budgets, so no head attends fewer blocks than its own budget.
-    Returned per query head (equal within a group).
+    Fluxion", "Componenti di Sistema", "Selettore Granularità-Budget"; one KV
+    block fetched serves every query head of its group).  Reading: the group
+    is the unit the budget is shifted between.  Its demand is that of its most
+    demanding head (the shared list has to cover that head), and Max-Min
+    shifting runs over the groups from the uniform budget, so the groups'
+    total stays Hkv * k_uniform and the heads' total Hq * k_uniform, as with
+    per-head budgets.  Returned per query head (equal within a group).
     """
-    out = []
-    for h in range(len(budgets)):
-        g = h // group
-        out.append(max(budgets[g * group:(g + 1) * group]))
-    return out
+    H = len(demand)
+    g_demand = [max(demand[g * group:(g + 1) * group]) for g in range(H // group)]
+    k_g = maxmin_shift(k_uniform, g_demand, k_min, nb)
+    return [k_g[h // group] for h in range(H)]
 
 
 def item_costs(budgets: list[int], nb: int) -> list[int]:

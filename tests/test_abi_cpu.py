@@ -204,6 +204,22 @@ def test_device_calls_reject_bad_arguments_before_launch(sa):
     assert lib.sparse_attn_forward(s, None, P, P, P, P, P, 9, P, 1, None, P, None) == 1
     # pool_kcache is decode only
     assert lib.sparse_attn_pool_kcache(s, P, P, None) == 1
+    # the per-kind decode calls: prefill plans, unknown kinds, not uploaded
+    assert lib.sparse_attn_select_kind(s, plan.handle, P, P, P, 9, 1, None) == 1
+    assert lib.sparse_attn_forward_kind(s, plan.handle, P, P, P, P, P, 9, P, 0, None, P, 1,
+                                        None) == 1
+    dshape = sa.Shape.decode(2048, 32, 8, 2, 128, 2)
+    dplan = sa.sparse_attn_plan(dshape, 8, head_kind=[1, 0] * 4, window_blocks=4,
+                                num_workers=1)
+    ds = ctypes.byref(dshape)
+    assert lib.sparse_attn_select_kind(ds, dplan.handle, P, P, P, 16, 2, None) == 1
+    assert lib.sparse_attn_select_kind(ds, dplan.handle, None, P, P, 16, 1, None) == 8
+    assert lib.sparse_attn_forward_kind(ds, dplan.handle, P, P, P, P, P, 16, P, 0, None, P, 7,
+                                        None) == 1
+    assert lib.sparse_attn_forward_kind(ds, None, P, P, P, P, P, 16, P, 0, None, P, 0,
+                                        None) == 1
+    assert lib.sparse_attn_forward_kind(ds, dplan.handle, P, P, P, P, P, 16, P, 0, None, P, 0,
+                                        None) == 8
     n = ctypes.c_size_t()
     assert lib.sparse_attn_score_workspace_size(s, ctypes.byref(n)) == 0
     assert n.value == (8 + 2) * 64 * 64 * 4
@@ -211,8 +227,8 @@ def test_device_calls_reject_bad_arguments_before_launch(sa):
 
 @pytest.mark.parametrize("seed", range(12))
 def test_group_shared_plan_matches_oracle(sa, seed):
-    # one list per KV group: every head of a group gets the group's largest
-    # Max-Min budget, and the schedule is built on those budgets
+    # one list per KV group: Max-Min shifting between the groups, each with
+    # its most demanding head's demand, and the schedule on those budgets
     r = random.Random(100 + seed)
     Hkv = r.choice([1, 2, 4])
     G = r.choice([1, 2, 4, 7])
@@ -226,7 +242,7 @@ def test_group_shared_plan_matches_oracle(sa, seed):
     shape = sa.Shape.prefill(nb * B, B, Hq, Hkv, 64)
     got = sa.sparse_attn_plan(shape, k_u, demand=demand, num_workers=W, schedule=policy,
                               group_shared=True).get()
-    k = op.group_budgets(op.maxmin_shift(k_u, demand, 2, nb), G)
+    k = op.group_budgets(k_u, demand, G, 2, nb)
     wptr, items, loads = op.schedule(k, nb, W, policy, G)
     assert got["budgets"].tolist() == k
     assert got["wptr"].tolist() == wptr

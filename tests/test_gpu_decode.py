@@ -250,3 +250,43 @@ def test_decode_all_streaming_with_block_sizes(env):
     o, _ = od.decode_attend(gen.bf16_to_f64(x["q"]), gen.bf16_to_f32(x["k"]),
                             gen.bf16_to_f32(x["v"]), idx, cnt, w.block)
     assert np.abs(out.cpu().numpy() - o).max() <= P.MAX_ABS
+
+
+@pytest.mark.parametrize("case", ["small", "full", "block_sizes"])
+def test_decode_overlapped_step_equals_the_serial_step(env, case):
+    """Streaming heads selected and attended on a side stream beside the
+    retrieval heads' scoring: the same kernels run on the same rows, so every
+    output, log-sum-exp, index and count equals the serial step's."""
+    import json
+    import os
+    sa, torch = env
+    from head_heterogeneous_block_gb300.layer import DecodeStep
+    from tests._parity import to_dev
+    from workloads import generate, scaled, workload
+    w = workload(5) if case != "small" else scaled(workload(5), 4096, batch=3)
+    x = generate.decode_inputs(w)
+    kinds = generate.head_kinds(w)
+    shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                            w.batch)
+    kw = {}
+    if case == "block_sizes":
+        root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+        with open(os.path.join(root, "workloads", "demands.json")) as f:
+            prof = json.load(f)["5"]["granularity"]
+        kw = {"granularity": prof["gran"], "head_budget": prof["budget"]}
+    t = {n: to_dev(x[n]) for n in "qkv"}
+    res = []
+    for overlap in (False, True):
+        step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
+                          with_lse=True, out_dtype=torch.float32, overlap=overlap, **kw)
+        step.build_cache(t["k"])
+        for _ in range(2):   # a second call on the same buffers changes nothing
+            step.idx.fill_(-5)
+            step.out.fill_(float("nan"))
+            out = step(t["q"], t["k"], t["v"])
+            torch.cuda.synchronize()
+            assert int(step.dev_status.item()) == 0
+        res.append((out.clone(), step.lse.clone(), step.idx.clone(), step.cnt.clone()))
+        del step
+    for a, b in zip(res[0], res[1]):
+        assert torch.equal(a, b)

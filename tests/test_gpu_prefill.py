@@ -260,7 +260,7 @@ def test_prefill_full_size(env, number):
         torch.cuda.empty_cache()
 
 
-def _check_group_shared(r, x, w, args_budgets):
+def _check_group_shared(r, x, w, k_uniform, demand):
     """Group-shared selection: one list per (KV group, row), equal across the
     group's heads, matching the oracle's selection on the group-pooled scores;
     attention checked on the GPU's own lists."""
@@ -268,7 +268,7 @@ def _check_group_shared(r, x, w, args_budgets):
     from oracle import plan as op
     from tests import _parity as P
     G, nb = w.group, w.nb
-    assert r["budgets"] == op.group_budgets(args_budgets, G)
+    assert r["budgets"] == op.group_budgets(k_uniform, demand, G, 2, nb)
     idx, cnt = r["idx"], r["cnt"]
     for g in range(w.num_kv_heads):
         for hh in range(1, G):
@@ -297,7 +297,7 @@ def test_prefill_group_shared_parity(env, number, S, Hq, Hkv):
     r = _run(sa, torch, w, x, {"k_uniform": k_u, "demand": demand, "group_shared": True},
              workers=16)
     assert r["status"] == 0
-    _check_group_shared(r, x, w, op.maxmin_shift(k_u, demand, 2, nb))
+    _check_group_shared(r, x, w, k_u, demand)
     P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, range(Hq * nb),
                       w.group)
 
@@ -319,7 +319,7 @@ def test_prefill_group_shared_full_size(env):
                  schedule="lpt_grouped", workers=W, out_dtype=out_dtype)
         assert r["status"] == 0
         if out_dtype == "float32":
-            _check_group_shared(r, x, w, prof["budgets_maxmin"])
+            _check_group_shared(r, x, w, prof["k_uniform"], prof["demand"])
         items = P.sample_items(r["budgets"], w.nb, per_head, seed=33)
         P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group,
                           bf16_out=out_dtype == "bfloat16")

@@ -15,9 +15,37 @@ from oracle import plan as P
 
 
 def test_group_budgets_hand_example():
-    assert P.group_budgets([2, 5, 3, 4, 7, 1, 1, 1], 4) == [5, 5, 5, 5, 7, 7, 7, 7]
-    assert P.group_budgets([3, 9, 2], 1) == [3, 9, 2]
-    assert P.group_budgets([4, 2, 6, 6], 2) == [4, 4, 6, 6]
+    # groups demand [5, 4]: levelled at once, every head keeps 4
+    assert P.group_budgets(4, [2, 5, 3, 4], 2, 2, 8) == [4, 4, 4, 4]
+    # groups demand [7, 2]: the second gives until it reaches k_min (4->3->2)
+    assert P.group_budgets(4, [1, 7, 2, 2], 2, 2, 8) == [6, 6, 2, 2]
+    # a group's demand is its most demanding head's, not the sum or mean
+    assert P.group_budgets(5, [9, 1, 1, 1, 2, 2, 2, 2], 4, 2, 16) == [8] * 4 + [2] * 4
+
+
+def test_group_budgets_of_groups_of_one_are_the_per_head_budgets():
+    r = np.random.default_rng(21)
+    for _ in range(20):
+        H, nb = int(r.integers(1, 9)), int(r.integers(4, 40))
+        k_u = int(r.integers(2, nb + 1))
+        demand = r.integers(0, nb + 1, H).tolist()
+        assert P.group_budgets(k_u, demand, 1, 2, nb) == P.maxmin_shift(k_u, demand, 2, nb)
+
+
+def test_group_budgets_conserve_the_total_and_follow_demand():
+    r = np.random.default_rng(22)
+    for _ in range(30):
+        Hkv, G, nb = int(r.integers(1, 6)), int(r.choice([2, 4, 7])), int(r.integers(8, 64))
+        k_u = int(r.integers(2, nb // 2 + 1))
+        demand = r.integers(0, nb + 1, Hkv * G).tolist()
+        k = P.group_budgets(k_u, demand, G, 2, nb)
+        assert sum(k) == Hkv * G * k_u                       # conserved, as per head
+        assert all(len(set(k[g * G:(g + 1) * G])) == 1 for g in range(Hkv))
+        gd = [max(demand[g * G:(g + 1) * G]) for g in range(Hkv)]
+        for a in range(Hkv):
+            for b in range(Hkv):
+                if gd[a] > gd[b]:
+                    assert k[a * G] >= k[b * G]
 
 
 def test_group_scores_equal_scores_of_the_mean_pooled_query():
@@ -50,7 +78,7 @@ def test_grouped_selection_when_heads_agree_is_per_head_selection():
     Hkv, G, nb = 2, 4, 10
     base = np.tril(r.standard_normal((Hkv, nb, nb))) + np.triu(np.full((nb, nb), -np.inf), 1)
     scores = np.repeat(base, G, axis=0)          # the G heads of a group have equal scores
-    budgets = P.group_budgets([3, 6, 2, 4, 5, 5, 8, 2], G)
+    budgets = P.group_budgets(4, [3, 6, 2, 4, 5, 5, 8, 2], G, 2, nb)
     a = A.select_all(scores, budgets, nb)
     b = A.select_all_grouped(scores, budgets, G, nb)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
@@ -80,7 +108,7 @@ def test_grouped_lists_are_shared_and_well_formed():
     r = np.random.default_rng(15)
     Hq, G, nb = 8, 4, 16
     scores = np.tril(r.standard_normal((Hq, nb, nb))) + np.triu(np.full((nb, nb), -np.inf), 1)
-    budgets = P.group_budgets([2, 9, 4, 3, 6, 6, 2, 16], G)
+    budgets = P.group_budgets(6, [2, 9, 4, 3, 6, 6, 2, 16], G, 2, 16)
     kmax = max(budgets)
     idx, cnt = A.select_all_grouped(scores, budgets, G, kmax)
     for h in range(Hq):
