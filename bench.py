@@ -295,7 +295,23 @@ def run_ours(args):
             "budgets": "Max-Min shifted between KV groups, each demanding its most "
                        "demanding head's blocks",
             "device_status": int(lg.dev_status.item())}
-        del lg
+        # the same lists with head pairs on one K/V block load each
+        lp = PrefillLayer(shape, prof["k_uniform"], demand=prof["demand"], k_min=prof["k_min"],
+                          num_workers=sms, schedule=args.schedule, device=dev,
+                          group_shared=True, share_kv=True)
+        lp.idx.copy_(lg.idx)
+        lp.cnt.copy_(lg.cnt)
+        for _ in range(2):
+            lp.attend(t["q"], t["k"], t["v"], stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(5):
+            lp.attend(t["q"], t["k"], t["v"], stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        group_shared["share_kv_forward_ms"] = round(a.elapsed_time(b) / 5, 4)
+        group_shared["share_kv_device_status"] = int(lp.dev_status.item())
+        del lg, lp
 
     # ---- output-aware demands (calibration signal only; same kernels)
     output_aware = None
@@ -499,6 +515,35 @@ def bench_decode(dev, stream):
         torch.cuda.synchronize(dev)
         ov_times.append(e0.elapsed_time(e1))
     ov_status = int(ov.dev_status.item())
+    # the overlapped step captured once in a CUDA graph and replayed, as a
+    # serving loop runs its decode steps
+    graph_ms = None
+    try:
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            ov(t["q"], t["k"], t["v"])
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            ov(t["q"], t["k"], t["v"])
+        torch.cuda.synchronize(dev)
+        for _ in range(3):
+            g.replay()
+        gr_times = []
+        for _ in range(10):
+            flush.max()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            gr_times.append(e0.elapsed_time(e1))
+        graph_ms = round(statistics.median(gr_times), 4)
+        del g
+    except RuntimeError as exc:   # capture refused: report it, keep the eager numbers
+        graph_ms = f"capture failed: {str(exc)[:80]}"
+    ov_status = max(ov_status, int(ov.dev_status.item()))
     del ov
     # touched bytes: union of selected blocks per (sequence, kv head), K and V
     idx = step.idx.view(w.batch, w.num_q_heads, step.kmax).cpu().numpy()
@@ -525,6 +570,7 @@ def bench_decode(dev, stream):
            "touched_kv_bytes": kv_bytes, "kbar_bytes": kbar_bytes,
            "kcache_pool_ms": round(a.elapsed_time(b), 4),
            "overlapped": {"ms_per_step": round(statistics.median(ov_times), 4),
+                          "graph_ms_per_step": graph_ms,
                           "how": "streaming heads selected and attended on a side stream "
                                  "while the retrieval heads score, select and attend",
                           "device_status": ov_status},

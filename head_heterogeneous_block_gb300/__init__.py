@@ -60,7 +60,8 @@ class _PlanParams(ctypes.Structure):
                 ("window_blocks", ctypes.c_int32), ("num_workers", ctypes.c_int32),
                 ("schedule", ctypes.c_int32), ("group_shared", ctypes.c_int32),
                 ("granularity", ctypes.POINTER(ctypes.c_int32)),
-                ("head_budget", ctypes.POINTER(ctypes.c_int32))]
+                ("head_budget", ctypes.POINTER(ctypes.c_int32)),
+                ("share_kv", ctypes.c_int32)]
 
 
 class SparseAttnError(RuntimeError):
@@ -230,7 +231,7 @@ class Plan:
 def sparse_attn_plan(shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
                      head_kind=None, window_blocks: int = 0, num_workers: int = 152,
                      schedule="lpt", group_shared: bool = False, granularity=None,
-                     head_budget=None) -> Plan:
+                     head_budget=None, share_kv: bool = False) -> Plan:
     if isinstance(schedule, str):
         schedule = SCHEDULES[schedule]
     params = _PlanParams()
@@ -254,6 +255,7 @@ def sparse_attn_plan(shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
     params.num_workers = num_workers
     params.schedule = schedule
     params.group_shared = 1 if group_shared else 0
+    params.share_kv = 1 if share_kv else 0
     out = ctypes.c_void_p()
     _check(_lib.sparse_attn_plan(ctypes.byref(shape), ctypes.byref(params), ctypes.byref(out)),
            "sparse_attn_plan")

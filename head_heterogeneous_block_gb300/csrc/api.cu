@@ -165,7 +165,7 @@ sa_status forward_rows(const sa_shape* shp, const sa_plan* plan, const void* q, 
   a.wptr = plan->d_wptr;
   a.items = plan->d_items;
   a.num_workers = plan->num_workers;
-  a.num_items = shp->num_q_heads * plan->nb;
+  a.num_items = (plan->paired ? shp->num_q_heads / 2 : shp->num_q_heads) * plan->nb;
   a.S = int(shp->seq_len);
   a.B = shp->block;
   a.d = shp->head_dim;
@@ -177,7 +177,8 @@ sa_status forward_rows(const sa_shape* shp, const sa_plan* plan, const void* q, 
   a.dev_status = dev_status;
   a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   bool encode_failed = false;
-  cudaError_t e = sa_k::launch_prefill_attention(a, st, &encode_failed);
+  cudaError_t e = plan->paired ? sa_k::launch_prefill_attention_pairs(a, st, &encode_failed)
+                               : sa_k::launch_prefill_attention(a, st, &encode_failed);
   if (encode_failed) return SA_ERR_CUDA;
   return cuda_status(e);
 }
@@ -328,7 +329,7 @@ sa_status sparse_attn_select_topp(const sa_shape* shp, const sa_plan* plan, cons
 
 sa_status sparse_attn_plan_rebuild(sa_plan* plan, const int32_t* cnt, sa_stream_t stream) {
   if (!plan || !cnt) return SA_ERR_INVALID_ARG;
-  if (plan->shape.mode != SA_MODE_PREFILL) return SA_ERR_INVALID_ARG;
+  if (plan->shape.mode != SA_MODE_PREFILL || plan->group_shared) return SA_ERR_INVALID_ARG;
   if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
   if (plan->num_workers > 256 || plan->nb > 2048) return SA_ERR_UNSUPPORTED;
   if (plan->items.size() > (size_t(1) << 19)) return SA_ERR_UNSUPPORTED;

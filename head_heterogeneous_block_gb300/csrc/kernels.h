@@ -105,6 +105,10 @@ struct PrefillArgs {
 // Returns cudaSuccess, or an error; *encode_failed is set when a TMA
 // descriptor could not be built.
 cudaError_t launch_prefill_attention(const PrefillArgs& a, cudaStream_t st, bool* encode_failed);
+// Group-shared lists, even G: items are head pairs p*nb + i (num_items = Hq/2 * nb),
+// each K/V block feeding both heads' tiles.
+cudaError_t launch_prefill_attention_pairs(const PrefillArgs& a, cudaStream_t st,
+                                           bool* encode_failed);
 
 struct DecodeArgs {
   const void* q;            // [Bt][Hq][d]

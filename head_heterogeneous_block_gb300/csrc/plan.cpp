@@ -285,8 +285,24 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* p, sa_plan
         for (int32_t h = 0; h < H; ++h) plan->budgets[h] = k_g[h / G];
       }
       plan->num_workers = p->num_workers;
-      sa_host::build_schedule(plan->budgets, nb, plan->group, p->num_workers, p->schedule,
-                              plan->wptr, plan->items, plan->loads);
+      if (p->share_kv != 0 && (p->share_kv != 1 || !p->group_shared || plan->group % 2 != 0)) {
+        delete plan;
+        return SA_ERR_INVALID_ARG;
+      }
+      if (p->share_kv) {
+        // the two heads of a pair share their list: the work item is (pair,
+        // query block), costing both heads' blocks; the greedy runs on the
+        // pairs' budgets, G/2 pairs per KV group
+        plan->paired = 1;
+        std::vector<int32_t> pair_budgets(H / 2);
+        for (int32_t x = 0; x < H / 2; ++x) pair_budgets[x] = plan->budgets[2 * x];
+        sa_host::build_schedule(pair_budgets, nb, plan->group / 2, p->num_workers, p->schedule,
+                                plan->wptr, plan->items, plan->loads);
+        for (int64_t& l : plan->loads) l *= 2;
+      } else {
+        sa_host::build_schedule(plan->budgets, nb, plan->group, p->num_workers, p->schedule,
+                                plan->wptr, plan->items, plan->loads);
+      }
       plan->kmax = 0;
       for (int32_t k : plan->budgets) plan->kmax = std::max(plan->kmax, std::min(k, nb));
       plan->total_blocks = 0;
@@ -296,7 +312,7 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* p, sa_plan
         plan->makespan = std::max(plan->makespan, l);
       }
     } else {
-      if (p->demand || p->group_shared) { delete plan; return SA_ERR_INVALID_ARG; }
+      if (p->demand || p->group_shared || p->share_kv) { delete plan; return SA_ERR_INVALID_ARG; }
       bool any_streaming = false;
       if (p->head_kind) {
         for (int32_t h = 0; h < H; ++h) {
@@ -374,7 +390,7 @@ sa_status sparse_attn_plan_info(const sa_plan* plan, int32_t* num_workers, int32
   if (num_workers) *num_workers = plan->num_workers;
   if (num_items)
     *num_items = plan->shape.mode == SA_MODE_PREFILL
-                     ? plan->shape.num_q_heads * plan->nb
+                     ? int32_t(plan->items.size())   // Hq*nb, or Hq/2*nb head pairs
                      : plan->shape.batch * plan->shape.num_q_heads;
   if (kmax) *kmax = plan->kmax;
   if (total_blocks) *total_blocks = plan->total_blocks;

@@ -16,6 +16,7 @@ struct sa_plan {
   int32_t k_uniform = 0;
   int32_t window_blocks = 0;
   int32_t group_shared = 0;       // one block list per KV group
+  int32_t paired = 0;             // group-shared, even G: items are head pairs
   int64_t total_blocks = 0;
   int64_t makespan = 0;
   std::vector<int32_t> budgets;   // [Hq]

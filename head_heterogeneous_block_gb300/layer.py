@@ -20,14 +20,15 @@ from . import (SA_HEAD_RETRIEVAL, SA_HEAD_STREAMING, Shape, sparse_attn_forward,
 class PrefillLayer:
     def __init__(self, shape: Shape, k_uniform: int, demand=None, k_min: int = 2,
                  num_workers: int | None = None, schedule="lpt_grouped", device="cuda",
-                 with_lse: bool = False, out_dtype=torch.bfloat16, group_shared: bool = False):
+                 with_lse: bool = False, out_dtype=torch.bfloat16, group_shared: bool = False,
+                 share_kv: bool = False):
         dev = torch.device(device)
         if num_workers is None:
             num_workers = torch.cuda.get_device_properties(dev).multi_processor_count
         self.shape = shape
         self.plan = sparse_attn_plan(shape, k_uniform, demand=demand, k_min=k_min,
                                      num_workers=num_workers, schedule=schedule,
-                                     group_shared=group_shared)
+                                     group_shared=group_shared, share_kv=share_kv)
         self.plan.upload()
         info = self.plan.info()
         self.kmax = info["kmax"]

@@ -124,10 +124,12 @@ typedef struct sa_plan_params {
   int32_t group_shared;     /* prefill: 0 = one block list per query head;
                                1 = one list per KV group (GQA-group-shared
                                selection): the G heads of a group share the
-                               blocks chosen on their summed scores, with the
-                               largest of their budgets.  Must be 0 for decode.
-                               (Fluxion, "Intuizioni Chiave": group-level KV
-                               access.)                                      */
+                               blocks chosen on their summed scores.  Budgets
+                               are Max-Min shifted between the KV groups, each
+                               group demanding its most demanding head's
+                               blocks, so the total stays Hq*k_uniform.
+                               Must be 0 for decode.  (Fluxion, "Componenti di
+                               Sistema": GQA access modelled per group.)     */
   const int32_t* granularity; /* decode: [Hq] tokens per selection block of each
                                retrieval head: a multiple of 16 that divides L,
                                with L / g <= 4096, at most 8 distinct sizes;
@@ -141,6 +143,12 @@ typedef struct sa_plan_params {
                                at its own block size, >= k_min (capped at its
                                block count); NULL = k_uniform.  Must be NULL
                                for prefill.                                   */
+  int32_t share_kv;         /* prefill, group-shared plans with an even G: 1 =
+                               the two heads of a head pair run on one K/V
+                               block load (items are head pairs, see the
+                               schedule below); 0 = one query head per item,
+                               the pair's shared blocks then meet in L2.
+                               Must be 0 otherwise.                           */
 } sa_plan_params;
 
 typedef struct sa_plan sa_plan;
@@ -158,7 +166,9 @@ const char* sa_status_string(sa_status status);
  * blocks; LPT walks items by cost descending (ties: lower id) and gives each
  * to the least-loaded worker (ties: lowest worker); LPT_GROUPED walks KV
  * group by KV group, cost descending inside a group; HEAD_ORDER gives worker
- * w the contiguous id range [w*N/W, (w+1)*N/W).
+ * w the contiguous id range [w*N/W, (w+1)*N/W).  Plans with share_kv = 1
+ * schedule head pairs instead: item (p, i) has id p*nb+i, covers heads 2p and
+ * 2p+1, and costs 2*min(k_p, i+1) blocks (G/2 pairs per KV group).
  * Decode: retrieval heads keep k_uniform blocks (or head_budget[h] blocks of
  * granularity[h] tokens), streaming heads block 0 plus the last window_blocks
  * blocks of B; no schedule is built.
@@ -172,7 +182,9 @@ sa_status sparse_attn_plan(const sa_shape* shp, const sa_plan_params* params,
                            sa_plan** out);
 
 /*
- * Sizes of a plan: workers W, items N (Hq*nb prefill, Bt*Hq decode), the
+ * Sizes of a plan: workers W, items N (Hq*nb prefill, Bt*Hq decode; Hq/2*nb
+ * for a plan with share_kv = 1, where an item is a head pair, see
+ * sparse_attn_plan), the
  * idx row stride kmax it needs (max over heads of the blocks one row keeps),
  * the total of all item costs in blocks, and the schedule's makespan (the
  * largest worker load, in blocks).  Any output pointer may be NULL.

@@ -168,6 +168,20 @@ def schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int 
     return wptr, items, loads
 
 
+def pair_schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int):
+    """Schedule of a group-shared plan whose KV groups have an even number of
+    query heads: the heads 2p and 2p+1 share their block list, so the work
+    item is (pair p, query block i), id p*nb + i, and one K/V block load
+    serves both.  Reading: the greedy of ``schedule`` runs on the pairs'
+    budgets with group/2 pairs per KV group; an item costs both heads'
+    blocks, 2 * min(k_p, i+1), so loads count head-blocks as per-head plans
+    do (the factor changes no decision of the greedy).
+    """
+    pair_budgets = [budgets[2 * x] for x in range(len(budgets) // 2)]
+    wptr, items, loads = schedule(pair_budgets, nb, workers, policy, group // 2)
+    return wptr, items, [2 * x for x in loads]
+
+
 def schedule_from_costs(costs: list[int], workers: int, within: str = "assignment"):
     """LPT over given item costs (e.g. the block counts a data-dependent
     selection produced): items by cost descending, ties lower id, each to the

@@ -240,10 +240,14 @@ def test_group_shared_plan_matches_oracle(sa, seed):
     demand = [r.randint(0, nb + 3) for _ in range(Hq)]
     from oracle import plan as op
     shape = sa.Shape.prefill(nb * B, B, Hq, Hkv, 64)
+    share = G % 2 == 0 and r.random() < 0.5   # head pairs on one K/V load
     got = sa.sparse_attn_plan(shape, k_u, demand=demand, num_workers=W, schedule=policy,
-                              group_shared=True).get()
+                              group_shared=True, share_kv=share).get()
     k = op.group_budgets(k_u, demand, G, 2, nb)
-    wptr, items, loads = op.schedule(k, nb, W, policy, G)
+    if share:
+        wptr, items, loads = op.pair_schedule(k, nb, W, policy, G)
+    else:
+        wptr, items, loads = op.schedule(k, nb, W, policy, G)
     assert got["budgets"].tolist() == k
     assert got["wptr"].tolist() == wptr
     assert got["items"].tolist() == items
@@ -254,6 +258,22 @@ def test_group_shared_is_prefill_only(sa):
     shape = sa.Shape.decode(4096, 32, 8, 2, 128, 2)
     with pytest.raises(sa.SparseAttnError):
         sa.sparse_attn_plan(shape, 8, num_workers=1, group_shared=True)
+
+
+def test_shared_kv_loads_need_group_shared_lists_and_an_even_group(sa):
+    # pairs of heads can share a K/V load only when they share the list
+    with pytest.raises(sa.SparseAttnError):
+        sa.sparse_attn_plan(sa.Shape.prefill(4096, 64, 8, 2, 64), 8, num_workers=4,
+                            share_kv=True)
+    with pytest.raises(sa.SparseAttnError):      # G = 3
+        sa.sparse_attn_plan(sa.Shape.prefill(4096, 64, 6, 2, 64), 8, num_workers=4,
+                            group_shared=True, share_kv=True)
+    with pytest.raises(sa.SparseAttnError):
+        sa.sparse_attn_plan(sa.Shape.decode(4096, 32, 8, 2, 128, 2), 8, num_workers=1,
+                            share_kv=True)
+    p = sa.sparse_attn_plan(sa.Shape.prefill(4096, 64, 8, 2, 64), 8, num_workers=4,
+                            group_shared=True, share_kv=True)
+    assert p.info()["num_items"] == 4 * 64
 
 
 @pytest.mark.parametrize("number", [1, 2, 3])

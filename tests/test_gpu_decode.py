@@ -290,3 +290,40 @@ def test_decode_overlapped_step_equals_the_serial_step(env, case):
         del step
     for a, b in zip(res[0], res[1]):
         assert torch.equal(a, b)
+
+
+def test_decode_overlapped_step_replays_from_a_cuda_graph(env):
+    """The overlapped step (two streams, five launches) captured in a CUDA
+    graph: replays give the eager step's output and lists exactly, and the
+    calls allocate nothing while captured."""
+    sa, torch = env
+    from head_heterogeneous_block_gb300.layer import DecodeStep
+    from tests._parity import to_dev
+    from workloads import generate, scaled, workload
+    w = scaled(workload(5), 8192, batch=4)
+    x = generate.decode_inputs(w)
+    kinds = generate.head_kinds(w)
+    shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                            w.batch)
+    t = {n: to_dev(x[n]) for n in "qkv"}
+    step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
+                      with_lse=True, out_dtype=torch.float32, overlap=True)
+    step.build_cache(t["k"])
+    want = step(t["q"], t["k"], t["v"]).clone()
+    want_idx = step.idx.clone()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        step(t["q"], t["k"], t["v"])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        step(t["q"], t["k"], t["v"])
+    for _ in range(2):
+        step.out.fill_(float("nan"))
+        step.idx.fill_(-3)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(step.out, want) and torch.equal(step.idx, want_idx)
+    assert int(step.dev_status.item()) == 0

@@ -188,7 +188,8 @@ def test_later_blocks_scoring_far_above_the_first(env, factor, exact):
     assert (s_jump / np.sqrt(w.head_dim) / np.log(2) > 100) == exact
 
 
-def test_wait_timeout_is_reported_and_the_context_stays_usable(env):
+@pytest.mark.parametrize("pairs", [False, True])
+def test_wait_timeout_is_reported_and_the_context_stays_usable(env, pairs):
     """The forward's watchdog: with every wait limited to 100 ns (far below
     the latency of the first copy from memory), waits run out on every CTA.
     The launch must report SA_DEV_TIMEOUT and return; each CTA drains its own
@@ -199,7 +200,8 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable(env):
     w = scaled(workload(1), 4096)
     x = generate.prefill_inputs(w)
     W = torch.cuda.get_device_properties(0).multi_processor_count
-    r = _run(sa, torch, w, x, {"k_uniform": 9}, workers=W)
+    r = _run(sa, torch, w, x, {"k_uniform": 9, "group_shared": pairs, "share_kv": pairs},
+             workers=W)
     layer, t = r["layer"], r["tensors"]
     assert r["status"] == 0
     want = layer.out.clone()
@@ -282,8 +284,10 @@ def _check_group_shared(r, x, w, k_uniform, demand):
 
 
 @pytest.mark.parametrize("number,S,Hq,Hkv", [(1, 4096, 8, 2), (2, 4096, 8, 2), (2, 2432, 8, 8),
-                                             (2, 8192, 16, 4)])
+                                             (2, 8192, 16, 4), (2, 4096, 8, 4), (1, 2368, 16, 2)])
 def test_prefill_group_shared_parity(env, number, S, Hq, Hkv):
+    """Group-shared lists, one query head per item; with an even G also head
+    pairs, one K/V block load feeding both heads' tiles."""
     sa, torch = env
     from oracle import plan as op
     from tests import _parity as P
@@ -294,12 +298,34 @@ def test_prefill_group_shared_parity(env, number, S, Hq, Hkv):
     k_u = max(2, op.budget_for_density(w.target_density, nb))
     rng = np.random.default_rng(S + 7)
     demand = rng.integers(1, nb, Hq).tolist()
-    r = _run(sa, torch, w, x, {"k_uniform": k_u, "demand": demand, "group_shared": True},
-             workers=16)
+    for share in ([False, True] if w.group % 2 == 0 else [False]):
+        r = _run(sa, torch, w, x, {"k_uniform": k_u, "demand": demand, "group_shared": True,
+                                   "share_kv": share}, workers=16)
+        assert r["status"] == 0
+        _check_group_shared(r, x, w, k_u, demand)
+        P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, range(Hq * nb),
+                          w.group)
+
+
+def test_prefill_group_shared_dense_pairs_equal_causal_attention(env):
+    # every block kept: the pair kernel's output is dense causal attention for
+    # every head, against the library's SDPA as well as the oracle
+    sa, torch = env
+    from tests import _parity as P
+    from workloads import generate, scaled, workload
+    w = scaled(workload(2), 4096, 8, 2)
+    x = generate.prefill_inputs(w)
+    r = _run(sa, torch, w, x, {"k_uniform": w.nb, "group_shared": True, "share_kv": True},
+             workers=11)
     assert r["status"] == 0
-    _check_group_shared(r, x, w, k_u, demand)
-    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, range(Hq * nb),
-                      w.group)
+    assert r["layer"].plan.info()["num_items"] == w.num_q_heads // 2 * w.nb
+    P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block,
+                      range(w.num_q_heads * w.nb), w.group)
+    t = r["tensors"]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        t["q"].float()[None], t["k"].float().repeat_interleave(w.group, 0)[None],
+        t["v"].float().repeat_interleave(w.group, 0)[None], is_causal=True)[0]
+    assert float((ref - torch.from_numpy(r["out"]).cuda()).abs().max()) < 1e-2
 
 
 def test_prefill_group_shared_full_size(env):
