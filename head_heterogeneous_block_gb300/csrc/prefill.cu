@@ -20,14 +20,19 @@
 //               the four schedulers.
 //   warps 4-19  softmax, four column groups of four warps: each thread owns
 //               one row of the tile and a quarter of its S columns (and of
-//               O's).  The groups exchange partial row maxima through a
-//               double-buffered shared array; a block's exponentials use the
-//               running maximum, and when the exchange shows that the block
-//               raised a row's maximum by more than 2^8 (rare), O and that
-//               row's P are scaled down before P V.  The stale maximum cancels
-//               in O / l.  The normaliser sums the same bf16-rounded weights
-//               that enter P V.  Epilogue: O / l in fp32 or bf16, and the
-//               log-sum-exp.
+//               O's).  The first block of every item is the sink block 0; its
+//               row maximum, exchanged once between the four groups, is the
+//               reference maximum m of the row for the whole item.  Every
+//               block's weights are 2^(s*c - m), so a later block may give
+//               weights above 1; m cancels in O / l, so there is no per-block
+//               exchange and no rescale of O.  The normaliser sums the same
+//               bf16-rounded weights that enter P V.  A row whose normaliser
+//               passes 2^100, or whose O is not finite, is marked and, after
+//               the worker's last item, recomputed exactly in fp32 on the CUDA
+//               cores.  Epilogue (after the next item's first block): O / l
+//               and the log-sum-exp; fp32 output is stored directly, bf16
+//               output is staged, 128-byte swizzled, in the finished item's Q
+//               stage and written by TMA stores.
 //
 // The work items and their order come from the plan's LPT schedule (S-HPLB,
 // "Algoritmo Greedy"), with workers = CTAs instead of GPUs.
