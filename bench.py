@@ -137,8 +137,8 @@ def job_value(flops_per_replica_step: float, world: int, steps: int, total_ms: f
 # summarised in profiles/prefill_attention_llama8b_128k.md.  It describes only
 # the kernel source with this SHA-256; for any other source it is not reported.
 FORWARD_TRAFFIC = {"workload": 3,
-                   "sha256": "41ef4947e3267ee245d86ff9bacc6f7176ce1c01da3541e013c121684d7b36ee",
-                   "bytes": 2561218048 + 1065906176}
+                   "sha256": "f8516bed2b3333b3d046dbe541c34e5df147c0eb998bdee4c0053b37bd4c8679",
+                   "bytes": 2685182208 + 1077068800}
 
 
 def _forward_traffic(workload_number: int):
