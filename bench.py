@@ -561,6 +561,12 @@ def bench_decode(dev, stream):
     q_o = 2 * w.batch * w.num_q_heads * w.head_dim * 2
     fwd_ms = statistics.median(fwd)
     peaks = _peaks()
+    # the whole step's compulsory DRAM bytes: pooled keys read by scoring, the
+    # selected K/V (union per KV head) and q / o; the score rows (3.7 MB) and
+    # index lists pass between kernels through L2 and are not counted
+    step_bytes = kbar_bytes + kv_bytes + q_o
+    step_ms = statistics.median(times)
+    ov_ms = statistics.median(ov_times)
     res = {"workload": w.name, "ms_per_step": round(statistics.median(times), 4),
            "score_ms": round(statistics.median(sco), 4),
            "select_ms": round(statistics.median(times) - statistics.median(sco) - fwd_ms, 4),
@@ -568,6 +574,10 @@ def bench_decode(dev, stream):
            "forward_gbs": round((kv_bytes + q_o) / (fwd_ms * 1e-3) / 1e9, 1),
            "forward_frac_hbm": round((kv_bytes + q_o) / (fwd_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
            "touched_kv_bytes": kv_bytes, "kbar_bytes": kbar_bytes,
+           "step_bytes": step_bytes,
+           "step_floor_ms": round(step_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
+           "step_frac_hbm": round(step_bytes / (step_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+           "overlapped_frac_hbm": round(step_bytes / (ov_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
            "kcache_pool_ms": round(a.elapsed_time(b), 4),
            "overlapped": {"ms_per_step": round(statistics.median(ov_times), 4),
                           "graph_ms_per_step": graph_ms,

@@ -705,9 +705,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == 4 && lane == 0) {
         sent = mbar_wait(&sh->stage_bar, pq & 1, abort, p.wait_ns);
         if (sent) {
+          // evict-first: the output is not read again, and its lines would
+          // otherwise push K/V blocks that later items reuse out of L2
 #pragma unroll
           for (int s = 0; s < C::kPanels; ++s)
-            tma_store_2d(&to, stg + s * C::kQPanel, s * 64, pit.h * p.S + pit.i * p.B);
+            tma_store_2d_hint(&to, stg + s * C::kQPanel, s * 64, pit.h * p.S + pit.i * p.B,
+                              l2_policy_evict_first());
           bulk_commit_group();
           bulk_wait_read_all();
           mbar_arrive(&sh->q_empty[pq % C::kNQ]);

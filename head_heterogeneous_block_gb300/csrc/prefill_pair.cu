@@ -649,8 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int x = 0; x < 2; ++x)
 #pragma unroll
             for (int s = 0; s < C::kPanels; ++s)
-              tma_store_2d(&to, sQ + (2 * qs + x) * C::kQBytes + s * C::kQPanel, s * 64,
-                           (2 * pit.p + x) * p.S + pit.i * p.B);
+              tma_store_2d_hint(&to, sQ + (2 * qs + x) * C::kQBytes + s * C::kQPanel, s * 64,
+                                (2 * pit.p + x) * p.S + pit.i * p.B, l2_policy_evict_first());
           bulk_commit_group();
           bulk_wait_read_all();
           mbar_arrive(&sh->q_empty[qs]);
