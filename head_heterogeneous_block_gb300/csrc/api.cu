@@ -150,6 +150,7 @@ sa_status forward_rows(const sa_shape* shp, const sa_plan* plan, const void* q, 
     a.gran = sized ? plan->d_gran : nullptr;
     a.heads = heads;
     a.nh = nh;
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     return cuda_status(sa_k::launch_decode_attention(a, st));
   }
   if (!plan) return SA_ERR_INVALID_ARG;

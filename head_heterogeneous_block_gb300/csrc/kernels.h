@@ -125,6 +125,7 @@ struct DecodeArgs {
   const int32_t* gran;      // [Hq] device block size per head (multiple of 16), or NULL: B
   const int32_t* heads;     // NULL (every head), or the nh heads to run, as for select
   int32_t nh;
+  uint64_t wait_ns;         // limit of each wait for a copy (0: the 4 s default)
 };
 cudaError_t launch_decode_attention(const DecodeArgs& a, cudaStream_t st);
 

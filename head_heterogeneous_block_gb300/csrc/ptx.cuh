@@ -130,6 +130,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global into shared memory; completion is signalled on the
+// mbarrier as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk async group of the
 // issuing thread).  c0 as for tma_load_2d; c1 must not be negative.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0,
