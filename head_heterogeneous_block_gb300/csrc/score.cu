@@ -82,8 +82,9 @@ __device__ __forceinline__ void cp_async8(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_2() {
-  asm volatile("cp.async.wait_group 2;" ::: "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // 16-byte chunk c of a row of kC chunks sits at c ^ 4(r mod kC/4): the rows
 // a quarter-warp reads together land on different banks
@@ -270,16 +271,22 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
     }
     cp_async_commit();                        // empty groups keep the count uniform
   };
-  // chunk k of this CTA's sequence goes to stage k % 3; cur, nx1 are chunks
-  // k and k + 1 (already issued), nx2 is issued into stage (k + 2) % 3
-  int cur = next_chunk(int(blockIdx.x) - int(gridDim.x));
-  int nx1 = next_chunk(cur);
-  issue(cur, 0);
-  issue(nx1, 1);
-  for (int k = 0; cur < total; ++k) {
-    const int nx2 = next_chunk(nx1);
-    issue(nx2, (k + 2) % kStages);
-    cp_async_wait_2();                        // this thread's copies of chunk k landed
+  // chunk k of this CTA's sequence goes to stage k % kStages; ahead[x] is
+  // chunk k + x (issued, x < kStages - 1), and chunk k + kStages - 1 is
+  // issued into the stage chunk k - 1 left
+  int ahead[kStages - 1];
+  ahead[0] = next_chunk(int(blockIdx.x) - int(gridDim.x));
+  issue(ahead[0], 0);
+#pragma unroll
+  for (int x = 1; x < kStages - 1; ++x) {
+    ahead[x] = next_chunk(ahead[x - 1]);
+    issue(ahead[x], x);
+  }
+  for (int k = 0; ahead[0] < total; ++k) {
+    const int cur = ahead[0];
+    const int nxt = next_chunk(ahead[kStages - 2]);
+    issue(nxt, (k + kStages - 1) % kStages);
+    cp_async_wait_group<kStages - 1>();       // this thread's copies of chunk k landed
     __syncthreads();                          // ... and every thread's
     const ScoreStage& sg = st[k % kStages];
     const int bg = cur / per, r0 = (cur - bg * per) * kRows;
@@ -326,9 +333,10 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
         }
       }
     }
-    __syncthreads();                          // stage k % 3 is free for chunk k + 3
-    cur = nx1;
-    nx1 = nx2;
+    __syncthreads();                          // stage k % kStages is free again
+#pragma unroll
+    for (int x = 0; x < kStages - 2; ++x) ahead[x] = ahead[x + 1];
+    ahead[kStages - 2] = nxt;
   }
 }
 }  // namespace
