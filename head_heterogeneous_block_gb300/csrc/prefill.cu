@@ -106,12 +106,14 @@ struct Shared {
   uint64_t o_free;        // one phase per item: every group finished the epilogue
   uint64_t xch_bar;       // exchange between the softmax groups
   uint64_t stage_bar;     // one phase per item: the output tile is staged
+  uint64_t store_done;    // the P.V issuer's output stores have all completed
   uint64_t drain_qk, drain_pv;
   uint64_t info_full[kNI], info_empty[kNI];
   ItemInfo info[kNI];
   uint32_t redo[kRedoWords];
   float xch[2][4][128];   // [use parity][group][row]: partial row max per block, or
                           // partial sum per item; use u goes to buffer u & 1
+  int32_t stage_row[2];   // first output row of the tile staged in Q stage x
   uint32_t tmem_base;
   int abort;
 };
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh->o_free, kSoftmaxThreads);
     mbar_init(&sh->xch_bar, kSoftmaxThreads);
     mbar_init(&sh->stage_bar, kSoftmaxThreads);
+    mbar_init(&sh->store_done, 1);
     mbar_init(&sh->drain_qk, 1);
     mbar_init(&sh->drain_pv, 1);
     sh->abort = 0;
@@ -526,6 +529,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qi = 0, stage = 0, phase = 0;   // S / P buffers
     uint32_t vstage = 0, vphase = 0;         // V ring
     bool ok = true;
+    // bf16 output: this warp also writes the staged output tiles (one TMA
+    // store per 64-column panel) and releases their Q stages, in the time it
+    // otherwise spends waiting for P, so no softmax warp waits for a store.
+    // Item x is staged after the first block of item x+1, so it is stored
+    // before this warp waits for block 1 of item x+1 (or, when that item has
+    // one block, for the first block of item x+2), by which time its staging
+    // has finished anyway.
+    uint32_t spq = 0;                        // next item whose tile is stored
+    auto store_upto = [&](uint32_t upto) -> bool {
+      for (; spq < upto; ++spq) {
+        if (!warp_wait(&sh->stage_bar, spq & 1, abort, p.wait_ns)) return false;
+        if (lane == 0) {
+          const uint8_t* stg = sQ + (spq % C::kNQ) * C::kQBytes;
+          const int32_t r0 = sh->stage_row[spq & 1];
+          // evict-first: the output is not read again, and its lines would
+          // otherwise push K/V blocks that later items reuse out of L2
+#pragma unroll
+          for (int s = 0; s < C::kPanels; ++s)
+            tma_store_2d_hint(&to, stg + s * C::kQPanel, s * 64, r0, l2_policy_evict_first());
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(&sh->q_empty[spq % C::kNQ]);
+        }
+        __syncwarp();
+      }
+      return true;
+    };
     for (;;) {
       const int slot = qi % kNI;
       if (!warp_wait(&sh->info_full[slot], (qi / kNI) & 1, abort, p.wait_ns)) {
@@ -538,6 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n == 0) break;
       for (int t = 0; t < n; ++t) {
         const bool first = t == 0;
+        if (!p.out_f32 && !store_upto(first ? (qi > 0 ? qi - 1 : 0) : qi)) {
+          ok = false;
+          break;
+        }
         const bool need_o = first && qi > 0;   // previous item's epilogue must read O first
         // lane 0: P, lane 1: V, lane 2: O
         uint64_t* bar = &sh->p_full[stage];
@@ -596,8 +630,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++qi;
     }
+    // the last items' tiles (the final one is staged after the list)
+    if (ok && !p.out_f32) ok = store_upto(qi);
     if (lane == 0) {
       if (!ok) raise_abort(sh, p);
+      // the stores complete before the exact pass may rewrite rows and
+      // before the CTA's shared memory goes
+      bulk_wait_all();
+      mbar_arrive(&sh->store_done);
       mma_commit(&sh->drain_pv);
       mbar_wait(&sh->drain_pv, 0, nullptr);
     }
@@ -700,23 +740,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       fence_proxy_async_smem();
+      if (warp == 4 && lane == 0) sh->stage_row[pq & 1] = pit.h * p.S + pit.i * p.B;
+      // the P.V issuer stores the tile once every thread has staged its part
       mbar_arrive(&sh->stage_bar);
-      bool sent = true;
-      if (warp == 4 && lane == 0) {
-        sent = mbar_wait(&sh->stage_bar, pq & 1, abort, p.wait_ns);
-        if (sent) {
-          // evict-first: the output is not read again, and its lines would
-          // otherwise push K/V blocks that later items reuse out of L2
-#pragma unroll
-          for (int s = 0; s < C::kPanels; ++s)
-            tma_store_2d_hint(&to, stg + s * C::kQPanel, s * 64, pit.h * p.S + pit.i * p.B,
-                              l2_policy_evict_first());
-          bulk_commit_group();
-          bulk_wait_read_all();
-          mbar_arrive(&sh->q_empty[pq % C::kNQ]);
-        }
-      }
-      return __all_sync(0xffffffffu, sent);   // the warp gives up together
+      return true;
     };
     for (;;) {
       const int slot = qi % kNI;
@@ -832,8 +859,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && pend) ok = epilogue();
     if (!ok) raise_abort(sh, p);
-    // the output tiles' stores complete before any exact rewrite and exit
-    if (warp == 4 && lane == 0) bulk_wait_all();
+    // the output tiles' stores complete before any exact rewrite
+    if (!p.out_f32 && !wait_all(&sh->store_done, 0, nullptr)) ok = false;
     // every epilogue of the list has set its bits: recompute the marked items,
     // one (row, column group) per thread
     asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
