@@ -67,14 +67,16 @@ class DecodeStep:
     attention.  With ``granularity`` (and ``head_budget``) each retrieval head
     selects ``head_budget[h]`` blocks of ``granularity[h]`` tokens.
 
-    With ``overlap`` the streaming heads, whose block lists do not depend on
-    the scores, are selected and attended on a side stream while the
-    retrieval heads score, select and attend on the caller's stream; the
-    step ends when both are done.  The kernels and results are the same."""
+    By default (``overlap``) the streaming heads, whose block lists do not
+    depend on the scores, are selected and attended on a side stream while
+    the retrieval heads score, select and attend on the caller's stream; the
+    step ends when both are done.  ``overlap=False`` runs the three calls
+    for every head in turn on the caller's stream.  The kernels and results
+    are the same."""
 
     def __init__(self, shape: Shape, budget_blocks: int, head_kind, window_blocks: int,
                  device="cuda", with_lse: bool = False, out_dtype=torch.bfloat16,
-                 granularity=None, head_budget=None, overlap: bool = False):
+                 granularity=None, head_budget=None, overlap: bool = True):
         dev = torch.device(device)
         self.shape = shape
         self.overlap = overlap
