@@ -604,24 +604,35 @@ def bench_decode(dev, stream):
            "kcache_pool_ms": round(a.elapsed_time(b), 4),
            "l2": "flushed between steps (a 256 MB read)"}
     del step
-    res["block_sizes"] = bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush)
+    with open(os.path.join(ROOT, "workloads", "demands.json")) as f:
+        prof = json.load(f)[str(w.number)]["granularity"]
+    res["block_sizes"] = bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush,
+                                                  prof["gran"], prof["budget"])
+    res["block_sizes"]["chosen_by"] = "fewest bytes per KV group"
+    res["block_sizes"]["modelled_bytes_per_sequence"] = prof["bytes"]
+    res["block_sizes"]["modelled_bytes_per_sequence_default"] = prof["bytes_default"]
+    tm = prof["time_model"]
+    res["block_sizes_time_model"] = bench_decode_block_sizes(w, t, kinds, shape, dev, stream,
+                                                             flush, tm["gran"], tm["budget"])
+    res["block_sizes_time_model"].update({
+        "chosen_by": "least modelled step time (measured kernel rates, one scoring pass per "
+                     "size, selection time by the longest row)",
+        "modelled_us": tm["time_us"], "modelled_us_default": tm["time_us_default"]})
     return res
 
 
-def bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush):
+def bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush, gran, budget):
     """The decode step with each retrieval head's block size and budget chosen
-    offline (per KV group, at least the default selection's attention mass at
-    the fewest bytes), against the default step timed above."""
+    offline (every head keeps at least the default selection's attention
+    mass), against the default step timed above."""
     import numpy as np
     import torch
 
     import head_heterogeneous_block_gb300 as sa
     from head_heterogeneous_block_gb300.layer import DecodeStep
 
-    with open(os.path.join(ROOT, "workloads", "demands.json")) as f:
-        prof = json.load(f)[str(w.number)]["granularity"]
     step = DecodeStep(shape, 2, kinds, w.window_tokens // w.block, device=dev,
-                      granularity=prof["gran"], head_budget=prof["budget"])
+                      granularity=gran, head_budget=budget)
     step.build_cache(t["k"], stream=stream)
     for _ in range(3):
         step(t["q"], t["k"], t["v"], stream=stream)
@@ -656,7 +667,7 @@ def bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush):
     # pooled keys: each block size a group's retrieval heads use, once
     idx = step.idx.view(w.batch, w.num_q_heads, step.kmax).cpu().numpy()
     cnt = step.cnt.view(w.batch, w.num_q_heads).cpu().numpy()
-    size = [prof["gran"][h] if kinds[h] != 1 else w.block for h in range(w.num_q_heads)]
+    size = [gran[h] if kinds[h] != 1 else w.block for h in range(w.num_q_heads)]
     G = w.group
     tokens = 0
     kbar_bytes = 0
@@ -678,8 +689,6 @@ def bench_decode_block_sizes(w, t, kinds, shape, dev, stream, flush):
             "forward_ms": round(statistics.median(fwd), 4),
             "touched_kv_bytes": tokens * w.head_dim * 2 * 2, "kbar_bytes": kbar_bytes,
             "sizes": sorted(set(size[h] for h in range(w.num_q_heads) if kinds[h] != 1)),
-            "modelled_bytes_per_sequence": prof["bytes"],
-            "modelled_bytes_per_sequence_default": prof["bytes_default"],
             "device_status": status}
 
 

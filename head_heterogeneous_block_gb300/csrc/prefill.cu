@@ -661,20 +661,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pq = 0;
     auto epilogue = [&]() -> bool {
       // exchange the partial sums (the same double buffer), then O / l for
-      // this group's columns.  o_last has exactly one phase per item, waited
-      // on every time.
+      // this group's columns.  O is read and released before the sums are
+      // collected, so the next item's first P.V does not wait for the
+      // exchange.  o_last has exactly one phase per item, waited on every time.
       float* xb = &sh->xch[xn & 1][0][0];
       xb[grp * 128 + row] = pl;
       mbar_arrive(&sh->xch_bar);
-      if (!wait_all(&sh->o_last, pq & 1, abort, p.wait_ns) || !wait_all(&sh->xch_bar, xn & 1, abort, p.wait_ns))
-        return false;
-      ++xn;
+      if (!wait_all(&sh->o_last, pq & 1, abort, p.wait_ns)) return false;
       tc_fence_after();
-      const float lt = (xb[row] + xb[128 + row]) + (xb[256 + row] + xb[384 + row]);
-      const float inv_l = 1.f / lt;
-      const bool store = row < p.B;
-      const size_t orow = size_t(pit.h) * p.S + size_t(pit.i) * p.B + size_t(row);
-      const int col = grp * C::kOCols;
       uint32_t r[C::kOCols];
       if constexpr (C::kOCols == 32) {
         tmem_ld32(lanes + o_col, r);
@@ -686,6 +680,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O is in registers: the next item's first P.V may overwrite it
       tc_fence_before();
       mbar_arrive(&sh->o_free);
+      if (!wait_all(&sh->xch_bar, xn & 1, abort, p.wait_ns)) return false;
+      ++xn;
+      const float lt = (xb[row] + xb[128 + row]) + (xb[256 + row] + xb[384 + row]);
+      const float inv_l = 1.f / lt;
+      const bool store = row < p.B;
+      const size_t orow = size_t(pit.h) * p.S + size_t(pit.i) * p.B + size_t(row);
+      const int col = grp * C::kOCols;
       // the range the tensor-core pass keeps: every weight below 2^100 (so
       // neither P nor l can overflow) and O finite; beyond it the row's
       // columns are recomputed exactly

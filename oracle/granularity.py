@@ -27,6 +27,11 @@ Readings taken here (the pages give no formula):
 * For each KV group the heads' sizes are chosen together over all
   combinations of the candidate sizes; ties go to the first combination in
   lexicographic order of the candidates (finer sizes, lower heads first).
+* choose_granularity_time charges time instead of bytes: the attention's
+  K/V bytes and the scoring's pooled bytes at their measured rates, a fixed
+  time per scoring pass (one per block size in use), and the selection
+  kernel's time for the longest row (its candidate count).  The rates are
+  inputs, measured on the device the plan is for.
 """
 from __future__ import annotations
 
@@ -136,6 +141,109 @@ def choose_granularity(masses, kinds, group: int, g0: int, k0: int, candidates, 
             kept[h] = kept_mass(masses[h][g], need[h, g])
     return {"gran": gran, "budget": budget, "target": target, "kept": kept,
             "bytes": total, "bytes_default": default}
+
+
+def select_time(rates: dict, candidates: int) -> float:
+    """Modelled time of the selection kernel when its longest row has
+    ``candidates`` blocks: the first bin of rates["select_s"] (pairs of (max
+    candidates, seconds), ascending) that holds it."""
+    for top, sec in rates["select_s"]:
+        if candidates <= top:
+            return sec
+    return rates["select_s"][-1][1]
+
+
+def step_time(assign: dict, need: dict, kinds, group: int, g0: int, L: int, d: int,
+              batch: int, rates: dict) -> float:
+    """Modelled decode-step time (seconds) of the retrieval heads' choice
+    assign[h] = g with need[h, g] blocks each, for ``batch`` sequences:
+
+      sum over heads of batch * kv_bytes / rates["attn_bps"]
+      + per block size in use: rates["score_pass_s"] + batch * (pooled bytes
+        of the groups that use it) / rates["score_bps"]   (one scoring pass
+        per size, a group reading each size's cache once)
+      + select_time(the longest row: L / the smallest size in use, streaming
+        rows counting L / g0)
+
+    The three kernels run one after another; the terms are their times."""
+    Hq = len(kinds)
+    t = 0.0
+    for h, g in assign.items():
+        t += batch * kv_bytes(need[h, g], g, d) / rates["attn_bps"]
+    used = {}
+    for grp in range(Hq // group):
+        for g in {assign[h] for h in range(grp * group, (grp + 1) * group) if h in assign}:
+            used[g] = used.get(g, 0) + 1
+    for g, ngroups in used.items():
+        t += rates["score_pass_s"] + batch * ngroups * pooled_bytes(L, g, d) / rates["score_bps"]
+    rows = [L // g for g in used]
+    if any(kinds[h] == STREAMING for h in range(Hq)):
+        rows.append(L // g0)
+    t += select_time(rates, max(rows) if rows else 0)
+    return t
+
+
+def choose_granularity_time(masses, kinds, group: int, g0: int, k0: int, candidates, L: int,
+                            d: int, batch: int, rates: dict):
+    """Per-head (g_h, k_h) for the retrieval heads minimising step_time
+    instead of bytes; the error bound (each head keeps at least the default
+    selection's mass) and the budget for a size (the fewest blocks reaching
+    it) are those of choose_granularity.
+
+    The scoring passes and the selection kernel are shared by every group,
+    so the choice is global.  For each set U of sizes allowed (every
+    non-empty subset of the candidates, in ascending order of the sorted
+    tuple), each group takes, among the combinations of sizes in U in
+    lexicographic order, the first that minimises its own K/V time plus its
+    pooled-key time; the assignment is then timed with the passes and the
+    selection of the sizes it actually uses, and the best U wins (ties: the
+    first).  This is the global minimum: at the optimum's own set of sizes
+    every group does at least as well, and fewer sizes cost no more.
+    Returns the dict of choose_granularity, with ``time_s`` and
+    ``time_s_default`` in place of the byte totals' role."""
+    Hq = len(kinds)
+    heads_of = []
+    need = {}
+    target = [0.0] * Hq
+    for grp in range(Hq // group):
+        heads = [h for h in range(grp * group, (grp + 1) * group) if kinds[h] != STREAMING]
+        heads_of.append(heads)
+        for h in heads:
+            target[h] = kept_mass(masses[h][g0], k0)
+            for g in set(candidates) | {g0}:
+                need[h, g] = blocks_for_mass(masses[h][g], target[h] * (1.0 - REL_TOL))
+    cands = list(candidates)
+    best = None
+    for r in range(1, len(cands) + 1):
+        for U in itertools.combinations(sorted(cands), r):
+            assign = {}
+            for heads in heads_of:
+                if not heads:
+                    continue
+                pick = None
+                for combo in itertools.product(U, repeat=len(heads)):
+                    c = sum(batch * kv_bytes(need[h, g], g, d) / rates["attn_bps"]
+                            for h, g in zip(heads, combo))
+                    c += sum(batch * pooled_bytes(L, g, d) / rates["score_bps"]
+                             for g in set(combo))
+                    if pick is None or c < pick[0]:
+                        pick = (c, combo)
+                for h, g in zip(heads, pick[1]):
+                    assign[h] = g
+            t = step_time(assign, need, kinds, group, g0, L, d, batch, rates)
+            if best is None or t < best[0]:
+                best = (t, assign)
+    default = {h: g0 for heads in heads_of for h in heads}
+    gran = [g0] * Hq
+    budget = [0] * Hq
+    kept = [0.0] * Hq
+    for h, g in best[1].items():
+        gran[h] = g
+        budget[h] = need[h, g]
+        kept[h] = kept_mass(masses[h][g], need[h, g])
+    return {"gran": gran, "budget": budget, "target": target, "kept": kept,
+            "time_s": best[0],
+            "time_s_default": step_time(default, need, kinds, group, g0, L, d, batch, rates)}
 
 
 def pool_cache(k: np.ndarray, g: int) -> np.ndarray:

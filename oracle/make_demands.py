@@ -104,6 +104,14 @@ def profile_output_aware(number: int, pool) -> dict:
 
 GRANULARITIES = (16, 32, 64, 128)   # candidate block sizes of a retrieval head
 
+# Rates of the decode kernels on a GB300 at the 16 x 64K shape, from the
+# bench's decode block: attention moves 320 MB of K/V in 60 us; one scoring
+# pass takes 17-19 us for 67 MB of pooled keys and two passes 35.5 us for
+# 117 MB, which a fixed 12 us per pass plus 11 TB/s reproduces; selection
+# takes 12.3 us when rows have up to 2048 candidates and 16.4 us up to 4096.
+DECODE_RATES = {"attn_bps": 5.3e12, "score_bps": 11.0e12, "score_pass_s": 12.0e-6,
+                "select_s": [[2048, 12.3e-6], [4096, 16.4e-6]]}
+
 
 def profile_granularity(number: int) -> dict:
     w = WORKLOADS[number]
@@ -117,6 +125,8 @@ def profile_granularity(number: int) -> dict:
               for h in range(w.num_q_heads) if kinds[h] != granularity.STREAMING}
     res = granularity.choose_granularity(masses, kinds, w.group, g0, k0, GRANULARITIES,
                                          w.seq_len, w.head_dim)
+    rt = granularity.choose_granularity_time(masses, kinds, w.group, g0, k0, GRANULARITIES,
+                                             w.seq_len, w.head_dim, w.batch, DECODE_RATES)
     return {
         "workload": w.name,
         "source": (f"decode query of a calibration draw (seed {w.calib_seed}, one sequence, "
@@ -128,6 +138,17 @@ def profile_granularity(number: int) -> dict:
         "target": [round(float(t), 12) for t in res["target"]],
         "kept": [round(float(t), 12) for t in res["kept"]],
         "bytes": res["bytes"], "bytes_default": res["bytes_default"],
+        "time_model": {
+            "rates": DECODE_RATES, "batch": w.batch,
+            "gran": rt["gran"], "budget": rt["budget"],
+            "time_us": round(rt["time_s"] * 1e6, 6),
+            "time_us_default": round(rt["time_s_default"] * 1e6, 6),
+            "time_us_of_byte_choice": round(granularity.step_time(
+                {h: res["gran"][h] for h in range(w.num_q_heads) if kinds[h] != granularity.STREAMING},
+                {(h, g): res["budget"][h] for h in range(w.num_q_heads)
+                 for g in [res["gran"][h]] if kinds[h] != granularity.STREAMING},
+                kinds, w.group, g0, w.seq_len, w.head_dim, w.batch, DECODE_RATES) * 1e6, 6),
+        },
     }
 
 

@@ -181,9 +181,11 @@ def test_decode_per_head_block_sizes(env, L, Bt, window, sizes):
         _check_sized(w, x, r, kinds, gran, budget, window, bf16_out=out_dtype == "bfloat16")
 
 
-def test_decode_per_head_block_sizes_full_size(env):
-    # the 64K decode workload with the block sizes and budgets chosen offline
-    # (rows of up to 4096 blocks)
+@pytest.mark.parametrize("choice", ["bytes", "time_model"])
+def test_decode_per_head_block_sizes_full_size(env, choice):
+    # the 64K decode workload with the block sizes and budgets chosen offline,
+    # by the byte model (two sizes) or the time model (one size, every
+    # retrieval head at 16 tokens); rows of up to 4096 blocks
     import json
     import os
     sa, torch = env
@@ -192,6 +194,8 @@ def test_decode_per_head_block_sizes_full_size(env):
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     with open(os.path.join(root, "workloads", "demands.json")) as f:
         prof = json.load(f)["5"]["granularity"]
+    if choice == "time_model":
+        prof = prof["time_model"]
     x = generate.decode_inputs(w)
     kinds = generate.head_kinds(w)
     window = w.window_tokens // w.block

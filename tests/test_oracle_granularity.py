@@ -156,6 +156,67 @@ def test_selector_reaches_the_group_optimum(seed):
     assert res["budget"][1] == 0 or kinds[1] == 0
 
 
+RATES0 = {"attn_bps": 1.0, "score_bps": 1.0, "score_pass_s": 0.0, "select_s": [[10 ** 9, 0.0]]}
+
+
+def _tiny(seed, kinds=None):
+    r = np.random.default_rng(300 + seed)
+    L, d, Hq, group = 64, 4, 4, 2
+    cands = (8, 16, 32)
+    kinds = kinds or [0, int(r.integers(0, 2)), 0, 0]
+    q = r.standard_normal((Hq, d)) * r.uniform(0.5, 4.0, (Hq, 1))
+    k = r.standard_normal((Hq // group, L, d))
+    masses = {h: {g: G.decode_block_mass(q[h], k[h // group], g) for g in cands}
+              for h in range(Hq) if kinds[h] != 1}
+    return L, d, Hq, group, cands, kinds, masses
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_time_selector_with_free_passes_and_selection_is_the_byte_selector(seed):
+    # no fixed costs and one rate for every byte: the modelled time is the
+    # byte count, and per-group choices are independent
+    L, d, Hq, group, cands, kinds, masses = _tiny(seed)
+    rb = G.choose_granularity(masses, kinds, group, 16, 2, cands, L, d)
+    rt = G.choose_granularity_time(masses, kinds, group, 16, 2, cands, L, d, 1, RATES0)
+    assert rt["time_s"] == pytest.approx(rb["bytes"], rel=1e-12)
+    assert rt["time_s_default"] == pytest.approx(rb["bytes_default"], rel=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_time_selector_reaches_the_global_optimum(seed):
+    # every assignment of sizes to every retrieval head, across groups
+    L, d, Hq, group, cands, kinds, masses = _tiny(seed)
+    rates = {"attn_bps": 3.0, "score_bps": 7.0, "score_pass_s": 40.0 + 30.0 * seed,
+             "select_s": [[2, 5.0], [4, 90.0], [8, 400.0]]}
+    res = G.choose_granularity_time(masses, kinds, group, 16, 2, cands, L, d, 2, rates)
+    heads = [h for h in range(Hq) if kinds[h] != 1]
+    need = {}
+    for h in heads:
+        target = G.kept_mass(masses[h][16], 2)
+        for g in cands:
+            need[h, g] = G.blocks_for_mass(masses[h][g], target * (1 - G.REL_TOL))
+    best = min(G.step_time(dict(zip(heads, combo)), need, kinds, group, 16, L, d, 2, rates)
+               for combo in itertools.product(cands, repeat=len(heads)))
+    assert res["time_s"] == pytest.approx(best, rel=1e-12)
+    for h in heads:
+        assert res["kept"][h] >= res["target"][h] * (1 - 1e-12)
+    assert res["time_s"] <= res["time_s_default"] * (1 + 1e-12)
+
+
+def test_step_time_hand_example():
+    # one group of two retrieval heads, L 64, d 4, batch 3, no streaming head:
+    # head 0 at 8 tokens keeps 5 blocks, head 1 at 16 keeps 2.
+    #   K/V: 3 * (5*8*4*4 + 2*16*4*4) = 3 * (640 + 512) = 3456 bytes at 2/s
+    #   scoring: sizes 8 and 16, one group each: 2 passes of 10 s, plus
+    #            3 * ((64/8)*4*4 + (64/16)*4*4) = 3 * (128 + 64) = 576 bytes at 4/s
+    #   selection: the longest row has 64/8 = 8 candidates -> the [8, 7] bin
+    kinds = [0, 0]
+    rates = {"attn_bps": 2.0, "score_bps": 4.0, "score_pass_s": 10.0,
+             "select_s": [[4, 1.0], [8, 7.0], [16, 50.0]]}
+    t = G.step_time({0: 8, 1: 16}, {(0, 8): 5, (1, 16): 2}, kinds, 2, 16, 64, 4, 3, rates)
+    assert t == pytest.approx(3456 / 2 + 20 + 576 / 4 + 7)
+
+
 def test_stored_decode_granularity_matches_the_oracle():
     from oracle import make_demands
     with open(os.path.join(ROOT, "workloads", "demands.json")) as f:
@@ -163,4 +224,7 @@ def test_stored_decode_granularity_matches_the_oracle():
     again = make_demands.profile_granularity(5)
     for key in ("gran", "budget", "bytes", "bytes_default", "candidates", "g0", "k0"):
         assert stored[key] == again[key], key
+    for key in ("gran", "budget", "rates", "batch"):
+        assert stored["time_model"][key] == again["time_model"][key], key
+    assert stored["time_model"]["time_us"] == pytest.approx(again["time_model"]["time_us"])
     np.testing.assert_allclose(stored["kept"], again["kept"], rtol=1e-9)
