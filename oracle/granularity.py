@@ -143,6 +143,19 @@ def choose_granularity(masses, kinds, group: int, g0: int, k0: int, candidates, 
             "bytes": total, "bytes_default": default}
 
 
+def attn_rate(rates: dict, g: int) -> float:
+    """Attention's K/V bytes per second at block size g: rates["attn_bps"] is
+    one rate, or pairs (size, rate) ascending, the first with size >= g
+    applying (the last beyond them)."""
+    r = rates["attn_bps"]
+    if isinstance(r, (int, float)):
+        return float(r)
+    for size, bps in r:
+        if g <= size:
+            return bps
+    return r[-1][1]
+
+
 def select_time(rates: dict, candidates: int) -> float:
     """Modelled time of the selection kernel when its longest row has
     ``candidates`` blocks: the first bin of rates["select_s"] (pairs of (max
@@ -158,7 +171,7 @@ def step_time(assign: dict, need: dict, kinds, group: int, g0: int, L: int, d: i
     """Modelled decode-step time (seconds) of the retrieval heads' choice
     assign[h] = g with need[h, g] blocks each, for ``batch`` sequences:
 
-      sum over heads of batch * kv_bytes / rates["attn_bps"]
+      sum over heads of batch * kv_bytes / attn_rate(rates, g_h)
       + per block size in use: rates["score_pass_s"] + batch * (pooled bytes
         of the groups that use it) / rates["score_bps"]   (one scoring pass
         per size, a group reading each size's cache once)
@@ -169,7 +182,7 @@ def step_time(assign: dict, need: dict, kinds, group: int, g0: int, L: int, d: i
     Hq = len(kinds)
     t = 0.0
     for h, g in assign.items():
-        t += batch * kv_bytes(need[h, g], g, d) / rates["attn_bps"]
+        t += batch * kv_bytes(need[h, g], g, d) / attn_rate(rates, g)
     used = {}
     for grp in range(Hq // group):
         for g in {assign[h] for h in range(grp * group, (grp + 1) * group) if h in assign}:
@@ -222,7 +235,7 @@ def choose_granularity_time(masses, kinds, group: int, g0: int, k0: int, candida
                     continue
                 pick = None
                 for combo in itertools.product(U, repeat=len(heads)):
-                    c = sum(batch * kv_bytes(need[h, g], g, d) / rates["attn_bps"]
+                    c = sum(batch * kv_bytes(need[h, g], g, d) / attn_rate(rates, g)
                             for h, g in zip(heads, combo))
                     c += sum(batch * pooled_bytes(L, g, d) / rates["score_bps"]
                              for g in set(combo))

@@ -105,12 +105,13 @@ def profile_output_aware(number: int, pool) -> dict:
 GRANULARITIES = (16, 32, 64, 128)   # candidate block sizes of a retrieval head
 
 # Rates of the decode kernels on a GB300 at the 16 x 64K shape, from the
-# bench's decode block: attention moves 320 MB of K/V in 60 us; one scoring
-# pass takes 17-19 us for 67 MB of pooled keys and two passes 35.5 us for
-# 117 MB, which a fixed 12 us per pass plus 11 TB/s reproduces; selection
-# takes 12.3 us when rows have up to 2048 candidates and 16.4 us up to 4096.
-DECODE_RATES = {"attn_bps": 5.3e12, "score_bps": 11.0e12, "score_pass_s": 12.0e-6,
-                "select_s": [[2048, 12.3e-6], [4096, 16.4e-6]]}
+# bench's decode block.  Attention: 320 MB of K/V at 32-token blocks in
+# 60 us (5.3 TB/s); 248-257 MB at 16-token blocks in 51-53 us (4.85 TB/s,
+# the selected pieces being half as long).  One scoring pass: 67 MB of
+# pooled keys in 18 us and 134 MB in 31.4 us, i.e. 4.6 us plus 5.0 TB/s.
+# Selection: 12.3 us when rows have up to 2048 candidates, 16.4 us up to 4096.
+DECODE_RATES = {"attn_bps": [[16, 4.85e12], [32, 5.3e12]], "score_bps": 5.0e12,
+                "score_pass_s": 4.6e-6, "select_s": [[2048, 12.3e-6], [4096, 16.4e-6]]}
 
 
 def profile_granularity(number: int) -> dict:

@@ -215,6 +215,10 @@ def test_step_time_hand_example():
              "select_s": [[4, 1.0], [8, 7.0], [16, 50.0]]}
     t = G.step_time({0: 8, 1: 16}, {(0, 8): 5, (1, 16): 2}, kinds, 2, 16, 64, 4, 3, rates)
     assert t == pytest.approx(3456 / 2 + 20 + 576 / 4 + 7)
+    # per-size attention rates: 8-token pieces at 1/s, 16-token ones at 4/s
+    rates["attn_bps"] = [[8, 1.0], [16, 4.0]]
+    t = G.step_time({0: 8, 1: 16}, {(0, 8): 5, (1, 16): 2}, kinds, 2, 16, 64, 4, 3, rates)
+    assert t == pytest.approx(3 * 640 / 1 + 3 * 512 / 4 + 20 + 576 / 4 + 7)
 
 
 def test_stored_decode_granularity_matches_the_oracle():
