@@ -27,7 +27,7 @@
 //               weights above 1; m cancels in O / l, so there is no per-block
 //               exchange and no rescale of O.  The normaliser sums the same
 //               bf16-rounded weights that enter P V.  A row whose normaliser
-//               passes 2^100, or whose O is not finite, is marked and, after
+//               passes 2^126, or whose O is not finite, is marked and, after
 //               the worker's last item, recomputed exactly in fp32 on the CUDA
 //               cores.  Epilogue (after the next item's first block): O / l
 //               and the log-sum-exp; fp32 output is stored directly, bf16
@@ -687,13 +687,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool store = row < p.B;
       const size_t orow = size_t(pit.h) * p.S + size_t(pit.i) * p.B + size_t(row);
       const int col = grp * C::kOCols;
-      // the range the tensor-core pass keeps: every weight below 2^100 (so
-      // neither P nor l can overflow) and O finite; beyond it the row's
+      // the range the tensor-core pass keeps: the sum below 2^126 (so
+      // neither P nor l overflows) and O finite; beyond it the row's
       // columns are recomputed exactly
       float osum = 0.f;
 #pragma unroll
       for (int x = 0; x < C::kOCols; ++x) osum += __uint_as_float(r[x]);
-      const bool in_range = lt <= 0x1p100f && fabsf(osum) <= 3.0e38f;
+      const bool in_range = lt <= 0x1p126f && fabsf(osum) <= 3.0e38f;
       if (store && !in_range) {
         // the whole item is recomputed after the list (the bit is set by
         // every thread that finds a row out of range; one is enough)

@@ -29,7 +29,7 @@
 //               tile's first block of an item sets that tile's reference row
 //               maximum (exchanged once between the groups); later blocks use
 //               it as is: weights above 1 stay exact and the reference cancels
-//               in O / l.  A row whose sum leaves the range (2^100, or O not
+//               in O / l.  A row whose sum leaves the range (2^126, or O not
 //               finite) is recomputed exactly after the list.  Epilogue: O / l
 //               for both heads, in fp32 by direct stores or in bf16 through
 //               the finished item's Q stages and a TMA store.
@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float osum = 0.f;
 #pragma unroll
         for (int e = 0; e < C::kOCols; ++e) osum += __uint_as_float(r[e]);
-        const bool in_range = lt[x] <= 0x1p100f && fabsf(osum) <= 3.0e38f;
+        const bool in_range = lt[x] <= 0x1p126f && fabsf(osum) <= 3.0e38f;
         if (store && !in_range) {
           if (pit.pos < 32 * kRedoWords)
             atomicOr(&sh->redo[pit.pos >> 5], 1u << (pit.pos & 31));
