@@ -650,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = p.scale_log2;
     const uint32_t o_col = C::kO + grp * C::kOCols;
     uint32_t kb = 0, qi = 0, xn = 0;   // xn: uses of the exchange buffer so far
+    uint32_t sst = 0, sph = 0;         // S ring stage and phase of block kb
     bool ok = true;
     // The epilogue of an item (O / l out to memory, O released) runs after the
     // next item's first block: by then that item's last P.V has finished, so
@@ -756,10 +757,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->info_empty[slot]);
       if (it.n == 0) break;
-      float m_used = -INFINITY, l = 0.f;
+      float m_used = -INFINITY;
+      // the item's normaliser, in four partial sums combined at its end
+      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
       for (int t = 0; t < it.n; ++t) {
-        const int sb = kb % C::kNS;
-        if (!wait_all(&sh->s_full[sb], (kb / C::kNS) & 1, abort, p.wait_ns)) {
+        const int sb = int(sst);
+        if (!wait_all(&sh->s_full[sb], sph, abort, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -814,7 +817,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // reference cancels in O / l, and no group has to wait for another.
         // A row whose sum leaves the range checked at the end of the item is
         // recomputed exactly.
-        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
         {
           uint32_t pk[C::kCols / 2];
           const float nm = -m_used;
@@ -825,11 +827,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[x] = pack_bf16x2(ex2(a0), ex2(a1));
             // the normaliser sums the rounded values
             if (x & 1)
-              add2(sum2, sum3, __uint_as_float(pk[x] << 16),
-                   __uint_as_float(pk[x] & 0xFFFF0000u));
+              add_bf16x2(sum2, sum3, pk[x]);
             else
-              add2(sum0, sum1, __uint_as_float(pk[x] << 16),
-                   __uint_as_float(pk[x] & 0xFFFF0000u));
+              add_bf16x2(sum0, sum1, pk[x]);
           }
           if constexpr (C::kCols == 32) {
             tmem_st16(lanes + scol, pk);
@@ -838,10 +838,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tmem_st_wait();
-        l += (sum0 + sum1) + (sum2 + sum3);
         tc_fence_before();
         mbar_arrive(&sh->p_full[sb]);
         ++kb;
+        if (++sst == uint32_t(C::kNS)) {
+          sst = 0;
+          sph ^= 1u;
+        }
         if (t == 0 && pend) {
           if (!epilogue()) {
             ok = false;
@@ -853,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       pend = true;
       pit = it;
-      pl = l;
+      pl = (sum0 + sum1) + (sum2 + sum3);
       pm = m_used;
       pq = qi;
       ++qi;

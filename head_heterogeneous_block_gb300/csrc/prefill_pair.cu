@@ -724,11 +724,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               fma2(a0, a1, s[2 * e], s[2 * e + 1], c, c, nm, nm);
               pk[e] = pack_bf16x2(ex2(a0), ex2(a1));
               if (e & 1)
-                add2(sum2, sum3, __uint_as_float(pk[e] << 16),
-                     __uint_as_float(pk[e] & 0xFFFF0000u));
+                add_bf16x2(sum2, sum3, pk[e]);
               else
-                add2(sum0, sum1, __uint_as_float(pk[e] << 16),
-                     __uint_as_float(pk[e] & 0xFFFF0000u));
+                add_bf16x2(sum0, sum1, pk[e]);
             }
             if constexpr (C::kCols == 32) {
               tmem_st16(lanes + scol, pk);

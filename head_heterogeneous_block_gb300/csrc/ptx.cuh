@@ -395,6 +395,15 @@ __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
       : "f"(a0), "f"(a1));
 }
 
+// s0 += low bf16 of pk, s1 += high bf16 of pk (each converted exactly, the
+// sum rounded to nearest in fp32)
+__device__ __forceinline__ void add_bf16x2(float& s0, float& s1, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(pk));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half
