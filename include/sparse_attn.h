@@ -91,7 +91,7 @@ enum {
   SA_DEV_BAD_LAUNCH = 16,    /* the kernel found its shared memory misaligned
                                 and did nothing; outputs are not written     */
   SA_DEV_RANGE = 32          /* rows beyond the tensor-core pass's range
-                                (weights above 2^100 or O overflowed) could
+                                (a row sum above 2^126 or O overflowed) could
                                 not all be recomputed exactly: a worker list
                                 longer than 32768 items; outputs invalid     */
 };
