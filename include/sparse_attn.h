@@ -383,10 +383,11 @@ sa_status sparse_attn_forward_kind(const sa_shape* shp, const sa_plan* plan,
                                    sa_stream_t stream);
 
 /*
- * Watchdog limit of the prefill forward kernel: every wait of one role on
- * another (a copy landing, a tensor-core result, a softmax step) gives up
- * after `ns` nanoseconds of GPU global time, for launches made after this
- * call by any thread of the process.  0 restores the default, 4 s.
+ * Watchdog limit of the forward kernels: every wait of one role on another
+ * in the prefill kernel (a copy landing, a tensor-core result, a softmax
+ * step), and every wait for a copy in the decode kernel, gives up after `ns`
+ * nanoseconds of GPU global time, for launches made after this call by any
+ * thread of the process.  0 restores the default, 4 s.
  * A CTA whose wait runs out ORs SA_DEV_TIMEOUT into dev_status, stops every
  * role of the CTA, lets the copies and tensor-core operations it already
  * issued complete (those waits keep the 4 s limit), frees its tensor memory
