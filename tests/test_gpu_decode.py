@@ -331,3 +331,48 @@ def test_decode_overlapped_step_replays_from_a_cuda_graph(env):
         torch.cuda.synchronize()
         assert torch.equal(step.out, want) and torch.equal(step.idx, want_idx)
     assert int(step.dev_status.item()) == 0
+
+
+def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
+    """The decode forward's waits for its copies, limited to 100 ns (far
+    below a copy's latency from memory), run out: the launch reports
+    SA_DEV_TIMEOUT and returns, each warp having waited (with the full limit)
+    for the copies it issued, so a normal launch right after gives the
+    previous output exactly."""
+    sa, torch = env
+    from head_heterogeneous_block_gb300.layer import DecodeStep
+    from tests._parity import to_dev
+    from workloads import generate, scaled, workload
+    w = scaled(workload(5), 8192, batch=4)
+    x = generate.decode_inputs(w)
+    kinds = generate.head_kinds(w)
+    shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                            w.batch)
+    t = {n: to_dev(x[n]) for n in "qkv"}
+    step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
+                      out_dtype=torch.float32, overlap=False)
+    step.build_cache(t["k"])
+    want = step(t["q"], t["k"], t["v"]).clone()
+    torch.cuda.synchronize()
+    assert int(step.dev_status.item()) == 0
+
+    def forward():
+        sa.sparse_attn_forward(shape, step.plan, t["q"], t["k"], t["v"], step.idx, step.cnt,
+                               step.kmax, step.out, None, step.dev_status)
+        torch.cuda.synchronize()
+        return int(step.dev_status.item())
+
+    try:
+        sa.sparse_attn_set_wait_limit(100)
+        step.dev_status.zero_()
+        step.out.fill_(float("nan"))
+        st = forward()
+    finally:
+        sa.sparse_attn_set_wait_limit(0)
+    assert st & sa.SA_DEV_TIMEOUT, st
+    assert not st & (sa.SA_DEV_BAD_INDEX | sa.SA_DEV_BAD_COUNT)
+    for _ in range(2):
+        step.dev_status.zero_()
+        step.out.fill_(float("nan"))
+        assert forward() == 0
+        assert torch.equal(step.out, want)
