@@ -334,8 +334,8 @@ def test_decode_overlapped_step_replays_from_a_cuda_graph(env):
 
 
 def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
-    """The decode forward's waits for its copies, limited to 100 ns (far
-    below a copy's latency from memory), run out: the launch reports
+    """The decode forward's waits for its copies, limited to 1 ns (far below
+    a copy's latency from memory, with L2 flushed first), run out: the launch reports
     SA_DEV_TIMEOUT and returns, each warp having waited (with the full limit)
     for the copies it issued, so a normal launch right after gives the
     previous output exactly."""
@@ -343,7 +343,7 @@ def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
     from head_heterogeneous_block_gb300.layer import DecodeStep
     from tests._parity import to_dev
     from workloads import generate, scaled, workload
-    w = scaled(workload(5), 8192, batch=4)
+    w = workload(5)
     x = generate.decode_inputs(w)
     kinds = generate.head_kinds(w)
     shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
@@ -351,6 +351,7 @@ def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
     t = {n: to_dev(x[n]) for n in "qkv"}
     step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
                       out_dtype=torch.float32, overlap=False)
+    flush = torch.zeros(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     step.build_cache(t["k"])
     want = step(t["q"], t["k"], t["v"]).clone()
     torch.cuda.synchronize()
@@ -363,9 +364,10 @@ def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
         return int(step.dev_status.item())
 
     try:
-        sa.sparse_attn_set_wait_limit(100)
+        sa.sparse_attn_set_wait_limit(1)
         step.dev_status.zero_()
         step.out.fill_(float("nan"))
+        flush.max()                    # the copies come from memory, not L2
         st = forward()
     finally:
         sa.sparse_attn_set_wait_limit(0)
