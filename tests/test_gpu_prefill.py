@@ -332,7 +332,8 @@ def test_prefill_group_shared_dense_pairs_equal_causal_attention(env):
 def test_prefill_group_shared_full_size(env):
     """The 128K Llama-3.1-8B workload with one list per KV group, in the
     bench's launch configuration; selection checked on every row, attention on
-    sampled items (fp32 output at the plain tolerance, then bf16 output)."""
+    sampled items (fp32 output at the plain tolerance, then bf16 output, then
+    fp32 output from head pairs on one K/V load)."""
     sa, torch = env
     from tests import _parity as P
     from workloads import generate, workload
@@ -340,12 +341,13 @@ def test_prefill_group_shared_full_size(env):
     prof = json.load(open(os.path.join(ROOT, "workloads", "demands.json")))["3"]
     x = generate.prefill_inputs(w)
     W = torch.cuda.get_device_properties(0).multi_processor_count
-    for out_dtype, per_head in (("float32", 32), ("bfloat16", 8)):
+    for out_dtype, per_head, pairs in (("float32", 32, False), ("bfloat16", 8, False),
+                                       ("float32", 8, True)):
         r = _run(sa, torch, w, x, {"k_uniform": prof["k_uniform"], "demand": prof["demand"],
-                                   "group_shared": True},
+                                   "group_shared": True, "share_kv": pairs},
                  schedule="lpt_grouped", workers=W, out_dtype=out_dtype)
         assert r["status"] == 0
-        if out_dtype == "float32":
+        if out_dtype == "float32" and not pairs:
             _check_group_shared(r, x, w, prof["k_uniform"], prof["demand"])
         items = P.sample_items(r["budgets"], w.nb, per_head, seed=33)
         P.check_attention(r["out"], r["lse"], x, r["idx"], r["cnt"], w.block, items, w.group,
