@@ -137,8 +137,8 @@ def job_value(flops_per_replica_step: float, world: int, steps: int, total_ms: f
 # summarised in profiles/prefill_attention_llama8b_128k.md.  It describes only
 # the kernel source with this SHA-256; for any other source it is not reported.
 FORWARD_TRAFFIC = {"workload": 3,
-                   "sha256": "8ce72b0c456159c468cee56ba8f818d4973a05e5bb0896162582e1b8e205d0a7",
-                   "bytes": 2533682176 + 1076779520}
+                   "sha256": "3d2f4f2810b160e3f70b0bc8ccf5f13a3eddbb334167b009cac61bf42a4253ba",
+                   "bytes": 2536118784 + 1076756992}
 
 
 def _forward_traffic(workload_number: int):

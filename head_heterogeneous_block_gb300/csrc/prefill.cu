@@ -73,7 +73,6 @@ struct Cfg {
   static constexpr uint32_t kO = kNS * BK;        // TMEM column of O
   static constexpr uint32_t kTmemCols = (kNS * BK + D <= 256) ? 256 : 512;
   static constexpr int kData = kNQ * kQBytes + kNK * kKVBytes + kNV * kKVBytes;
-  static constexpr int kPrefetch = 0;             // blocks ahead prefetched into L2 (0: off)
   static_assert(kNS * BK + D <= 512, "tensor memory budget");
   static_assert(kCols == 16 || kCols == 32, "group width");
   static_assert(kOCols == 16 || kOCols == 32, "group width");
@@ -305,14 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t jl = (lane < n) ? list[lane] : 0;
       const int32_t jlast = list[n - 1];
       const int g = h / p.G;
-      // L2 prefetch of the first blocks (later ones are prefetched ahead below)
-      if (C::kPrefetch > 0 && lane < min(n, C::kPrefetch)) {
-        const int32_t jp = clamp_block(jl, i);
-        for (int s = 0; s < C::kPanels; ++s) {
-          tma_prefetch_2d(&tk, s * 64, g * p.S + jp * BK);
-          tma_prefetch_2d(&tv, s * 64, g * p.S + jp * BK);
-        }
-      }
       if (lane == 0) {
         // publish the item's metadata for the MMA, V-producer and softmax warps
         const int slot = qi % kNI;
@@ -343,22 +334,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < n; ++t) {
         if ((t & 31) == 0 && t > 0) jl = (t + lane < n) ? list[t + lane] : 0;
         const int32_t jraw = __shfl_sync(0xffffffffu, jl, t & 31);
-        // block kPrefetch positions ahead, into L2
-        const int tp = t + C::kPrefetch;
-        const int32_t jp = __shfl_sync(0xffffffffu, jl, tp & 31);
         if (jraw < 0 || jraw > i || jraw <= jprev) {   // out of range or not ascending
           if (lane == 0) atomicOr(p.dev_status, SA_DEV_BAD_INDEX);
         }
         const int32_t j = clamp_block(jraw, i);
         jprev = jraw;
         if (lane == 0) {
-          if (C::kPrefetch > 0 && tp < n && (tp & ~31) == (t & ~31)) {
-            const int32_t jq = clamp_block(jp, i);
-            for (int s = 0; s < C::kPanels; ++s) {
-              tma_prefetch_2d(&tk, s * 64, g * p.S + jq * BK);
-              tma_prefetch_2d(&tv, s * 64, g * p.S + jq * BK);
-            }
-          }
           const int ks = kiss % C::kNK;
           if (kiss >= uint32_t(C::kNK) &&
               !mbar_wait(&sh->k_empty[ks], ((kiss / C::kNK) - 1) & 1, abort, p.wait_ns))
