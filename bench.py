@@ -466,10 +466,11 @@ def bench_decode(dev, stream):
     kinds = generate.head_kinds(w)
     shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
                             w.batch)
-    # the serial step (every head's score, select and attention in turn) gives
-    # the stage times; the default step (below) overlaps the streaming heads
+    # the serial step (every head's score, select and attention in turn, as
+    # separate calls) gives the stage times; the default step (below) fuses
+    # the retrieval heads' scoring and selection and overlaps the streaming heads
     step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
-                      device=dev, overlap=False)
+                      device=dev, overlap=False, fused=False)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step.build_cache(t["k"], stream=stream)
     for _ in range(3):
@@ -511,23 +512,42 @@ def bench_decode(dev, stream):
     step.build_cache(t["k"], stream=stream)
     b.record(stream)
     torch.cuda.synchronize(dev)
-    # the default step: the streaming heads on a side stream beside the
-    # retrieval heads' scoring and selection (same kernels, same results)
-    ov = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
-                    device=dev)
-    ov.build_cache(t["k"], stream=stream)
-    for _ in range(3):
-        ov(t["q"], t["k"], t["v"], stream=stream)
-    ov_times = []
-    for _ in range(10):
+    # the fused scoring and selection of the retrieval heads alone
+    fz = []
+    for _ in range(20):
         flush.max()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        ov(t["q"], t["k"], t["v"], stream=stream)
+        sa.sparse_attn_score_select(shape, step.plan, t["q"], step.kbar, None, step.idx,
+                                    step.cnt, step.kmax, stream=stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        ov_times.append(e0.elapsed_time(e1))
-    ov_status = int(ov.dev_status.item())
+        fz.append(e0.elapsed_time(e1))
+
+    def overlapped(fused):
+        # the streaming heads on a side stream beside the retrieval heads'
+        # scoring and selection (fused into one launch, or apart)
+        ov = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
+                        device=dev, fused=fused)
+        ov.build_cache(t["k"], stream=stream)
+        for _ in range(3):
+            ov(t["q"], t["k"], t["v"], stream=stream)
+        ts = []
+        for _ in range(20):
+            flush.max()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ov(t["q"], t["k"], t["v"], stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return ov, ts
+
+    ov, unfused_times = overlapped(False)
+    unfused_status = int(ov.dev_status.item())
+    del ov
+    ov, ov_times = overlapped(True)
+    ov_status = max(unfused_status, int(ov.dev_status.item()))
     # the overlapped step captured once in a CUDA graph and replayed, as a
     # serving loop runs its decode steps
     graph_ms = None
@@ -552,7 +572,7 @@ def bench_decode(dev, stream):
             e1.record(stream)
             torch.cuda.synchronize(dev)
             gr_times.append(e0.elapsed_time(e1))
-        graph_ms = round(statistics.median(gr_times), 4)
+        graph_ms = round(statistics.mean(gr_times), 4)
         del g
     except RuntimeError as exc:   # capture refused: report it, keep the eager numbers
         graph_ms = f"capture failed: {str(exc)[:80]}"
@@ -579,11 +599,15 @@ def bench_decode(dev, stream):
     # index lists pass between kernels through L2 and are not counted
     step_bytes = kbar_bytes + kv_bytes + q_o
     step_ms = statistics.median(whole)
-    ov_ms = statistics.median(ov_times)
+    # means: single launches are timed in steps of ~2 us here
+    ov_ms = statistics.mean(ov_times)
     res = {"workload": w.name,
            "ms_per_step": round(ov_ms, 4),
            "step": "DecodeStep default: streaming heads selected and attended on a side "
-                   "stream while the retrieval heads score, select and attend",
+                   "stream while the retrieval heads score and select (one fused launch) "
+                   "and attend",
+           "unfused_ms_per_step": round(statistics.mean(unfused_times), 4),
+           "score_select_ms": round(statistics.mean(fz), 4),
            "graph_ms_per_step": graph_ms,
            "step_frac_hbm": round(step_bytes / (ov_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
            "device_status": ov_status,
@@ -600,7 +624,9 @@ def bench_decode(dev, stream):
            "step_bytes": step_bytes,
            "step_floor_ms": round(step_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
            "stages": "score_ms, select_ms and forward_ms time the serial step's kernels "
-                     "between events",
+                     "between events (separate score and select calls); score_select_ms "
+                     "times the fused launch alone; ms_per_step and unfused_ms_per_step "
+                     "are means over 20 steps",
            "kcache_pool_ms": round(a.elapsed_time(b), 4),
            "l2": "flushed between steps (a 256 MB read)"}
     del step

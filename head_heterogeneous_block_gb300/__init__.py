@@ -22,6 +22,7 @@ __all__ = [
     "sparse_attn_pool_kcache", "sa_status_string", "library_path",
     "sparse_attn_select_topp", "sparse_attn_pool_kcache_plan", "sparse_attn_score_plan",
     "sparse_attn_set_wait_limit", "sparse_attn_select_kind", "sparse_attn_forward_kind",
+    "sparse_attn_score_select",
 ]
 
 SA_OK = 0
@@ -112,6 +113,8 @@ def _load():
                                                    P]),
         "sparse_attn_forward_kind": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P, P,
                                                     I32, P, I32, P, P, I32, P]),
+        "sparse_attn_score_select": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P, P,
+                                                    I32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -288,6 +291,16 @@ def sparse_attn_select_kind(shape: Shape, plan: Plan, scores, idx, cnt, kmax: in
     _check(_lib.sparse_attn_select_kind(ctypes.byref(shape), plan.handle, _ptr(scores), _ptr(idx),
                                         _ptr(cnt), kmax, int(head_kind), _stream(stream)),
            "sparse_attn_select_kind")
+
+
+def sparse_attn_score_select(shape: Shape, plan: Plan, q, kbar, scores, idx, cnt, kmax: int,
+                             stream=None):
+    """Decode: scores and selection of the retrieval heads in one launch
+    (``scores`` may be None)."""
+    _check(_lib.sparse_attn_score_select(ctypes.byref(shape), plan.handle, _ptr(q), _ptr(kbar),
+                                         _ptr(scores), _ptr(idx), _ptr(cnt), kmax,
+                                         _stream(stream)),
+           "sparse_attn_score_select")
 
 
 def sparse_attn_select_topp(shape: Shape, plan: Plan, scores, p: float, idx, cnt, kmax: int,

@@ -41,6 +41,28 @@ cudaError_t launch_decode_scores(const void* q, const float* kbar, float* scores
                                  const uint8_t* kinds = nullptr,
                                  const int32_t* gran = nullptr, int size = 0);
 
+// Decode Index and Select of the retrieval heads in one launch: one cluster
+// per (sequence, KV group) scores the group's pooled keys for its retrieval
+// heads (the scores of launch_decode_scores, bit for bit) and selects each
+// retrieval row as launch_select does.  Rows of streaming heads are left as
+// they are.  d = 128, group <= 16, nb <= 4096; rows_per_cta is set by the
+// launcher.
+struct IndexSelectArgs {
+  const void* q;            // [Bt][Hq][128] bf16
+  const float* kbar;        // [Bt][Hkv][nb][128] pooled keys
+  float* scores;            // [Bt][Hq][nb] retrieval rows written, or NULL
+  const int32_t* budgets;   // [Hq] device
+  const uint8_t* kinds;     // [Hq] device
+  int32_t* idx;             // [Bt*Hq][kmax]
+  int32_t* cnt;             // [Bt*Hq]
+  int32_t kmax;
+  int32_t Bt, Hq, Hkv, group, nb;
+  float scale;
+  int32_t max_retrieval;    // most retrieval heads in one KV group (>= 1)
+  int32_t rows_per_cta;
+};
+cudaError_t launch_decode_index_select(const IndexSelectArgs& a, cudaStream_t st);
+
 struct SelectArgs {
   const float* scores;
   const int32_t* budgets;   // [Hq] device

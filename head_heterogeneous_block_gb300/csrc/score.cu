@@ -24,6 +24,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "index.cuh"
 #include "kernels.h"
 #include "sparse_attn.h"
 
@@ -67,48 +68,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4* __restrict__ x,
   }
 }
 
-// ---------------------------------------------------------------- tf32 MMA helpers
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// 16-byte chunk c of a row of kC chunks sits at c ^ 4(r mod kC/4): the rows
-// a quarter-warp reads together land on different banks
-template <int kC>
-__device__ __forceinline__ int swz(int r, int c) { return c ^ ((r & (kC / 4 - 1)) << 2); }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-// x = hi + lo with hi a tf32 value (the 10 leading mantissa bits of x)
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = __float_as_uint(x) & 0xFFFFE000u;
-  lo = __float_as_uint(x - __uint_as_float(hi));
-}
-
-// D += A . B for one m16n8k8 tile (A 16x8 row-major, B 8x8 column-major, tf32)
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
+using namespace sa_ix;
 
 // Prefill scores on the tensor cores: one 64x64 tile of (query block i, key
 // block j), j <= i, per CTA over the lower triangle.  The tile's pooled query
@@ -203,16 +163,8 @@ __global__ void __launch_bounds__(256) prefill_scores_kernel(const float* __rest
 // three-stage shared-memory ring with cp.async while the previous chunks are
 // scored, so the loads of one chunk overlap the arithmetic of the others.
 // The scores of a chunk are a small dense product, [64 rows x 128] x
-// [128 x G heads]: warp w takes rows [16w, 16w+16) and runs it on the tensor
-// cores as m16n8k8 tf32 MMAs (rows x 8 heads per tile, fp32 accumulation).
-// A pooled key x is split into x_hi (x with its 13 low mantissa bits cleared,
-// a tf32 value) and x_lo = x - x_hi (exact in fp32; the MMA reads its top
-// tf32 bits), and both are multiplied by the query (bf16, exact in tf32) into
-// separate accumulators, so the products keep about 20 bits of x -- fp32-level
-// scores.  The k order inside an MMA is
-// permuted (lane t of a quad takes dimensions 16m + 4t .. +4, two k-steps),
-// and a row's 16-byte chunks are stored XOR-swizzled by the row, so every
-// shared-memory read is conflict-free.  D = 128.
+// [128 x G heads], on the tf32 tensor cores at fp32-level accuracy
+// (sa_ix::score_chunk).  D = 128.
 constexpr int kMaxGroup = 16;
 constexpr int kRows = 64;                     // pooled rows per chunk
 constexpr int kStages = 3;
@@ -234,7 +186,6 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   ScoreStage* st = reinterpret_cast<ScoreStage*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gq = lane >> 2, tq = lane & 3;    // MMA fragment coordinates
   const int per = (nb + kRows - 1) / kRows;   // chunks per (sequence, KV head)
   const int total = Bt * Hkv * per;
   // each group's heads this pass scores: all, or the retrieval heads of `size`
@@ -292,46 +243,12 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm)
     const int bg = cur / per, r0 = (cur - bg * per) * kRows;
     const int b = bg / Hkv, g = bg - b * Hkv;
     const uint32_t hmask = gmask[g];
-    const int ra = 16 * warp + gq;            // this lane's rows: ra and ra + 8
     if (r0 + 16 * warp < nb) {
-      for (int n0 = 0; n0 < group; n0 += 8) { // 8 heads per tile
-        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acl[4] = {0.f, 0.f, 0.f, 0.f};
-        const int hn = n0 + gq;               // the head of this lane's B column
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {         // dimensions 16m .. 16m + 16: two k-steps
-          const float4 xa = sg.k[ra][swz<32>(ra, 4 * m + tq)];
-          const float4 xb = sg.k[ra + 8][swz<32>(ra + 8, 4 * m + tq)];
-          uint2 qb = make_uint2(0u, 0u);
-          if (hn < group) qb = sg.q[hn][4 * m + tq];
-          const uint32_t q0 = qb.x << 16, q1 = qb.x & 0xFFFF0000u;
-          const uint32_t q2 = qb.y << 16, q3 = qb.y & 0xFFFF0000u;
-          uint32_t hi[4], lo[4];
-          // k-step 2m: dimensions +0 (k = t) and +1 (k = t + 4)
-          split_tf32(xa.x, hi[0], lo[0]);
-          split_tf32(xb.x, hi[1], lo[1]);
-          split_tf32(xa.y, hi[2], lo[2]);
-          split_tf32(xb.y, hi[3], lo[3]);
-          mma_tf32(acc, hi, q0, q1);
-          mma_tf32(acl, lo, q0, q1);
-          // k-step 2m + 1: dimensions +2 and +3
-          split_tf32(xa.z, hi[0], lo[0]);
-          split_tf32(xb.z, hi[1], lo[1]);
-          split_tf32(xa.w, hi[2], lo[2]);
-          split_tf32(xb.w, hi[3], lo[3]);
-          mma_tf32(acc, hi, q2, q3);
-          mma_tf32(acl, lo, q2, q3);
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += acl[e];
-        // acc: rows ra (0, 1) and ra + 8 (2, 3), heads n0 + 2t and n0 + 2t + 1
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int hh = n0 + 2 * tq + (e & 1);
-          const int j = r0 + ra + ((e & 2) ? 8 : 0);
-          if (hh < group && ((hmask >> hh) & 1u) && j < nb)
-            scores[(size_t(b) * Hq + g * group + hh) * stride + j] = acc[e] * scale;
-        }
-      }
+      score_chunk(sg.k, sg.q, group, warp, lane, [&](int hh, int r, float v) {
+        const int j = r0 + r;
+        if (((hmask >> hh) & 1u) && j < nb)
+          scores[(size_t(b) * Hq + g * group + hh) * stride + j] = v * scale;
+      });
     }
     __syncthreads();                          // stage k % kStages is free again
 #pragma unroll

@@ -9,20 +9,17 @@
 // retrieval head is the row i = nb-1; a decode streaming head keeps block 0
 // and the last window_blocks blocks ("Intuizioni Chiave" 2).
 //
-// The threshold is found by radix selection over the order-preserving bit
-// pattern of the fp32 scores: four passes, each a 256-bin shared-memory
-// histogram of the next 8 bits among the candidates that still match the
-// prefix, and a warp scan that picks the bin holding the k-th largest.  The
-// result is the exact k-th largest score T: every candidate above T is kept,
-// and of those equal to T the lowest indices are kept (ordered by a block
-// scan, only when ties straddle the threshold).  Kept blocks are marked in a
-// bitmap and written in ascending order with warp ballots.
+// The threshold is the exact k-th largest score, found by radix selection
+// over the order-preserving bit pattern of the scores (sa_topk::mark_top);
+// kept blocks are marked in a bitmap and written in ascending order with
+// warp ballots (sa_topk::emit_ascending).
 
 #include <algorithm>
 #include <cstdint>
 
 #include "kernels.h"
 #include "sparse_attn.h"
+#include "topk.cuh"
 
 namespace {
 
@@ -30,19 +27,14 @@ constexpr int kThreads = 128;
 constexpr int kPerThread = 16;            // candidates per thread: nb <= 2048
 constexpr int kMaxWords = 2048 / 32;
 
-__device__ __forceinline__ uint32_t order_bits(float s) {
-  const uint32_t u = __float_as_uint(s);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+using sa_topk::order_bits;
 
 // kT threads with kPer candidates each: rows of up to kPer * kT blocks.
 template <int kT, int kPer>
 __global__ void __launch_bounds__(kT) select_kernel(sa_k::SelectArgs a) {
   __shared__ uint32_t bits[kPer * kT / 32];
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t ctl[4];
-  __shared__ uint32_t wsum[kT / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ sa_topk::Scratch scr;
+  const int tid = threadIdx.x;
   // decode rows may be restricted to a list of heads (one kind of head)
   const int row = a.heads ? (int(blockIdx.x) / a.nh) * a.Hq + a.heads[blockIdx.x % a.nh]
                           : int(blockIdx.x);
@@ -108,128 +100,18 @@ __global__ void __launch_bounds__(kT) select_kernel(sa_k::SelectArgs a) {
             u[r] = (j <= i - 1) ? order_bits(sc) : 0u;
           }
         }
-        uint32_t prefix = 0, mask = 0, need = uint32_t(rest), eq_total = 0;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-          for (int b = tid; b < 256; b += kT) hist[b] = 0u;
-          __syncthreads();
-          if (kT > 128 && shift == 24) {
-            // the top byte (sign and high exponent bits) puts most scores in
-            // a few bins: one atomic per bin and warp instead of per lane
-#pragma unroll
-            for (int r = 0; r < kPer; ++r) {
-              const int j = 1 + tid + r * kT;
-              const uint32_t bin = j <= i - 1 ? (u[r] >> 24) : 256u;
-              const uint32_t same = __match_any_sync(0xffffffffu, bin);
-              if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
-            }
-          } else {
-#pragma unroll
-            for (int r = 0; r < kPer; ++r) {
-              const int j = 1 + tid + r * kT;
-              if (j <= i - 1 && (u[r] & mask) == prefix) atomicAdd(&hist[(u[r] >> shift) & 255u], 1u);
-            }
-          }
-          __syncthreads();
-          if (warp == 0) {
-            // lane l holds bins 255-8l .. 248-8l (descending)
-            uint32_t c[8], local = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              c[k] = hist[255 - 8 * lane - k];
-              local += c[k];
-            }
-            uint32_t incl = local;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += v;
-            }
-            const uint32_t excl = incl - local;
-            if (excl < need && need <= incl) {
-              uint32_t acc = excl;
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                if (acc + c[k] >= need) {
-                  ctl[0] = uint32_t(255 - 8 * lane - k);
-                  ctl[1] = acc;
-                  ctl[2] = c[k];
-                  break;
-                }
-                acc += c[k];
-              }
-            }
-          }
-          __syncthreads();
-          const uint32_t b = ctl[0];
-          need -= ctl[1];
-          eq_total = ctl[2];
-          prefix |= b << shift;
-          mask |= 0xFFu << shift;
-          __syncthreads();
-          // the bin holds exactly the candidates still needed: all of them,
-          // and everything above, are kept (u >= prefix, lower bits zero)
-          if (eq_total == need) break;
-        }
-        const uint32_t T = prefix;
-        if (eq_total == need) {
-          // every candidate >= T is kept
-#pragma unroll
-          for (int r = 0; r < kPer; ++r) {
-            const int j = 1 + tid + r * kT;
-            if (j <= i - 1 && u[r] >= T) atomicOr(&bits[j >> 5], 1u << (j & 31));
-          }
-        } else {
-          // ties straddle the threshold: above T all, equal to T by index
-          uint32_t taken = 0;
-          for (int r = 0; r < kPer; ++r) {
-            const int j = 1 + tid + r * kT;
-            const bool valid = j <= i - 1;
-            const bool eq = valid && u[r] == T;
-            const uint32_t m = __ballot_sync(0xffffffffu, eq);
-            if (lane == 0) wsum[warp] = __popc(m);
-            __syncthreads();
-            uint32_t before = taken;
-            for (int w = 0; w < warp; ++w) before += wsum[w];
-            before += __popc(m & ((1u << lane) - 1u));
-            if (valid && (u[r] > T || (eq && before < need)))
-              atomicOr(&bits[j >> 5], 1u << (j & 31));
-            for (int w = 0; w < kT / 32; ++w) taken += wsum[w];
-            __syncthreads();
-          }
-        }
+        sa_topk::mark_top<kT, kPer, (kT > 128)>(u, i - 1, uint32_t(rest), bits, scr, tid, 0);
       }
     }
   }
   __syncthreads();
 
-  // Emit ascending block indices, then pad with -1, into the row of every
-  // head that shares the list.  Warp w takes a contiguous range of the
-  // bitmap's words: counts, a prefix over the warps, then ballots per word.
+  // ascending block indices, padded with -1, into the row of every head
+  // that shares the list
   {
-    constexpr int kWarps = kT / 32;
     const size_t orow = a.decode ? size_t(row) : size_t(h) * a.nb + i;
     int32_t* out = a.idx + orow * a.kmax;
-    const int nw = (i + 32) / 32;             // words holding blocks 0..i
-    const int wper = (nw + kWarps - 1) / kWarps;
-    const int w0 = min(nw, warp * wper), w1 = min(nw, w0 + wper);
-    uint32_t mine = 0;
-    for (int x = w0 + lane; x < w1; x += 32) mine += __popc(bits[x]);
-    mine = __reduce_add_sync(0xffffffffu, mine);
-    if (lane == 0) wsum[warp] = mine;
-    __syncthreads();
-    int written = 0, total = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      if (w < warp) written += int(wsum[w]);
-      total += int(wsum[w]);
-    }
-    for (int x = w0; x < w1; ++x) {
-      const bool on = ((bits[x] >> lane) & 1u) != 0;   // bits past i are zero
-      const uint32_t m = __ballot_sync(0xffffffffu, on);
-      const int pos = written + __popc(m & ((1u << lane) - 1u));
-      if (on && pos < a.kmax) out[pos] = 32 * x + lane;
-      written += __popc(m);
-    }
-    for (int t = total + tid; t < a.kmax; t += kT) out[t] = -1;
+    const int total = sa_topk::emit_ascending<kT>(bits, i, out, a.kmax, scr, tid, 0);
     if (tid == 0) a.cnt[orow] = min(total, a.kmax);
     if (G > 1) {
       // the other heads of a group-shared row get copies of the list

@@ -14,7 +14,8 @@ import torch
 from . import (SA_HEAD_RETRIEVAL, SA_HEAD_STREAMING, Shape, sparse_attn_forward,
                sparse_attn_forward_kind, sparse_attn_plan, sparse_attn_pool_kcache,
                sparse_attn_pool_kcache_plan, sparse_attn_score, sparse_attn_score_plan,
-               sparse_attn_score_workspace_size, sparse_attn_select, sparse_attn_select_kind)
+               sparse_attn_score_select, sparse_attn_score_workspace_size, sparse_attn_select,
+               sparse_attn_select_kind)
 
 
 class PrefillLayer:
@@ -70,16 +71,20 @@ class DecodeStep:
     By default (``overlap``) the streaming heads, whose block lists do not
     depend on the scores, are selected and attended on a side stream while
     the retrieval heads score, select and attend on the caller's stream; the
-    step ends when both are done.  ``overlap=False`` runs the three calls
-    for every head in turn on the caller's stream.  The kernels and results
-    are the same."""
+    step ends when both are done.  ``overlap=False`` runs the calls for every
+    head in turn on the caller's stream.  With ``fused`` (the default, for
+    plans without per-head block sizes) the retrieval heads' scores and
+    selection are one launch (``sparse_attn_score_select``); ``fused=False``
+    runs the score and select calls apart.  The results are the same; the
+    streaming heads' rows of ``scores`` are written only when not fused."""
 
     def __init__(self, shape: Shape, budget_blocks: int, head_kind, window_blocks: int,
                  device="cuda", with_lse: bool = False, out_dtype=torch.bfloat16,
-                 granularity=None, head_budget=None, overlap: bool = True):
+                 granularity=None, head_budget=None, overlap: bool = True, fused: bool = True):
         dev = torch.device(device)
         self.shape = shape
         self.overlap = overlap
+        self.fused = fused and granularity is None
         if overlap:
             self.side = torch.cuda.Stream(device=dev)
         self.plan = sparse_attn_plan(shape, budget_blocks, head_kind=head_kind,
@@ -111,12 +116,21 @@ class DecodeStep:
         out = self.out if out is None else out
         if self.overlap:
             return self._overlapped(q, k, v, out, stream)
-        self._score(q, stream)
-        sparse_attn_select(self.shape, self.plan, self.scores, self.idx, self.cnt, self.kmax,
-                           stream=stream)
+        if self.fused:
+            self._score_select(q, stream)
+            sparse_attn_select_kind(self.shape, self.plan, None, self.idx, self.cnt, self.kmax,
+                                    SA_HEAD_STREAMING, stream=stream)
+        else:
+            self._score(q, stream)
+            sparse_attn_select(self.shape, self.plan, self.scores, self.idx, self.cnt, self.kmax,
+                               stream=stream)
         sparse_attn_forward(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax, out,
                             self.lse, self.dev_status, stream=stream)
         return out
+
+    def _score_select(self, q, stream):
+        sparse_attn_score_select(self.shape, self.plan, q, self.kbar, self.scores, self.idx,
+                                 self.cnt, self.kmax, stream=stream)
 
     def _score(self, q, stream):
         if self.sized:
@@ -134,9 +148,12 @@ class DecodeStep:
                                  out, self.lse, self.dev_status, SA_HEAD_STREAMING,
                                  stream=self.side)
         # retrieval heads: scores, top-k, attention
-        self._score(q, main)
-        sparse_attn_select_kind(self.shape, self.plan, self.scores, self.idx, self.cnt,
-                                self.kmax, SA_HEAD_RETRIEVAL, stream=main)
+        if self.fused:
+            self._score_select(q, main)
+        else:
+            self._score(q, main)
+            sparse_attn_select_kind(self.shape, self.plan, self.scores, self.idx, self.cnt,
+                                    self.kmax, SA_HEAD_RETRIEVAL, stream=main)
         sparse_attn_forward_kind(self.shape, self.plan, q, k, v, self.idx, self.cnt, self.kmax,
                                  out, self.lse, self.dev_status, SA_HEAD_RETRIEVAL, stream=main)
         main.wait_stream(self.side)

@@ -324,6 +324,32 @@ sa_status sparse_attn_select_kind(const sa_shape* shp, const sa_plan* plan,
                                   int32_t kmax, int32_t head_kind, sa_stream_t stream);
 
 /*
+ * Decode plans without per-head block sizes: the Index and Select steps of
+ * the retrieval heads in one launch (Spin's Index / Select split, "Abstracción
+ * de Partición Unificada"; the retrieval rows of "Riepilogo Tecnico: Fluxion",
+ * "Intuizioni Chiave" 1 and 2).  The results are those of sparse_attn_score
+ * followed by sparse_attn_select_kind(SA_HEAD_RETRIEVAL), bit for bit, but the
+ * scores need not leave the chip: one thread-block cluster per (sequence, KV
+ * group) scores the group's pooled keys in shared memory and selects from
+ * there, so the selection does not wait for a second launch.
+ *  - q: bf16 [Bt][Hq][d]; kbar: the pooled key cache (fp32 [Bt][Hkv][nb][d],
+ *    sparse_attn_pool_kcache).
+ *  - scores: fp32 [Bt][Hq][nb], or NULL.  When given, the rows of the
+ *    retrieval heads receive their scores; other rows are left as they are.
+ *  - idx [Bt*Hq][kmax], cnt [Bt*Hq]: the rows b*Hq+h of the retrieval heads,
+ *    as sparse_attn_select writes them; the streaming heads' rows are left as
+ *    they are (sparse_attn_select_kind(SA_HEAD_STREAMING) writes them).
+ * All pointers are device pointers, q, kbar and scores 16-byte aligned.  A
+ * plan with no retrieval head returns SA_OK and launches nothing.
+ * Errors: INVALID_ARG (NULL pointers, misalignment, prefill plan), SHAPE
+ * (shape differs from the plan's, kmax too small), NOT_UPLOADED, UNSUPPORTED
+ * (a plan with per-head block sizes, d != 128, Hq/Hkv > 16, nb > 4096), CUDA.
+ */
+sa_status sparse_attn_score_select(const sa_shape* shp, const sa_plan* plan, const void* q,
+                                   const float* kbar, float* scores, int32_t* idx,
+                                   int32_t* cnt, int32_t kmax, sa_stream_t stream);
+
+/*
  * Top-p selection, the data-dependent alternative the S-HPLB pages compare
  * against (Italian summary, "Sparsita' Eterogenea": an adaptive top-p budget
  * fixes accuracy but makes every head's work different).  Prefill only.

@@ -50,7 +50,9 @@ def _check(w, x, r, kinds, budget, window, bf16_out=False):
         kb = od.pool_cache(generate.bf16_to_f32(x["k"][b:b + 1]), w.block)
         np.testing.assert_allclose(r["kbar"][b], kb[0], rtol=1e-5, atol=1e-6)
         sc = od.decode_scores(generate.bf16_to_f64(x["q"][b:b + 1]), kb)[0]
-        np.testing.assert_allclose(r["scores"][b], sc, rtol=1e-4, atol=1e-6)
+        # the retrieval heads' scores (the fused step writes no others)
+        ret = kinds != 1
+        np.testing.assert_allclose(r["scores"][b][ret], sc[ret], rtol=1e-4, atol=1e-6)
         for h in range(w.num_q_heads):
             sel = r["idx"][b, h, :r["cnt"][b, h]]
             assert all(v == -1 for v in r["idx"][b, h, r["cnt"][b, h]:])
@@ -259,8 +261,9 @@ def test_decode_all_streaming_with_block_sizes(env):
 @pytest.mark.parametrize("case", ["small", "full", "block_sizes"])
 def test_decode_overlapped_step_equals_the_serial_step(env, case):
     """Streaming heads selected and attended on a side stream beside the
-    retrieval heads' scoring: the same kernels run on the same rows, so every
-    output, log-sum-exp, index and count equals the serial step's."""
+    retrieval heads' scoring, and the retrieval heads' scoring and selection
+    fused into one launch: every output, log-sum-exp, index and count equals
+    the serial step's with separate calls."""
     import json
     import os
     sa, torch = env
@@ -280,9 +283,10 @@ def test_decode_overlapped_step_equals_the_serial_step(env, case):
         kw = {"granularity": prof["gran"], "head_budget": prof["budget"]}
     t = {n: to_dev(x[n]) for n in "qkv"}
     res = []
-    for overlap in (False, True):
+    for overlap, fused in ((False, False), (False, True), (True, False), (True, True)):
         step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
-                          with_lse=True, out_dtype=torch.float32, overlap=overlap, **kw)
+                          with_lse=True, out_dtype=torch.float32, overlap=overlap, fused=fused,
+                          **kw)
         step.build_cache(t["k"])
         for _ in range(2):   # a second call on the same buffers changes nothing
             step.idx.fill_(-5)
@@ -292,8 +296,9 @@ def test_decode_overlapped_step_equals_the_serial_step(env, case):
             assert int(step.dev_status.item()) == 0
         res.append((out.clone(), step.lse.clone(), step.idx.clone(), step.cnt.clone()))
         del step
-    for a, b in zip(res[0], res[1]):
-        assert torch.equal(a, b)
+    for other in res[1:]:
+        for a, b in zip(res[0], other):
+            assert torch.equal(a, b)
 
 
 def test_decode_overlapped_step_replays_from_a_cuda_graph(env):
@@ -378,3 +383,66 @@ def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
         step.out.fill_(float("nan"))
         assert forward() == 0
         assert torch.equal(step.out, want)
+
+
+@pytest.mark.parametrize("L,Hq,Hkv,Bt,budget,zero_q", [
+    (65536, 28, 4, 16, 64, False),    # the 64K workload: 2048 blocks, clusters of four CTAs
+    (8192, 28, 4, 1, 64, False),      # one sequence: clusters of eight CTAs
+    (131072, 16, 1, 1, 100, False),   # 4096 blocks, one KV group of 16 heads
+    (4096, 4, 4, 2, 9, False),        # groups of one head
+    (256, 8, 2, 2, 3, False),         # 8 blocks: the first CTA of a cluster holds them all
+    (2048, 8, 2, 2, 64, False),       # the budget keeps every block
+    (4096, 8, 2, 2, 20, True),        # zero queries: every score ties, lowest indices win
+])
+def test_score_select_equals_separate_calls(env, L, Hq, Hkv, Bt, budget, zero_q):
+    """The fused Index + Select launch gives the separate score and select
+    calls' scores, lists and counts bit for bit on the retrieval heads' rows,
+    and leaves the streaming heads' rows as they were."""
+    sa, torch = env
+    from tests._parity import to_dev
+    from workloads import generate, scaled, workload
+    w = scaled(workload(5), L, num_q_heads=Hq, num_kv_heads=Hkv, batch=Bt)
+    x = generate.decode_inputs(w, tensors="qk")
+    kinds = generate.head_kinds(w)
+    if not (kinds == 1).any():
+        kinds[0] = 1                        # keep one streaming row to check it is untouched
+    nb = w.nb
+    shape = sa.Shape.decode(L, w.block, Hq, Hkv, w.head_dim, Bt)
+    plan = sa.sparse_attn_plan(shape, min(budget, nb), head_kind=kinds, window_blocks=2,
+                               num_workers=1)
+    plan.upload()
+    kmax = plan.info()["kmax"]
+    q, k = to_dev(x["q"]), to_dev(x["k"])
+    if zero_q:
+        q.zero_()
+    kbar = torch.empty(Bt * Hkv * nb * w.head_dim, dtype=torch.float32, device="cuda")
+    sa.sparse_attn_pool_kcache(shape, k, kbar)
+    rows = Bt * Hq
+
+    def buffers():
+        return (torch.full((rows * nb,), float("nan"), dtype=torch.float32, device="cuda"),
+                torch.full((rows * kmax,), -7, dtype=torch.int32, device="cuda"),
+                torch.full((rows,), -7, dtype=torch.int32, device="cuda"))
+
+    sc_a, idx_a, cnt_a = buffers()
+    sa.sparse_attn_score(shape, q, kbar, sc_a, None, 0)
+    sa.sparse_attn_select_kind(shape, plan, sc_a, idx_a, cnt_a, kmax, sa.SA_HEAD_RETRIEVAL)
+    sc_b, idx_b, cnt_b = buffers()
+    sa.sparse_attn_score_select(shape, plan, q, kbar, sc_b, idx_b, cnt_b, kmax)
+    _, idx_c, cnt_c = buffers()
+    sa.sparse_attn_score_select(shape, plan, q, kbar, None, idx_c, cnt_c, kmax)
+    torch.cuda.synchronize()
+    ret = torch.tensor(np.tile(kinds != 1, Bt), device="cuda")
+    sc_a, sc_b = sc_a.view(rows, nb), sc_b.view(rows, nb)
+    idx_a, idx_b, idx_c = (t.view(rows, kmax) for t in (idx_a, idx_b, idx_c))
+    assert torch.equal(sc_a[ret], sc_b[ret])
+    assert torch.isnan(sc_b[~ret]).all()
+    for idx, cnt in ((idx_b, cnt_b), (idx_c, cnt_c)):
+        assert torch.equal(idx[ret], idx_a[ret])
+        assert torch.equal(cnt[ret], cnt_a[ret])
+        assert (idx[~ret] == -7).all() and (cnt[~ret] == -7).all()
+    keep = min(budget, nb)
+    assert (cnt_a[ret] == keep).all()
+    if zero_q:
+        want = list(range(keep - 1)) + [nb - 1]
+        assert all(r.tolist()[:keep] == want for r in idx_a[ret].cpu())
