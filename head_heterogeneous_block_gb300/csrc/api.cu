@@ -457,9 +457,9 @@ sa_status sparse_attn_score_select(const sa_shape* shp, const sa_plan* plan, con
   if (!aligned16(q) || !aligned16(kbar) || (scores && !aligned16(scores)))
     return SA_ERR_INVALID_ARG;
   if (kmax < plan->kmax) return SA_ERR_SHAPE;
-  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
   if (has_granularity(plan) || shp->head_dim != 128 || plan->group > 16 || plan->nb > 4096)
     return SA_ERR_UNSUPPORTED;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
   if (int32_t(plan->kinds.size()) == plan->n_streaming) return SA_OK;
   sa_k::IndexSelectArgs a;
   a.q = q;

@@ -220,6 +220,25 @@ def test_device_calls_reject_bad_arguments_before_launch(sa):
                                         None) == 1
     assert lib.sparse_attn_forward_kind(ds, dplan.handle, P, P, P, P, P, 16, P, 0, None, P, 0,
                                         None) == 8
+    # fused decode scoring and selection: prefill plans, null or misaligned
+    # pointers, kmax below the plan's, unsupported plans, not uploaded
+    ss = lib.sparse_attn_score_select
+    assert ss(s, plan.handle, P, P, P, P, P, 9, None) == 1
+    assert ss(ds, None, P, P, P, P, P, 16, None) == 1
+    assert ss(ds, dplan.handle, None, P, P, P, P, 16, None) == 1
+    assert ss(ds, dplan.handle, P, P, P, None, P, 16, None) == 1
+    assert ss(ds, dplan.handle, P, P + 4, P, P, P, 16, None) == 1
+    assert ss(ds, dplan.handle, P, P, P + 8, P, P, 16, None) == 1
+    assert ss(ds, dplan.handle, P, P, P, P, P, 3, None) == 2
+    assert ss(ctypes.byref(sa.Shape.decode(4096, 32, 8, 2, 128, 2)), dplan.handle, P, P, P, P, P,
+              16, None) == 2
+    assert ss(ds, dplan.handle, P, P, None, P, P, 16, None) == 8   # scores may be NULL
+    d64 = sa.Shape.decode(2048, 32, 8, 2, 64, 2)
+    p64 = sa.sparse_attn_plan(d64, 8, head_kind=[0] * 8, num_workers=1)
+    assert ss(ctypes.byref(d64), p64.handle, P, P, P, P, P, 16, None) == 3
+    sized = sa.sparse_attn_plan(dshape, 8, head_kind=[1, 0] * 4, window_blocks=4, num_workers=1,
+                                granularity=[32, 16] * 4, head_budget=[8] * 8)
+    assert ss(ds, sized.handle, P, P, P, P, P, sized.info()["kmax"], None) == 3
     n = ctypes.c_size_t()
     assert lib.sparse_attn_score_workspace_size(s, ctypes.byref(n)) == 0
     assert n.value == (8 + 2) * 64 * 64 * 4
