@@ -29,9 +29,10 @@ constexpr int kMaxWords = 2048 / 32;
 
 using sa_topk::order_bits;
 
-// kT threads with kPer candidates each: rows of up to kPer * kT blocks.
+// One row per CTA of kT threads with kPer candidates each: rows of up to
+// kPer * kT blocks.
 template <int kT, int kPer>
-__global__ void __launch_bounds__(kT) select_kernel(sa_k::SelectArgs a) {
+__device__ __forceinline__ void select_row(const sa_k::SelectArgs& a) {
   __shared__ uint32_t bits[kPer * kT / 32];
   __shared__ sa_topk::Scratch scr;
   const int tid = threadIdx.x;
@@ -123,6 +124,18 @@ __global__ void __launch_bounds__(kT) select_kernel(sa_k::SelectArgs a) {
       }
     }
   }
+}
+
+// Prefill launches tens of thousands of short rows: nine 128-thread CTAs per
+// SM (at most 56 registers) keep more of them in flight.  Decode rows take a
+// 512-thread CTA each.
+template <int kPer>
+__global__ void __launch_bounds__(128, 9) select_kernel(sa_k::SelectArgs a) {
+  select_row<128, kPer>(a);
+}
+template <int kPer>
+__global__ void __launch_bounds__(512) select_kernel_wide(sa_k::SelectArgs a) {
+  select_row<512, kPer>(a);
 }
 
 // Top-p selection of prefill row (h, i): block probabilities are the
@@ -368,11 +381,11 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
   // decode launches few rows (sequences x heads): wider CTAs per row
   const int row = std::max(a.nb, a.max_row);
   if (!a.decode && row <= 16 * kThreads)
-    select_kernel<kThreads, 16><<<unsigned(a.rows), kThreads, 0, st>>>(a);
+    select_kernel<16><<<unsigned(a.rows), kThreads, 0, st>>>(a);
   else if (a.decode && row <= 4 * 512)
-    select_kernel<512, 4><<<unsigned(a.rows), 512, 0, st>>>(a);
+    select_kernel_wide<4><<<unsigned(a.rows), 512, 0, st>>>(a);
   else if (a.decode && row <= 8 * 512)
-    select_kernel<512, 8><<<unsigned(a.rows), 512, 0, st>>>(a);
+    select_kernel_wide<8><<<unsigned(a.rows), 512, 0, st>>>(a);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -13,10 +13,8 @@
 //
 // A row is handled by a group of kT threads (a whole CTA, or one warpgroup of
 // it) that synchronise on their own named barrier, so several rows can be
-// selected at once in one CTA.  Each pass costs one barrier: the histograms
-// rotate through three buffers (a pass counts into one, every warp then
-// reads it and finds the threshold bin by itself, and the buffer two passes
-// ahead is cleared meanwhile), so no result has to be broadcast.
+// selected at once in one CTA.  In each pass one warp scans the histogram and
+// hands the bin on through shared memory.
 //
 // Candidate layout: thread t of the group holds the candidates
 // j = 1 + t + r*kT, r < kPer, as order bits u[r] (entries with j > last are
@@ -48,8 +46,9 @@ __device__ __forceinline__ void group_sync(int bar) {
 }
 
 struct Scratch {
-  uint32_t hist[3][256];
+  uint32_t hist[256];
   uint32_t cnt[256];       // per (candidate column r, warp): counts of a class of candidates
+  uint32_t ctl[4];         // the threshold bin of a pass
 };
 
 // The threshold of a row: candidates with order bits above T (or, when
@@ -61,78 +60,98 @@ struct Threshold {
   bool ties;
 };
 
+// Adds to hist the next 8 bits (at `shift`) of the candidates of 1..last
+// whose higher bits equal prefix.
+template <int kT, int kPer, bool kMatch>
+__device__ __forceinline__ void count_pass(const uint32_t (&u)[kPer], int last, uint32_t prefix,
+                                           uint32_t mask, int shift, uint32_t* hist, int tid) {
+  const int lane = tid & 31;
+  if (kMatch && shift == 24) {
+    // the top byte (sign and high exponent bits) puts most scores in a few
+    // bins: one atomic per bin and warp instead of per lane
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int j = 1 + tid + r * kT;
+      const uint32_t bin = j <= last ? (u[r] >> 24) : 256u;
+      const uint32_t same = __match_any_sync(0xffffffffu, bin);
+      if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int j = 1 + tid + r * kT;
+      if (j <= last && (u[r] & mask) == prefix) atomicAdd(&hist[(u[r] >> shift) & 255u], 1u);
+    }
+  }
+}
+
+// One warp finds the bin holding the need-th largest: lane l holds bins
+// 255-8l .. 248-8l (descending), a scan over the lanes, then the lane whose
+// range holds it picks the bin.  Every lane gets the bin, the count above it
+// and the count in it.
+__device__ __forceinline__ void scan_bins(const uint32_t* hist, uint32_t need, int lane,
+                                          uint32_t& bin, uint32_t& above, uint32_t& in_bin) {
+  uint32_t c[8], local = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    c[k] = hist[255 - 8 * lane - k];
+    local += c[k];
+  }
+  uint32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint32_t excl = incl - local;
+  const bool here = excl < need && need <= incl;
+  bin = above = in_bin = 0;
+  if (here) {
+    uint32_t acc = excl;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (acc + c[k] >= need) {
+        bin = uint32_t(255 - 8 * lane - k);
+        above = acc;
+        in_bin = c[k];
+        break;
+      }
+      acc += c[k];
+    }
+  }
+  const int src = __ffs(__ballot_sync(0xffffffffu, here)) - 1;
+  bin = __shfl_sync(0xffffffffu, bin, src);
+  above = __shfl_sync(0xffffffffu, above, src);
+  in_bin = __shfl_sync(0xffffffffu, in_bin, src);
+}
+
 // Finds the threshold that keeps the `need` (>= 1, < number of candidates)
 // highest candidates of 1..last, ties to the lower index.  kPer * kT <= 4096.
 template <int kT, int kPer, bool kMatch>
 __device__ __forceinline__ Threshold find_threshold(const uint32_t (&u)[kPer], int last,
                                                     uint32_t need, Scratch& s, int tid, int bar) {
   const int lane = tid & 31;
-  for (int b = tid; b < 2 * 256; b += kT) (&s.hist[0][0])[b] = 0u;
-  group_sync<kT>(bar);
   uint32_t prefix = 0, mask = 0, eq_total = 0;
-  int p = 0;
-  for (int shift = 24; shift >= 0; shift -= 8, ++p) {
-    uint32_t* hist = s.hist[p % 3];
-    if (kMatch && shift == 24) {
-      // the top byte (sign and high exponent bits) puts most scores in a few
-      // bins: one atomic per bin and warp instead of per lane
-#pragma unroll
-      for (int r = 0; r < kPer; ++r) {
-        const int j = 1 + tid + r * kT;
-        const uint32_t bin = j <= last ? (u[r] >> 24) : 256u;
-        const uint32_t same = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256u && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
-      }
-    } else {
-#pragma unroll
-      for (int r = 0; r < kPer; ++r) {
-        const int j = 1 + tid + r * kT;
-        if (j <= last && (u[r] & mask) == prefix) atomicAdd(&hist[(u[r] >> shift) & 255u], 1u);
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += kT) s.hist[b] = 0u;
+    group_sync<kT>(bar);
+    count_pass<kT, kPer, kMatch>(u, last, prefix, mask, shift, s.hist, tid);
+    group_sync<kT>(bar);
+    if (tid < 32) {
+      uint32_t bin, above, in_bin;
+      scan_bins(s.hist, need, lane, bin, above, in_bin);
+      if (lane == 0) {
+        s.ctl[0] = bin;
+        s.ctl[1] = above;
+        s.ctl[2] = in_bin;
       }
     }
     group_sync<kT>(bar);
-    // every warp finds the bin holding the need-th largest: lane l holds bins
-    // 255-8l .. 248-8l (descending), a scan over the lanes, then the lane
-    // whose range holds it picks the bin
-    uint32_t c[8], local = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      c[k] = hist[255 - 8 * lane - k];
-      local += c[k];
-    }
-    uint32_t incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const uint32_t excl = incl - local;
-    const bool here = excl < need && need <= incl;
-    uint32_t bin = 0, above = 0, in_bin = 0;
-    if (here) {
-      uint32_t acc = excl;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (acc + c[k] >= need) {
-          bin = uint32_t(255 - 8 * lane - k);
-          above = acc;
-          in_bin = c[k];
-          break;
-        }
-        acc += c[k];
-      }
-    }
-    const int src = __ffs(__ballot_sync(0xffffffffu, here)) - 1;
-    bin = __shfl_sync(0xffffffffu, bin, src);
-    above = __shfl_sync(0xffffffffu, above, src);
-    in_bin = __shfl_sync(0xffffffffu, in_bin, src);
-    // the buffer pass p + 2 counts into: its readers (pass p - 1) are past
-    // this pass's barrier, its writers (pass p + 2) behind the next one
-    for (int b = tid; b < 256; b += kT) s.hist[(p + 2) % 3][b] = 0u;
-    need -= above;
-    eq_total = in_bin;
-    prefix |= bin << shift;
+    need -= s.ctl[1];
+    eq_total = s.ctl[2];
+    prefix |= s.ctl[0] << shift;
     mask |= 0xFFu << shift;
+    group_sync<kT>(bar);
     // the bin holds exactly the candidates still needed: all of them, and
     // everything above, are kept (u >= prefix, lower bits zero)
     if (eq_total == need) break;
@@ -143,7 +162,7 @@ __device__ __forceinline__ Threshold find_threshold(const uint32_t (&u)[kPer], i
 // Marks in `bits` the `need` (>= 1, < number of candidates) highest
 // candidates of 1..last, ties to the lower index.  Ends without a barrier:
 // synchronise the group before reading `bits`.  kPer * kT <= 4096.
-template <int kT, int kPer, bool kMatch = true>
+template <int kT, int kPer, bool kMatch>
 __device__ __forceinline__ void mark_top(const uint32_t (&u)[kPer], int last, uint32_t need_in,
                                          uint32_t* bits, Scratch& s, int tid, int bar) {
   static_assert(kPer * (kT / 32) <= 128, "tie counts");
@@ -162,30 +181,23 @@ __device__ __forceinline__ void mark_top(const uint32_t (&u)[kPer], int last, ui
   // ties straddle the threshold: every candidate above T, and the `need`
   // lowest-indexed ones equal to T.  Candidate (t, r) has index 1 + t + r*kT,
   // so the equal ones before it are those of the columns r' < r and those of
-  // column r at lower t: count each (column, warp) once, then add up.
-  uint32_t eqm[kPer];
+  // column r at lower t: column by column, two barriers each (the fewest
+  // registers; ties at the threshold are rare)
+  uint32_t taken = 0;
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
     const int j = 1 + tid + r * kT;
-    eqm[r] = __ballot_sync(0xffffffffu, j <= last && u[r] == T);
-    if (lane == 0) s.cnt[r * kWarps + warp] = __popc(eqm[r]);
-  }
-  group_sync<kT>(bar);
-  uint32_t before = 0;
-#pragma unroll
-  for (int r = 0; r < kPer; ++r) {
-    const int j = 1 + tid + r * kT;
-    uint32_t col = 0, mine = before;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const uint32_t n = s.cnt[r * kWarps + w];
-      col += n;
-      if (w < warp) mine += n;
-    }
-    mine += __popc(eqm[r] & ((1u << lane) - 1u));
-    const bool eq = (eqm[r] >> lane) & 1u;
-    if (j <= last && (u[r] > T || (eq && mine < need))) atomicOr(&bits[j >> 5], 1u << (j & 31));
-    before += col;
+    const bool valid = j <= last;
+    const bool eq = valid && u[r] == T;
+    const uint32_t m = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) s.cnt[warp] = __popc(m);
+    group_sync<kT>(bar);
+    uint32_t before = taken;
+    for (int w = 0; w < warp; ++w) before += s.cnt[w];
+    before += __popc(m & ((1u << lane) - 1u));
+    if (valid && (u[r] > T || (eq && before < need))) atomicOr(&bits[j >> 5], 1u << (j & 31));
+    for (int w = 0; w < kWarps; ++w) taken += s.cnt[w];
+    group_sync<kT>(bar);
   }
 }
 
@@ -241,16 +253,17 @@ __device__ __forceinline__ int emit_top(const uint32_t (&u)[kPer], int last, Thr
   constexpr int kEq = kPer * kWarps;        // equal-to-T counts follow the above-T ones
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t lt = (1u << lane) - 1u;
-  uint32_t am[kPer], em[kPer];
+  auto above = [&](int r) {
+    return 1 + tid + r * kT <= last && (th.ties ? u[r] > th.T : u[r] >= th.T);
+  };
+  auto equal = [&](int r) { return 1 + tid + r * kT <= last && th.ties && u[r] == th.T; };
 #pragma unroll
   for (int r = 0; r < kPer; ++r) {
-    const int j = 1 + tid + r * kT;
-    const bool ok = j <= last;
-    am[r] = __ballot_sync(0xffffffffu, ok && (th.ties ? u[r] > th.T : u[r] >= th.T));
-    em[r] = __ballot_sync(0xffffffffu, ok && th.ties && u[r] == th.T);
+    const uint32_t am = __ballot_sync(0xffffffffu, above(r));
+    const uint32_t em = __ballot_sync(0xffffffffu, equal(r));
     if (lane == 0) {
-      s.cnt[r * kWarps + warp] = __popc(am[r]);
-      s.cnt[kEq + r * kWarps + warp] = __popc(em[r]);
+      s.cnt[r * kWarps + warp] = __popc(am);
+      s.cnt[kEq + r * kWarps + warp] = __popc(em);
     }
   }
   group_sync<kT>(bar);
@@ -268,10 +281,11 @@ __device__ __forceinline__ int emit_top(const uint32_t (&u)[kPer], int last, Thr
         e_mine += ne;
       }
     }
-    a_mine += __popc(am[r] & lt);
-    e_mine += __popc(em[r] & lt);
-    const bool above = (am[r] >> lane) & 1u, eq = (em[r] >> lane) & 1u;
-    if (above || (eq && e_mine < th.need)) {
+    // the ballots again rather than kept (registers are the scarcer)
+    const bool ab = above(r), eq = equal(r);
+    a_mine += __popc(__ballot_sync(0xffffffffu, ab) & lt);
+    e_mine += __popc(__ballot_sync(0xffffffffu, eq) & lt);
+    if (ab || (eq && e_mine < th.need)) {
       const uint32_t pos = 1 + a_mine + min(e_mine, th.need);
       if (pos < uint32_t(kmax)) out[pos] = 1 + tid + r * kT;
     }
