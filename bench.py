@@ -404,6 +404,30 @@ def run_ours(args):
     pipe.run(steps_in, stream=stream, before_step=replan)
     e2e_s = (time.perf_counter() - t1) / e2e_steps
     e2e_value = flops / e2e_s / 1e12
+
+    # the host link alone: one step's copies with no compute, each direction
+    # by itself and both at once on the pipeline's two copy streams; the
+    # larger of the both-at-once time and the device step bounds e2e
+    def link(direction, reps=3):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            if direction in ("in", "both"):
+                with torch.cuda.stream(pipe.copy_in):
+                    for n in "qkv":
+                        pipe.bufs[0][n].copy_(host[n], non_blocking=True)
+            if direction in ("out", "both"):
+                with torch.cuda.stream(pipe.copy_out):
+                    out_host[0].copy_(pipe.bufs[0]["o"], non_blocking=True)
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / reps
+
+    link("both", 1)
+    t_in, t_out, t_both = link("in"), link("out"), link("both")
+    host_link = {"h2d_gbs": round(h2d / t_in / 1e9, 1), "d2h_gbs": round(d2h / t_out / 1e9, 1),
+                 "copies_ms_per_step": round(t_both * 1e3, 3),
+                 "floor_ms_per_step": round(max(t_both * 1e3, ms_step), 3),
+                 "bound": "host link" if t_both * 1e3 > ms_step else "device"}
     del pipe
 
     # ---- decode step (workload 5), reported beside the prefill line
@@ -437,7 +461,8 @@ def run_ours(args):
         "topp": topp,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_s * 1e3, 3),
-                "overlap": "double-buffered: copies of one step overlap another's compute"},
+                "overlap": "double-buffered: copies of one step overlap another's compute",
+                "host_link": host_link},
         "gpu_launches": 5 * args.steps,
         "clocks": clk,
         "device_status": status,
