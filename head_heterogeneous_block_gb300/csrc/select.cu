@@ -127,11 +127,20 @@ __device__ __forceinline__ void select_row(const sa_k::SelectArgs& a) {
 }
 
 // Prefill launches tens of thousands of short rows: nine 128-thread CTAs per
-// SM (at most 56 registers) keep more of them in flight.  Decode rows take a
+// SM (at most 56 registers) keep more of them in flight, and a row takes only
+// as many candidates per thread as its length needs.  Decode rows take a
 // 512-thread CTA each.
 template <int kPer>
 __global__ void __launch_bounds__(128, 9) select_kernel(sa_k::SelectArgs a) {
-  select_row<128, kPer>(a);
+  // (prefill rows only) a row i has i - 1 candidates: shorter rows take
+  // fewer per thread
+  const int i = int(blockIdx.x) % a.nb;
+  if (kPer > 4 && i < 4 * 128)
+    select_row<128, 4>(a);
+  else if (kPer > 8 && i < 8 * 128)
+    select_row<128, 8>(a);
+  else
+    select_row<128, kPer>(a);
 }
 template <int kPer>
 __global__ void __launch_bounds__(512) select_kernel_wide(sa_k::SelectArgs a) {
