@@ -393,6 +393,7 @@ def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
     (256, 8, 2, 2, 3, False),         # 8 blocks: the first CTA of a cluster holds them all
     (2048, 8, 2, 2, 64, False),       # the budget keeps every block
     (4096, 8, 2, 2, 20, True),        # zero queries: every score ties, lowest indices win
+    (4096, 8, 2, 3, 16, "group0"),    # KV group 0 all streaming: its clusters return at once
 ])
 def test_score_select_equals_separate_calls(env, L, Hq, Hkv, Bt, budget, zero_q):
     """The fused Index + Select launch gives the separate score and select
@@ -404,6 +405,11 @@ def test_score_select_equals_separate_calls(env, L, Hq, Hkv, Bt, budget, zero_q)
     w = scaled(workload(5), L, num_q_heads=Hq, num_kv_heads=Hkv, batch=Bt)
     x = generate.decode_inputs(w, tensors="qk")
     kinds = generate.head_kinds(w)
+    if zero_q == "group0":
+        G = Hq // Hkv
+        kinds[:G] = 1                       # every head of KV group 0 streams
+        kinds[G:] = [0, 1] * (G // 2)
+        zero_q = False
     if not (kinds == 1).any():
         kinds[0] = 1                        # keep one streaming row to check it is untouched
     nb = w.nb
@@ -446,3 +452,21 @@ def test_score_select_equals_separate_calls(env, L, Hq, Hkv, Bt, budget, zero_q)
     if zero_q:
         want = list(range(keep - 1)) + [nb - 1]
         assert all(r.tolist()[:keep] == want for r in idx_a[ret].cpu())
+
+
+def test_score_select_with_no_retrieval_head_launches_nothing(env):
+    """A plan whose heads all stream: the fused call returns at once and
+    leaves every output as it was."""
+    sa, torch = env
+    shape = sa.Shape.decode(2048, 32, 8, 2, 128, 2)
+    plan = sa.sparse_attn_plan(shape, 8, head_kind=[1] * 8, window_blocks=4, num_workers=1)
+    plan.upload()
+    kmax = plan.info()["kmax"]
+    q = torch.zeros(2, 8, 128, dtype=torch.bfloat16, device="cuda")
+    kbar = torch.zeros(2 * 2 * 64 * 128, dtype=torch.float32, device="cuda")
+    sc = torch.full((2 * 8 * 64,), float("nan"), device="cuda")
+    idx = torch.full((2 * 8 * kmax,), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((16,), -7, dtype=torch.int32, device="cuda")
+    sa.sparse_attn_score_select(shape, plan, q, kbar, sc, idx, cnt, kmax)
+    torch.cuda.synchronize()
+    assert torch.isnan(sc).all() and (idx == -7).all() and (cnt == -7).all()
