@@ -50,11 +50,12 @@ constexpr int kStageBytes = kRows * 32 * 16;
 constexpr int kMaxGroup = 16;
 
 // Dynamic shared memory: kStages chunk buffers, the group's queries
-// [G][32] uint2, the scores [G][R] fp32.  After scoring, the two warpgroups'
-// gathered score rows and scratch reuse the chunk buffers.
-size_t smem_bytes(int group, int rows_per_cta) {
+// [G][32] uint2, the scores [max_retrieval][R] fp32 (a row per retrieval head
+// of the group, by its slot).  After scoring, the two warpgroups' gathered
+// score rows and scratch reuse the chunk buffers.
+size_t smem_bytes(int group, int max_retrieval, int rows_per_cta) {
   return size_t(kStages) * kStageBytes + size_t(group) * 256 +
-         size_t(group) * size_t(rows_per_cta) * 4;
+         size_t(max_retrieval) * size_t(rows_per_cta) * 4;
 }
 
 template <int kCP, int kPer>
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int j = base + r;
         if (((rmask >> hh) & 1u) && j < rows) {
           const float s = v * a.scale;
-          sc[hh * R + j] = s;
+          sc[__popc(rmask & ((1u << hh) - 1u)) * R + j] = s;   // the head's slot
           if (a.scores) a.scores[(size_t(b) * a.Hq + g * G + hh) * nb + r0 + j] = s;
         }
       });
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       // 64, so the four lie in one CTA)
       for (int j0 = 4 * gt; j0 < nb; j0 += 4 * 128) {
         const int owner = j0 / R;
-        const float* src = cluster.map_shared_rank(sc, owner) + hh * R + (j0 - owner * R);
+        const float* src = cluster.map_shared_rank(sc, owner) + slot * R + (j0 - owner * R);
         *reinterpret_cast<float4*>(srow + j0) = *reinterpret_cast<const float4*>(src);
       }
       sa_topk::group_sync<128>(bar);
@@ -224,7 +225,8 @@ cudaError_t launch_decode_index_select(const IndexSelectArgs& args, cudaStream_t
   IndexSelectArgs a = args;
   const int per = (a.nb + cp - 1) / cp;
   a.rows_per_cta = (per + kRows - 1) / kRows * kRows;
-  const size_t smem = smem_bytes(a.group, a.rows_per_cta);
+  if (a.max_retrieval < 1 || a.max_retrieval > a.group) return cudaErrorInvalidValue;
+  const size_t smem = smem_bytes(a.group, a.max_retrieval, a.rows_per_cta);
   const int grid = int(pairs * cp);
   // a warpgroup selects a row: 16 candidates per thread up to 2048 blocks, else 32
   if (a.nb <= 16 * 128)

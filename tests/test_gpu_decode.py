@@ -394,6 +394,7 @@ def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
     (2048, 8, 2, 2, 64, False),       # the budget keeps every block
     (4096, 8, 2, 2, 20, True),        # zero queries: every score ties, lowest indices win
     (4096, 8, 2, 3, 16, "group0"),    # KV group 0 all streaming: its clusters return at once
+    (65536, 32, 4, 4, 64, False),     # groups of 8 heads (score rows kept per retrieval head)
 ])
 def test_score_select_equals_separate_calls(env, L, Hq, Hkv, Bt, budget, zero_q):
     """The fused Index + Select launch gives the separate score and select
