@@ -25,7 +25,6 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kPerThread = 16;            // candidates per thread: nb <= 2048
-constexpr int kMaxWords = 2048 / 32;
 
 using sa_topk::order_bits;
 
@@ -154,8 +153,12 @@ __global__ void __launch_bounds__(512) select_kernel_wide(sa_k::SelectArgs a) {
 // of 2^-32 of the row's total), so the result does not depend on the order of
 // the additions.  The threshold is found as in select_kernel, with histograms
 // of probability mass next to the counts.
-__global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a) {
-  __shared__ uint32_t bits[kMaxWords];
+// The rows i in [i0, i0 + span) of every head, kPer candidates per thread
+// (rows of up to kPer * kThreads blocks).
+template <int kPer>
+__global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a, int i0,
+                                                                int span) {
+  __shared__ uint32_t bits[kPer * kThreads / 32];
   __shared__ unsigned long long hmass[kThreads / 32][256];   // one histogram per warp
   __shared__ uint32_t hcount[kThreads / 32][256];
   __shared__ float redf[kThreads / 32];
@@ -163,17 +166,17 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
   __shared__ uint32_t ctl[3];
   __shared__ uint32_t wsum[kThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x;
-  const int h = row / a.nb, i = row - h * a.nb;
+  const int h = int(blockIdx.x) / span, i = i0 + int(blockIdx.x) % span;
+  const int row = h * a.nb + i;
   const float* srow = a.scores + (size_t(h) * a.nb + i) * a.nb;
   const int nwords = (i + 1 + 31) / 32;
   for (int w = tid; w < nwords; w += kThreads) bits[w] = 0u;
 
   // scores of blocks j = tid + r*kThreads (all j <= i, mandatory ones included)
-  float sv[kPerThread];
+  float sv[kPer];
   float mx = -INFINITY;
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
+  for (int r = 0; r < kPer; ++r) {
     const int j = tid + r * kThreads;
     sv[r] = (j <= i) ? srow[j] : -INFINITY;
     mx = fmaxf(mx, sv[r]);
@@ -186,9 +189,9 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
 #pragma unroll
   for (int w = 1; w < kThreads / 32; ++w) mx = fmaxf(mx, redf[w]);
   __syncthreads();
-  float e[kPerThread], tot = 0.f;
+  float e[kPer], tot = 0.f;
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
+  for (int r = 0; r < kPer; ++r) {
     const int j = tid + r * kThreads;
     e[r] = (j <= i) ? exp2f((sv[r] - mx) * 1.4426950408889634f) : 0.f;
     tot += e[r];
@@ -203,10 +206,10 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
   const float scale = 4294967296.0f / tot;                  // 2^32 / total
   // fixed-point masses (a block's share is at most 2^32, kept as 2^32 - 1);
   // the mandatory blocks' mass is taken first
-  uint32_t q[kPerThread];
+  uint32_t q[kPer];
   unsigned long long mand = 0;
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
+  for (int r = 0; r < kPer; ++r) {
     const int j = tid + r * kThreads;
     const float x = e[r] * scale;
     q[r] = (j <= i) ? (x >= 4294967296.0f ? 0xFFFFFFFFu : uint32_t(x)) : 0u;
@@ -226,10 +229,10 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
   __syncthreads();
   if (i >= 2 && goal > have) {
     unsigned long long need = goal - have;           // mass wanted from blocks 1..i-1
-    uint32_t u[kPerThread];
+    uint32_t u[kPer];
     unsigned long long cand = 0;
 #pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
+    for (int r = 0; r < kPer; ++r) {
       const int j = tid + r * kThreads;
       const bool c = j >= 1 && j <= i - 1;
       u[r] = c ? order_bits(sv[r]) : 0u;
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
         }
         __syncthreads();
 #pragma unroll
-        for (int r = 0; r < kPerThread; ++r) {
+        for (int r = 0; r < kPer; ++r) {
           const int j = tid + r * kThreads;
           if (j >= 1 && j <= i - 1 && (u[r] & mask) == prefix) {
             const uint32_t b = (u[r] >> shift) & 255u;
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
         if (eq_count == 1 && shift > 0) {
           // one candidate left in the bin: it is the threshold
 #pragma unroll
-          for (int r = 0; r < kPerThread; ++r) {
+          for (int r = 0; r < kPer; ++r) {
             const int j = tid + r * kThreads;
             if (j >= 1 && j <= i - 1 && (u[r] & mask) == prefix) ctl[2] = u[r];
           }
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
       // the lowest indices, as many as the remaining mass needs
       unsigned long long qT = 0;
 #pragma unroll
-      for (int r = 0; r < kPerThread; ++r) {
+      for (int r = 0; r < kPer; ++r) {
         const int j = tid + r * kThreads;
         if (j >= 1 && j <= i - 1 && u[r] == T) qT = q[r];
       }
@@ -333,13 +336,13 @@ __global__ void __launch_bounds__(kThreads) select_topp_kernel(sa_k::TopPArgs a)
       if (take == eq_count) {
         // every candidate at T is kept: no order among them is needed
 #pragma unroll
-        for (int r = 0; r < kPerThread; ++r) {
+        for (int r = 0; r < kPer; ++r) {
           const int j = tid + r * kThreads;
           if (j >= 1 && j <= i - 1 && u[r] >= T) atomicOr(&bits[j >> 5], 1u << (j & 31));
         }
       } else {
       uint32_t taken = 0;
-      for (int r = 0; r < kPerThread; ++r) {
+      for (int r = 0; r < kPer; ++r) {
         const int j = tid + r * kThreads;
         const bool valid = j >= 1 && j <= i - 1;
         const bool eq = valid && u[r] == T;
@@ -380,8 +383,24 @@ namespace sa_k {
 cudaError_t launch_select_topp(const TopPArgs& a, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;
   if (a.nb > kPerThread * kThreads) return cudaErrorInvalidValue;
-  select_topp_kernel<<<unsigned(a.rows), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  // a row i holds i + 1 blocks: rows below 512 and 1024 blocks take 4 and 8
+  // candidates per thread (three launches, each with its own registers)
+  const int heads = a.rows / a.nb;
+  const int bounds[4] = {0, 4 * kThreads, 8 * kThreads, kPerThread * kThreads};
+  for (int r = 0; r < 3; ++r) {
+    const int lo = bounds[r], hi = std::min(bounds[r + 1], a.nb);
+    if (hi <= lo) continue;
+    const unsigned grid = unsigned(heads) * unsigned(hi - lo);
+    if (r == 0)
+      select_topp_kernel<4><<<grid, kThreads, 0, st>>>(a, lo, hi - lo);
+    else if (r == 1)
+      select_topp_kernel<8><<<grid, kThreads, 0, st>>>(a, lo, hi - lo);
+    else
+      select_topp_kernel<kPerThread><<<grid, kThreads, 0, st>>>(a, lo, hi - lo);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t st) {
