@@ -137,18 +137,21 @@ def job_value(flops_per_replica_step: float, world: int, steps: int, total_ms: f
 # summarised in profiles/prefill_attention_llama8b_128k.md.  It describes only
 # the kernel source with this SHA-256; for any other source it is not reported.
 FORWARD_TRAFFIC = {"workload": 3,
-                   "sha256": "3d2f4f2810b160e3f70b0bc8ccf5f13a3eddbb334167b009cac61bf42a4253ba",
-                   "bytes": 2536118784 + 1076756992}
+                   "sha256": {"prefill.cu": "3d2f4f2810b160e3f70b0bc8ccf5f13a3eddbb334167b009cac61bf42a4253ba",
+                              "plan.cpp": "876534d0d2ac8d9e33e0528bf3edf092a5487aa9d686c9017571918a2dd82811"},
+                   "bytes": 2493507584 + 1076896000,
+                   "group_shared_bytes": 1737392128 + 1070797056}
 
 
 def _forward_traffic(workload_number: int):
+    # the kernel and the schedule (its order sets what L2 catches) as captured
     import hashlib
 
-    src = os.path.join(ROOT, "head_heterogeneous_block_gb300", "csrc", "prefill.cu")
-    with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    ok = (FORWARD_TRAFFIC["sha256"] == digest and FORWARD_TRAFFIC["workload"] == workload_number)
-    return FORWARD_TRAFFIC["bytes"] if ok else None
+    for name, want in FORWARD_TRAFFIC["sha256"].items():
+        with open(os.path.join(ROOT, "head_heterogeneous_block_gb300", "csrc", name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != want:
+                return None
+    return FORWARD_TRAFFIC if FORWARD_TRAFFIC["workload"] == workload_number else None
 
 
 def _attention_flops(total_blocks: int, B: int, d: int) -> float:
@@ -437,6 +440,11 @@ def run_ours(args):
 
     peaks = _peaks()
     achieved = attn_flops / (fwd_ms * 1e-3) / 1e12
+    # DRAM bytes of one forward launch, from ncu, while the sources are the
+    # ones captured (else null)
+    traffic = _forward_traffic(args.workload)
+    if group_shared is not None:
+        group_shared["traffic"] = traffic["group_shared_bytes"] if traffic else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -453,7 +461,7 @@ def run_ours(args):
                      "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                      "peak_source": peaks["source"] + " bf16 burst",
-                     "traffic": _forward_traffic(args.workload),
+                     "traffic": traffic["bytes"] if traffic else None,
                      "algorithmic_flops_per_launch": attn_flops},
         "schedules": sched,
         "group_shared": group_shared,

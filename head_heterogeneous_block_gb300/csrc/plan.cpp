@@ -104,10 +104,12 @@ void build_schedule(const std::vector<int32_t>& budgets, int32_t nb, int32_t gro
     return;
   }
 
-  // Walk order: cost descending, ties by id; LPT_GROUPED first by KV group.
+  // Walk order: cost descending, ties by id; LPT_GROUPED first by KV group,
+  // and its ties by query block, then head (so a group's heads with equal
+  // budgets reach each query block together and share its K/V in L2).
   // Costs are integers in [0, nb], so a stable counting sort over the key
   // (group, nb - cost) -- the group part only for LPT_GROUPED -- walking the
-  // ids in ascending order gives exactly that order in linear time.
+  // ids in the tie order gives exactly that order in linear time.
   std::vector<int32_t> order(n);
   {
     const int32_t ngroups = policy == SA_SCHED_LPT_GROUPED ? (heads + group - 1) / group : 1;
@@ -123,7 +125,15 @@ void build_schedule(const std::vector<int32_t>& budgets, int32_t nb, int32_t gro
     }
     for (int64_t id = 0; id < n; ++id) ++start[keys[id] + 1];
     for (int64_t k = 0; k < nkeys; ++k) start[k + 1] += start[k];
-    for (int64_t id = 0; id < n; ++id) order[start[keys[id]]++] = int32_t(id);
+    if (policy == SA_SCHED_LPT_GROUPED) {
+      for (int32_t i = 0; i < nb; ++i)
+        for (int32_t h = 0; h < heads; ++h) {
+          const int64_t id = int64_t(h) * nb + i;
+          order[start[keys[id]]++] = int32_t(id);
+        }
+    } else {
+      for (int64_t id = 0; id < n; ++id) order[start[keys[id]]++] = int32_t(id);
+    }
   }
 
   // Least-loaded worker first; equal loads go to the lower worker id.  The

@@ -165,7 +165,8 @@ const char* sa_status_string(sa_status status);
  * Schedule (prefill): item (h, i) has id h*nb+i and cost min(k_h, i+1)
  * blocks; LPT walks items by cost descending (ties: lower id) and gives each
  * to the least-loaded worker (ties: lowest worker); LPT_GROUPED walks KV
- * group by KV group, cost descending inside a group; HEAD_ORDER gives worker
+ * group by KV group, cost descending inside a group, ties by query block
+ * then head; HEAD_ORDER gives worker
  * w the contiguous id range [w*N/W, (w+1)*N/W).  Plans with share_kv = 1
  * schedule head pairs instead: item (p, i) has id p*nb+i, covers heads 2p and
  * 2p+1, and costs 2*min(k_p, i+1) blocks (G/2 pairs per KV group).

@@ -137,8 +137,10 @@ def schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int 
                     greedy least-loaded assignment -- the pages' heuristic.
       "lpt_grouped" the same greedy, but items are walked KV group by KV group
                     (g = h // group ascending; within a group cost descending,
-                    ties lower id).  All workers then finish each group at
-                    nearly the same time.
+                    ties by query block i, then head).  All workers then
+                    finish each group at nearly the same time, and heads of a
+                    group with equal budgets (all of them, under
+                    group-shared selection) reach each query block together.
       "head_order"  the naive baseline of the Chinese summary ("电脑 1 拿头
                     1-4"): items in id order cut into W contiguous chunks of
                     equal count; chunk w is [w*N//W, (w+1)*N//W).
@@ -156,7 +158,7 @@ def schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int 
         order = sorted(range(n), key=lambda x: (-costs[x], x))
         lists, loads = lpt_assign(order, costs, workers)
     elif policy == "lpt_grouped":
-        order = sorted(range(n), key=lambda x: ((x // nb) // group, -costs[x], x))
+        order = sorted(range(n), key=lambda x: ((x // nb) // group, -costs[x], x % nb, x // nb))
         lists, loads = lpt_assign(order, costs, workers)
     else:
         raise ValueError(policy)

@@ -156,6 +156,41 @@ def test_schedule_is_a_partition(policy):
     assert sum(loads) == sum(costs)
 
 
+def test_lpt_grouped_walk_order_by_hand():
+    # one worker: its list is the walk order itself.  Two KV groups of two
+    # heads; group 0's heads share a budget (as under group-shared selection),
+    # group 1's differ.  Within a group: cost descending, then query block,
+    # then head.
+    nb, G = 4, 2
+    budgets = [3, 3, 2, 3]
+    wptr, items, _ = plan.schedule(budgets, nb, 1, "lpt_grouped", G)
+    assert wptr == [0, 2 * 2 * nb]
+    hi = [(x // nb, x % nb) for x in items]
+    assert hi == [
+        # group 0 (heads 0, 1): cost 3 at i = 2, 3 for both heads, then cost 2, 1
+        (0, 2), (1, 2), (0, 3), (1, 3), (0, 1), (1, 1), (0, 0), (1, 0),
+        # group 1 (head 2: budget 2, costs 1 2 2 2; head 3: budget 3, costs
+        # 1 2 3 3): cost 3, then the cost-2 items by query block, then cost 1
+        (3, 2), (3, 3), (2, 1), (3, 1), (2, 2), (2, 3), (2, 0), (3, 0),
+    ]
+
+
+def test_lpt_grouped_keeps_a_groups_heads_together():
+    # equal budgets in a group: at every cost, a worker's items of a group run
+    # in query-block order with the heads of each block together
+    r = random.Random(11)
+    H, nb, W, G = 8, 40, 3, 4
+    budgets = []
+    for _ in range(H // G):
+        budgets += [r.randint(2, nb)] * G
+    wptr, items, loads = plan.schedule(budgets, nb, W, "lpt_grouped", G)
+    costs = plan.item_costs(budgets, nb)
+    for w in range(W):
+        lst = items[wptr[w]:wptr[w + 1]]
+        keys = [((x // nb) // G, -costs[x], x % nb, x // nb) for x in lst]
+        assert keys == sorted(keys)
+
+
 def test_lpt_balances_better_than_head_order():
     r = random.Random(3)
     H, nb, W = 32, 256, 152
