@@ -156,39 +156,44 @@ def test_schedule_is_a_partition(policy):
     assert sum(loads) == sum(costs)
 
 
-def test_lpt_grouped_walk_order_by_hand():
-    # one worker: its list is the walk order itself.  Two KV groups of two
-    # heads; group 0's heads share a budget (as under group-shared selection),
-    # group 1's differ.  Within a group: cost descending, then query block,
-    # then head.
+def test_lpt_grouped_assignment_and_run_order_by_hand():
+    # two KV groups of two heads, two workers.  The greedy walks group 0 by
+    # cost descending, ties by query block then head, each item to the
+    # least-loaded worker (ties: the lower one); then group 1 from those
+    # loads.  Each worker then runs its items by (group, query block
+    # descending, head).
     nb, G = 4, 2
     budgets = [3, 3, 2, 3]
-    wptr, items, _ = plan.schedule(budgets, nb, 1, "lpt_grouped", G)
-    assert wptr == [0, 2 * 2 * nb]
+    # costs: head 0 and 1: 1 2 3 3; head 2: 1 2 2 2; head 3: 1 2 3 3
+    # group 0 walk: (0,2)3 (1,2)3 (0,3)3 (1,3)3 (0,1)2 (1,1)2 (0,0)1 (1,0)1
+    #   w0: (0,2) [3] (0,3) [6] (0,1) [8] (0,0) [9]
+    #   w1: (1,2) [3] (1,3) [6] (1,1) [8] (1,0) [9]
+    # group 1 walk: (3,2)3 (3,3)3 (2,1)2 (3,1)2 (2,2)2 (2,3)2 (2,0)1 (3,0)1
+    #   w0: (3,2) [12] (2,1) [14] (2,2) [16] (2,0) [17]
+    #   w1: (3,3) [12] (3,1) [14] (2,3) [16] (3,0) [17]
+    wptr, items, loads = plan.schedule(budgets, nb, 2, "lpt_grouped", G)
+    assert wptr == [0, 8, 16] and loads == [17, 17]
     hi = [(x // nb, x % nb) for x in items]
-    assert hi == [
-        # group 0 (heads 0, 1): cost 3 at i = 2, 3 for both heads, then cost 2, 1
-        (0, 2), (1, 2), (0, 3), (1, 3), (0, 1), (1, 1), (0, 0), (1, 0),
-        # group 1 (head 2: budget 2, costs 1 2 2 2; head 3: budget 3, costs
-        # 1 2 3 3): cost 3, then the cost-2 items by query block, then cost 1
-        (3, 2), (3, 3), (2, 1), (3, 1), (2, 2), (2, 3), (2, 0), (3, 0),
-    ]
+    assert hi[:8] == [(0, 3), (0, 2), (0, 1), (0, 0), (2, 2), (3, 2), (2, 1), (2, 0)]
+    assert hi[8:] == [(1, 3), (1, 2), (1, 1), (1, 0), (2, 3), (3, 3), (3, 1), (3, 0)]
 
 
-def test_lpt_grouped_keeps_a_groups_heads_together():
-    # equal budgets in a group: at every cost, a worker's items of a group run
-    # in query-block order with the heads of each block together
+def test_lpt_grouped_runs_a_groups_query_blocks_together():
+    # every worker runs its items by group, query block descending, head
     r = random.Random(11)
     H, nb, W, G = 8, 40, 3, 4
-    budgets = []
-    for _ in range(H // G):
-        budgets += [r.randint(2, nb)] * G
+    budgets = [r.randint(2, nb) for _ in range(H)]
     wptr, items, loads = plan.schedule(budgets, nb, W, "lpt_grouped", G)
-    costs = plan.item_costs(budgets, nb)
     for w in range(W):
         lst = items[wptr[w]:wptr[w + 1]]
-        keys = [((x // nb) // G, -costs[x], x % nb, x // nb) for x in lst]
+        keys = [((x // nb) // G, -(x % nb), x // nb) for x in lst]
         assert keys == sorted(keys)
+    # the loads are the greedy's over the grouped walk
+    costs = plan.item_costs(budgets, nb)
+    order = sorted(range(H * nb), key=lambda x: ((x // nb) // G, -costs[x], x % nb, x // nb))
+    lists, want = plan.lpt_assign(order, costs, W)
+    assert loads == want
+    assert [sorted(items[wptr[w]:wptr[w + 1]]) for w in range(W)] == [sorted(l) for l in lists]
 
 
 def test_lpt_balances_better_than_head_order():
