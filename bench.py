@@ -138,9 +138,9 @@ def job_value(flops_per_replica_step: float, world: int, steps: int, total_ms: f
 # the kernel source with this SHA-256; for any other source it is not reported.
 FORWARD_TRAFFIC = {"workload": 3,
                    "sha256": {"prefill.cu": "3d2f4f2810b160e3f70b0bc8ccf5f13a3eddbb334167b009cac61bf42a4253ba",
-                              "plan.cpp": "eb0b3bdf6653c81372397835929d3b01094432e5745ec400991d530a82c47bd6"},
-                   "bytes": 1987138816 + 1032702976,
-                   "group_shared_bytes": 1804212480 + 1031212800}
+                              "plan.cpp": "c616ba6a80c1066d0afaeaf52cd474c5e421f84c00f0bec29446911e2367f6d2"},
+                   "bytes": 1872382208 + 1081516544,
+                   "group_shared_bytes": 1739555072 + 1074110464}
 
 
 def _forward_traffic(workload_number: int):

@@ -227,16 +227,16 @@ void build_schedule(const std::vector<int32_t>& budgets, int32_t nb, int32_t gro
   std::vector<int32_t> fill(wptr.begin(), wptr.end() - 1);
   for (int64_t r = 0; r < n; ++r) items[fill[owner[r]]++] = order[r];
   if (policy == SA_SCHED_LPT_GROUPED) {
-    // Each worker runs its items by KV group, query block descending, then
-    // head: the assignment (and every load) is the greedy's, but all workers
-    // now sweep a group's query blocks together, so the blocks each sweep
-    // reads are still in L2 when the group's other heads need them.
+    // Each worker runs its items by KV group, query block, then head: the
+    // assignment (and every load) is the greedy's, but all workers now sweep
+    // a group's query blocks together, so the blocks each sweep reads are
+    // still in L2 when the group's other heads need them.
     for (int32_t w = 0; w < workers; ++w)
       std::sort(items.begin() + wptr[w], items.begin() + wptr[w + 1],
                 [&](int32_t a, int32_t b) {
                   const int32_t ha = a / nb, hb = b / nb;
                   if (ha / group != hb / group) return ha / group < hb / group;
-                  if (a - ha * nb != b - hb * nb) return a - ha * nb > b - hb * nb;
+                  if (a - ha * nb != b - hb * nb) return a - ha * nb < b - hb * nb;
                   return ha < hb;
                 });
   }

@@ -138,9 +138,9 @@ def schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int 
       "lpt_grouped" the same greedy, but items are walked KV group by KV group
                     (g = h // group ascending; within a group cost descending,
                     ties by query block i, then head).  Each worker then runs
-                    its items by (g, i descending, head): the assignment and
-                    the loads are the greedy's, and all workers sweep a
-                    group's query blocks together, its heads side by side.
+                    its items by (g, i, head): the assignment and the loads
+                    are the greedy's, and all workers sweep a group's query
+                    blocks together, its heads side by side.
       "head_order"  the naive baseline of the Chinese summary ("电脑 1 拿头
                     1-4"): items in id order cut into W contiguous chunks of
                     equal count; chunk w is [w*N//W, (w+1)*N//W).
@@ -160,7 +160,7 @@ def schedule(budgets: list[int], nb: int, workers: int, policy: str, group: int 
     elif policy == "lpt_grouped":
         order = sorted(range(n), key=lambda x: ((x // nb) // group, -costs[x], x % nb, x // nb))
         lists, loads = lpt_assign(order, costs, workers)
-        lists = [sorted(lst, key=lambda x: ((x // nb) // group, -(x % nb), x // nb))
+        lists = [sorted(lst, key=lambda x: ((x // nb) // group, x % nb, x // nb))
                  for lst in lists]
     else:
         raise ValueError(policy)

@@ -160,8 +160,7 @@ def test_lpt_grouped_assignment_and_run_order_by_hand():
     # two KV groups of two heads, two workers.  The greedy walks group 0 by
     # cost descending, ties by query block then head, each item to the
     # least-loaded worker (ties: the lower one); then group 1 from those
-    # loads.  Each worker then runs its items by (group, query block
-    # descending, head).
+    # loads.  Each worker then runs its items by (group, query block, head).
     nb, G = 4, 2
     budgets = [3, 3, 2, 3]
     # costs: head 0 and 1: 1 2 3 3; head 2: 1 2 2 2; head 3: 1 2 3 3
@@ -174,19 +173,19 @@ def test_lpt_grouped_assignment_and_run_order_by_hand():
     wptr, items, loads = plan.schedule(budgets, nb, 2, "lpt_grouped", G)
     assert wptr == [0, 8, 16] and loads == [17, 17]
     hi = [(x // nb, x % nb) for x in items]
-    assert hi[:8] == [(0, 3), (0, 2), (0, 1), (0, 0), (2, 2), (3, 2), (2, 1), (2, 0)]
-    assert hi[8:] == [(1, 3), (1, 2), (1, 1), (1, 0), (2, 3), (3, 3), (3, 1), (3, 0)]
+    assert hi[:8] == [(0, 0), (0, 1), (0, 2), (0, 3), (2, 0), (2, 1), (2, 2), (3, 2)]
+    assert hi[8:] == [(1, 0), (1, 1), (1, 2), (1, 3), (3, 0), (3, 1), (2, 3), (3, 3)]
 
 
 def test_lpt_grouped_runs_a_groups_query_blocks_together():
-    # every worker runs its items by group, query block descending, head
+    # every worker runs its items by group, query block, head
     r = random.Random(11)
     H, nb, W, G = 8, 40, 3, 4
     budgets = [r.randint(2, nb) for _ in range(H)]
     wptr, items, loads = plan.schedule(budgets, nb, W, "lpt_grouped", G)
     for w in range(W):
         lst = items[wptr[w]:wptr[w + 1]]
-        keys = [((x // nb) // G, -(x % nb), x // nb) for x in lst]
+        keys = [((x // nb) // G, x % nb, x // nb) for x in lst]
         assert keys == sorted(keys)
     # the loads are the greedy's over the grouped walk
     costs = plan.item_costs(budgets, nb)
