@@ -503,7 +503,7 @@ def bench_decode(dev, stream):
     # separate calls) gives the stage times; the default step (below) fuses
     # the retrieval heads' scoring and selection and overlaps the streaming heads
     step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
-                      device=dev, overlap=False, fused=False)
+                      device=dev, overlap=False, fused=False, one_launch=False)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step.build_cache(t["k"], stream=stream)
     for _ in range(3):
@@ -557,11 +557,12 @@ def bench_decode(dev, stream):
         torch.cuda.synchronize(dev)
         fz.append(e0.elapsed_time(e1))
 
-    def overlapped(fused):
+    def overlapped(fused, one_launch=False):
         # the streaming heads on a side stream beside the retrieval heads'
-        # scoring and selection (fused into one launch, or apart)
+        # scoring and selection (fused into one launch, or apart); or the
+        # whole step as one launch
         ov = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
-                        device=dev, fused=fused)
+                        device=dev, fused=fused, one_launch=one_launch)
         ov.build_cache(t["k"], stream=stream)
         for _ in range(3):
             ov(t["q"], t["k"], t["v"], stream=stream)
@@ -579,9 +580,13 @@ def bench_decode(dev, stream):
     ov, unfused_times = overlapped(False)
     unfused_status = int(ov.dev_status.item())
     del ov
-    ov, ov_times = overlapped(True)
+    ov, fused_times = overlapped(True)
+    unfused_status = max(unfused_status, int(ov.dev_status.item()))
+    del ov
+    # the default step: one launch
+    ov, ov_times = overlapped(True, one_launch=True)
     ov_status = max(unfused_status, int(ov.dev_status.item()))
-    # the overlapped step captured once in a CUDA graph and replayed, as a
+    # the default step captured once in a CUDA graph and replayed, as a
     # serving loop runs its decode steps
     graph_ms = None
     try:
@@ -636,9 +641,11 @@ def bench_decode(dev, stream):
     ov_ms = statistics.mean(ov_times)
     res = {"workload": w.name,
            "ms_per_step": round(ov_ms, 4),
-           "step": "DecodeStep default: streaming heads selected and attended on a side "
-                   "stream while the retrieval heads score and select (one fused launch) "
-                   "and attend",
+           "step": "DecodeStep default: one launch (sparse_attn_decode_step): per (sequence, "
+                   "KV group) a cluster scores and selects the retrieval heads, and each head "
+                   "is attended by the warpgroup that selected it; the streaming heads by "
+                   "the cluster's other warpgroups",
+           "overlapped_ms_per_step": round(statistics.mean(fused_times), 4),
            "unfused_ms_per_step": round(statistics.mean(unfused_times), 4),
            "score_select_ms": round(statistics.mean(fz), 4),
            "graph_ms_per_step": graph_ms,
@@ -658,8 +665,10 @@ def bench_decode(dev, stream):
            "step_floor_ms": round(step_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3, 4),
            "stages": "score_ms, select_ms and forward_ms time the serial step's kernels "
                      "between events (separate score and select calls); score_select_ms "
-                     "times the fused launch alone; ms_per_step and unfused_ms_per_step "
-                     "are means over 20 steps",
+                     "times the fused launch alone; ms_per_step (one launch), "
+                     "overlapped_ms_per_step (streaming heads on a side stream, the retrieval "
+                     "heads' scoring and selection fused) and unfused_ms_per_step (the same "
+                     "with separate score and select launches) are means over 20 steps",
            "kcache_pool_ms": round(a.elapsed_time(b), 4),
            "l2": "flushed between steps (a 256 MB read)"}
     del step

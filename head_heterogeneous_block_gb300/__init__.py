@@ -23,6 +23,7 @@ __all__ = [
     "sparse_attn_select_topp", "sparse_attn_pool_kcache_plan", "sparse_attn_score_plan",
     "sparse_attn_set_wait_limit", "sparse_attn_select_kind", "sparse_attn_forward_kind",
     "sparse_attn_score_select",
+    "sparse_attn_decode_step",
 ]
 
 SA_OK = 0
@@ -115,6 +116,8 @@ def _load():
                                                     I32, P, I32, P, P, I32, P]),
         "sparse_attn_score_select": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P, P,
                                                     I32, P]),
+        "sparse_attn_decode_step": (ctypes.c_int, [ctypes.POINTER(Shape), P, P, P, P, P, P, P,
+                                                   P, I32, P, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -328,6 +331,18 @@ def sparse_attn_forward(shape: Shape, plan, q, k, v, idx, cnt, kmax: int, o, lse
                                     _out_dtype(o, o_dtype), _ptr(lse), _ptr(dev_status),
                                     _stream(stream)),
            "sparse_attn_forward")
+
+
+def sparse_attn_decode_step(shape: Shape, plan: Plan, q, kbar, k, v, scores, idx, cnt, kmax: int,
+                            o, lse, dev_status, stream=None, o_dtype=None):
+    """Decode: the whole step (scores and selection of the retrieval heads,
+    the streaming heads' lists, every row's attention) in one launch
+    (``scores`` and ``lse`` may be None)."""
+    _check(_lib.sparse_attn_decode_step(ctypes.byref(shape), plan.handle, _ptr(q), _ptr(kbar),
+                                        _ptr(k), _ptr(v), _ptr(scores), _ptr(idx), _ptr(cnt),
+                                        kmax, _ptr(o), _out_dtype(o, o_dtype), _ptr(lse),
+                                        _ptr(dev_status), _stream(stream)),
+           "sparse_attn_decode_step")
 
 
 def sparse_attn_forward_kind(shape: Shape, plan: Plan, q, k, v, idx, cnt, kmax: int, o, lse,

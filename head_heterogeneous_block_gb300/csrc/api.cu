@@ -461,7 +461,7 @@ sa_status sparse_attn_score_select(const sa_shape* shp, const sa_plan* plan, con
     return SA_ERR_UNSUPPORTED;
   if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
   if (int32_t(plan->kinds.size()) == plan->n_streaming) return SA_OK;
-  sa_k::IndexSelectArgs a;
+  sa_k::IndexSelectArgs a = {};
   a.q = q;
   a.kbar = kbar;
   a.scores = scores;
@@ -485,6 +485,60 @@ sa_status sparse_attn_score_select(const sa_shape* shp, const sa_plan* plan, con
   }
   a.rows_per_cta = 0;
   return cuda_status(sa_k::launch_decode_index_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sa_status sparse_attn_decode_step(const sa_shape* shp, const sa_plan* plan, const void* q,
+                                  const float* kbar, const void* k, const void* v, float* scores,
+                                  int32_t* idx, int32_t* cnt, int32_t kmax, void* o,
+                                  int32_t o_dtype, float* lse, int32_t* dev_status,
+                                  sa_stream_t stream) {
+  sa_status s = sa_host::check_supported(shp);
+  if (s != SA_OK) return s;
+  if (!plan || shp->mode != SA_MODE_DECODE) return SA_ERR_INVALID_ARG;
+  if (!same_shape(shp, plan->shape)) return SA_ERR_SHAPE;
+  if (!q || !kbar || !k || !v || !idx || !cnt || !o || !dev_status) return SA_ERR_INVALID_ARG;
+  if (o_dtype != SA_DTYPE_BF16 && o_dtype != SA_DTYPE_F32) return SA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kbar) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (scores && !aligned16(scores)))
+    return SA_ERR_INVALID_ARG;
+  if (kmax < plan->kmax) return SA_ERR_SHAPE;
+  if (has_granularity(plan) || shp->head_dim != 128 || shp->block != 32 || plan->group > 16 ||
+      plan->nb > 4096)
+    return SA_ERR_UNSUPPORTED;
+  if (plan->device < 0) return SA_ERR_NOT_UPLOADED;
+  sa_k::IndexSelectArgs a = {};
+  a.q = q;
+  a.kbar = kbar;
+  a.scores = scores;
+  a.budgets = plan->d_budgets;
+  a.kinds = plan->d_kinds;
+  a.idx = idx;
+  a.cnt = cnt;
+  a.kmax = kmax;
+  a.Bt = shp->batch;
+  a.Hq = shp->num_q_heads;
+  a.Hkv = shp->num_kv_heads;
+  a.group = plan->group;
+  a.nb = plan->nb;
+  a.scale = float(1.0 / std::sqrt(double(shp->head_dim)));
+  a.max_retrieval = 0;
+  for (int32_t g = 0; g < shp->num_kv_heads; ++g) {
+    int32_t n = 0;
+    for (int32_t x = 0; x < plan->group; ++x)
+      n += plan->kinds[size_t(g) * plan->group + x] != SA_HEAD_STREAMING;
+    a.max_retrieval = std::max(a.max_retrieval, n);
+  }
+  a.rows_per_cta = 0;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.out_f32 = o_dtype == SA_DTYPE_F32;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  a.window_blocks = plan->window_blocks;
+  a.L = int32_t(shp->seq_len);
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  return cuda_status(sa_k::launch_decode_step(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

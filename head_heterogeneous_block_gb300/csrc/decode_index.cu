@@ -24,6 +24,14 @@
 //   3. A second cluster barrier, so no CTA exits while another reads its
 //      scores.
 //
+// The one-launch decode step (kAttend) goes on where the separate calls would
+// launch the attention: the warpgroup that selected a retrieval head attends
+// it at once (sa_da::attend_warp, the decode attention kernel's routine, with
+// one stage per warp in the chunk ring), and the group's streaming heads, whose
+// lists are block 0 and the last window_blocks blocks, are dealt to the other
+// warpgroups.  No head waits for the others' selection or for a launch, so
+// the heads that attend keep HBM busy while others still select.
+//
 // Every wait is a hardware barrier of the CTA or the cluster, whose CTAs the
 // cluster launch schedules together, or a cp.async group wait; no CTA spins
 // on memory another writes.  d = 128, G <= 16, nb <= 4096.
@@ -33,6 +41,7 @@
 
 #include <cstdint>
 
+#include "decode_attn.cuh"
 #include "index.cuh"
 #include "kernels.h"
 #include "sparse_attn.h"
@@ -48,17 +57,74 @@ constexpr int kRows = 64;           // pooled rows per chunk (32 KB)
 constexpr int kStages = 3;          // two chunks in flight
 constexpr int kStageBytes = kRows * 32 * 16;
 constexpr int kMaxGroup = 16;
+constexpr int kAttnStage = 2 * int(sa_da::kUnitBytes);   // one unit of K and V per warp
 
-// Dynamic shared memory: kStages chunk buffers, the group's queries
-// [G][32] uint2, the scores [max_retrieval][R] fp32 (a row per retrieval head
-// of the group, by its slot).  After scoring, the two warpgroups' gathered
-// score rows and scratch reuse the chunk buffers.
-size_t smem_bytes(int group, int max_retrieval, int rows_per_cta) {
-  return size_t(kStages) * kStageBytes + size_t(group) * 256 +
+// Dynamic shared memory: region 0, the group's queries [G][32] uint2, the
+// scores [max_retrieval][R] fp32 (a row per retrieval head of the group, by
+// its slot).  Region 0 holds the kStages chunk buffers while scoring; then
+// the two warpgroups' gathered score rows and selection scratch, and (with
+// kAttend) from attn_base on the eight warps' attention stages and the two
+// warpgroups' merge areas.
+__host__ __device__ constexpr int select_bytes(int per) {
+  return 2 * per * 128 * 4 + 2 * int(sizeof(sa_topk::Scratch));
+}
+__host__ __device__ constexpr int attn_base(int per) { return (select_bytes(per) + 127) / 128 * 128; }
+__host__ __device__ constexpr int region0_bytes(int per, bool attend) {
+  const int ring = kStages * kStageBytes;
+  const int att = attn_base(per) + 8 * kAttnStage + 2 * int(sizeof(sa_da::Merge));
+  return ((attend && att > ring ? att : ring) + 127) / 128 * 128;
+}
+size_t smem_bytes(int group, int max_retrieval, int rows_per_cta, int per, bool attend) {
+  return size_t(region0_bytes(per, attend)) + size_t(group) * 256 +
          size_t(max_retrieval) * size_t(rows_per_cta) * 4;
 }
 
-template <int kCP, int kPer>
+// The attention of decode row `row` by one warpgroup (warps wi = 0..3 of
+// warpgroup wg), once its list and count are written and the warpgroup has
+// passed its barrier: warp wg*4 + wi streams its units through its own stage
+// at `att` + (wg*4 + wi) * kAttnStage, and the four states are merged in the
+// warpgroup's merge area.
+__device__ __forceinline__ void attend_row(const sa_k::IndexSelectArgs& a, size_t row,
+                                           const uint2 (&qrow)[32], unsigned char* att,
+                                           uint64_t* afull, uint32_t& abase, int wg, int wi,
+                                           int lane, int gt, int bar) {
+  const int w8 = wg * 4 + wi;
+  int n = a.cnt[row];
+  if (n < 1 || n > a.kmax) {
+    if (gt == 0) atomicOr(a.dev_status, SA_DEV_BAD_COUNT);
+    n = max(1, min(n, a.kmax));
+  }
+  const int b = int(row / size_t(a.Hq)), h = int(row % size_t(a.Hq));
+  const size_t head_off = (size_t(b) * a.Hkv + h / a.group) * size_t(a.L) * sa_da::kD;
+  sa_da::Row r;
+  r.K = static_cast<const __nv_bfloat16*>(a.k) + head_off;
+  r.V = static_cast<const __nv_bfloat16*>(a.v) + head_off;
+  r.list = a.idx + row * a.kmax;
+  r.n = n;
+  r.gsz = sa_da::kB;
+  r.per = sa_da::kB / sa_da::kU;
+  r.nb = a.L / sa_da::kB;
+  r.limit = a.wait_ns ? a.wait_ns : sa_dev::kWaitLimitNs;
+  r.dev_status = a.dev_status;
+  // the query in fp32, exactly as bf16 widens
+  const uint2 qv = qrow[lane];
+  const float q4[4] = {__uint_as_float(qv.x << 16), __uint_as_float(qv.x & 0xFFFF0000u),
+                       __uint_as_float(qv.y << 16), __uint_as_float(qv.y & 0xFFFF0000u)};
+  auto sk = reinterpret_cast<uint2 (*)[sa_da::kU][32]>(att + w8 * kAttnStage);
+  auto sv = reinterpret_cast<uint2 (*)[sa_da::kU][32]>(att + w8 * kAttnStage + sa_da::kUnitBytes);
+  // the stage was last written or read by ordinary loads and stores (the
+  // chunk ring, or this warp's previous row)
+  sa_dev::fence_proxy_async_smem();
+  float m, l, o[4];
+  sa_da::attend_warp<1>(r, q4, sk, sv, &afull[w8], abase, wi, lane, sa_da::kScaleLog2, m, l, o);
+  sa_da::Merge& mg = reinterpret_cast<sa_da::Merge*>(att + 8 * kAttnStage)[wg];
+  sa_da::post_state(mg, wi, lane, m, l, o);
+  sa_topk::group_sync<128>(bar);
+  if (wi == 0) sa_da::merge_store(mg, lane, row, a.o, a.out_f32 != 0, a.lse);
+  sa_topk::group_sync<128>(bar);                // the merge area is reused by the next row
+}
+
+template <int kCP, int kPer, bool kAttend>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_index_select_kernel(sa_k::IndexSelectArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -73,30 +139,43 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t rmask = 0;
   for (int hh = 0; hh < G; ++hh)
     if (a.kinds[g * G + hh] != SA_HEAD_STREAMING) rmask |= 1u << hh;
-  if (rmask == 0) return;
+  if (!kAttend && rmask == 0) return;
 
   // the heads' budgets, read while the scores stream in; retrieval head
-  // number x of the group (in head order) is selected by CTA x % kCP,
-  // warpgroup (x / kCP) % 2
+  // number x of the group (in head order) has slot x, and (kAttend) the
+  // streaming heads follow in head order.  Slot x is taken by CTA x % kCP,
+  // warpgroup (x / kCP) % 2.
   __shared__ int32_t s_budget[kMaxGroup];
   __shared__ int32_t s_slot[kMaxGroup];
+  __shared__ uint64_t s_afull[8];               // (kAttend) a warp's attention stage
   if (tid < G) {
+    const uint32_t below = (1u << tid) - 1u;
     s_budget[tid] = a.budgets[g * G + tid];
-    s_slot[tid] = ((rmask >> tid) & 1u) ? __popc(rmask & ((1u << tid) - 1u)) : -1;
+    s_slot[tid] = ((rmask >> tid) & 1u)
+                      ? __popc(rmask & below)
+                      : (kAttend ? __popc(rmask) + __popc(~rmask & below) : -1);
   }
 
+  constexpr int kRegion0 = region0_bytes(kPer, kAttend);
   float4 (*stage)[kRows][32] = reinterpret_cast<float4 (*)[kRows][32]>(smem_raw);
-  uint2 (*qs)[32] = reinterpret_cast<uint2 (*)[32]>(smem_raw + kStages * kStageBytes);
-  float* sc = reinterpret_cast<float*>(smem_raw + kStages * kStageBytes + G * 256);
+  uint2 (*qs)[32] = reinterpret_cast<uint2 (*)[32]>(smem_raw + kRegion0);
+  float* sc = reinterpret_cast<float*>(smem_raw + kRegion0 + G * 256);
+  const uint2* qg = reinterpret_cast<const uint2*>(a.q) + (size_t(b) * a.Hq + g * G) * 32;
+  if constexpr (kAttend) {
+    // every CTA attends with the group's queries, whether or not it scores
+    if (tid < 8) sa_dev::mbar_init(&s_afull[tid], 1);
+    sa_dev::fence_mbar_init();
+    for (int e = tid; e < G * 32; e += kThreads) qs[e >> 5][e & 31] = qg[e];
+    __syncthreads();
+  }
 
   // ---- 1. scores of rows [r0, r0 + rows) for the retrieval heads
   const int r0 = rank * R;
   const int rows = max(0, min(nb - r0, R));
-  const int nch = (rows + kRows - 1) / kRows;
+  const int nch = rmask ? (rows + kRows - 1) / kRows : 0;
   const float4* kb = reinterpret_cast<const float4*>(a.kbar) + (size_t(pair) * nb + r0) * 32;
-  if (nch > 0) {
+  if (!kAttend && nch > 0) {
     // the queries join the first chunk's copy group
-    const uint2* qg = reinterpret_cast<const uint2*>(a.q) + (size_t(b) * a.Hq + g * G) * 32;
     for (int e = tid; e < G * 32; e += kThreads) cp_async8(&qs[e >> 5][e & 31], qg + e);
   }
   auto issue = [&](int c) {
@@ -134,18 +213,31 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // ---- 2. every CTA's scores are in its shared memory; up to 2 * kCP heads
   // are selected at once, each by 128 threads on the warpgroup's own named
-  // barrier
-  cluster.sync();
+  // barrier (a group without retrieval heads, which only attends, has no
+  // scores to share: the same for every CTA of the cluster)
+  if (rmask) cluster.sync();
   const int wg = warp >> 2, gt = tid & 127, bar = 1 + wg;
   float* srow = reinterpret_cast<float*>(smem_raw) + wg * (kPer * 128);
   sa_topk::Scratch& scr =
       reinterpret_cast<sa_topk::Scratch*>(smem_raw + 2 * kPer * 128 * 4)[wg];
-  const int i = nb - 1;                         // a retrieval row is the last block's
+  const int i = nb - 1;                         // a decode row is the last block's
+  uint32_t abase = 0;                           // this warp's units through its stage
   for (int hh = 0; hh < G; ++hh) {
     const int slot = s_slot[hh];
     if (slot < 0 || slot % kCP != rank || (slot / kCP) % 2 != wg) continue;
     const size_t row = size_t(b) * a.Hq + g * G + hh;
     int32_t* out = a.idx + row * a.kmax;
+    if (kAttend && !((rmask >> hh) & 1u)) {
+      // a streaming head: block 0 and blocks lo..i, ascending, padded with -1
+      const int lo = max(1, nb - a.window_blocks);
+      const int total = 1 + max(0, i - lo + 1);
+      for (int j = gt; j < a.kmax; j += 128) out[j] = j >= total ? -1 : (j == 0 ? 0 : lo + j - 1);
+      if (gt == 0) a.cnt[row] = min(total, a.kmax);
+      sa_topk::group_sync<128>(bar);
+      if constexpr (kAttend) attend_row(a, row, qs[hh], smem_raw + attn_base(kPer), s_afull,
+                                        abase, wg, warp & 3, lane, gt, bar);
+      continue;
+    }
     const int keep = min(s_budget[hh], i + 1);
     const int rest = keep - ((i == 0) ? 1 : 2);
     const int ncand = max(0, i - 1);            // blocks 1..i-1
@@ -177,15 +269,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (gt == 0) a.cnt[row] = min(total, a.kmax);
     sa_topk::group_sync<128>(bar);              // the row buffer is reused by the next head
+    if constexpr (kAttend) attend_row(a, row, qs[hh], smem_raw + attn_base(kPer), s_afull, abase,
+                                      wg, warp & 3, lane, gt, bar);
   }
 
   // ---- 3. no CTA leaves while another may still read its scores
-  cluster.sync();
+  if (rmask) cluster.sync();
 }
 
-template <int kCP, int kPer>
+template <int kCP, int kPer, bool kAttend>
 cudaError_t launch_with(const sa_k::IndexSelectArgs& a, int grid, size_t smem, cudaStream_t st) {
-  auto kern = decode_index_select_kernel<kCP, kPer>;
+  auto kern = decode_index_select_kernel<kCP, kPer, kAttend>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(smem));
   if (e != cudaSuccess) return e;
@@ -206,32 +300,49 @@ cudaError_t launch_with(const sa_k::IndexSelectArgs& a, int grid, size_t smem, c
   return cudaGetLastError();
 }
 
-}  // namespace
-
-namespace sa_k {
-
-cudaError_t launch_decode_index_select(const IndexSelectArgs& args, cudaStream_t st) {
+// Cluster size and rows per CTA, then the launch: four CTAs per group when
+// that fills the GPU, else eight; a warpgroup selects a row with 16
+// candidates per thread up to 2048 blocks, else 32.
+template <bool kAttend>
+cudaError_t launch_clusters(const sa_k::IndexSelectArgs& args, cudaStream_t st) {
   if (args.group < 1 || args.group > kMaxGroup || args.nb < 1 || args.nb > 4096)
     return cudaErrorInvalidValue;
   const long long pairs = (long long)args.Bt * args.Hkv;
   if (pairs == 0) return cudaSuccess;
   if (pairs > (1ll << 26)) return cudaErrorInvalidValue;
+  if (args.max_retrieval < (kAttend ? 0 : 1) || args.max_retrieval > args.group)
+    return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // four CTAs per group when that fills the GPU, else eight
   const int cp = pairs * 4 >= sms ? 4 : 8;
-  IndexSelectArgs a = args;
+  sa_k::IndexSelectArgs a = args;
   const int per = (a.nb + cp - 1) / cp;
   a.rows_per_cta = (per + kRows - 1) / kRows * kRows;
-  if (a.max_retrieval < 1 || a.max_retrieval > a.group) return cudaErrorInvalidValue;
-  const size_t smem = smem_bytes(a.group, a.max_retrieval, a.rows_per_cta);
   const int grid = int(pairs * cp);
-  // a warpgroup selects a row: 16 candidates per thread up to 2048 blocks, else 32
-  if (a.nb <= 16 * 128)
-    return cp == 4 ? launch_with<4, 16>(a, grid, smem, st) : launch_with<8, 16>(a, grid, smem, st);
-  return cp == 4 ? launch_with<4, 32>(a, grid, smem, st) : launch_with<8, 32>(a, grid, smem, st);
+  if (a.nb <= 16 * 128) {
+    const size_t smem = smem_bytes(a.group, a.max_retrieval, a.rows_per_cta, 16, kAttend);
+    return cp == 4 ? launch_with<4, 16, kAttend>(a, grid, smem, st)
+                   : launch_with<8, 16, kAttend>(a, grid, smem, st);
+  }
+  const size_t smem = smem_bytes(a.group, a.max_retrieval, a.rows_per_cta, 32, kAttend);
+  return cp == 4 ? launch_with<4, 32, kAttend>(a, grid, smem, st)
+                 : launch_with<8, 32, kAttend>(a, grid, smem, st);
+}
+
+}  // namespace
+
+namespace sa_k {
+
+cudaError_t launch_decode_index_select(const IndexSelectArgs& args, cudaStream_t st) {
+  return launch_clusters<false>(args, st);
+}
+
+cudaError_t launch_decode_step(const IndexSelectArgs& args, cudaStream_t st) {
+  if (args.L != args.nb * sa_da::kB || !args.k || !args.v || !args.o || !args.dev_status)
+    return cudaErrorInvalidValue;
+  return launch_clusters<true>(args, st);
 }
 
 }  // namespace sa_k

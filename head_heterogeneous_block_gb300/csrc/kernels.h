@@ -58,10 +58,24 @@ struct IndexSelectArgs {
   int32_t kmax;
   int32_t Bt, Hq, Hkv, group, nb;
   float scale;
-  int32_t max_retrieval;    // most retrieval heads in one KV group (>= 1)
+  int32_t max_retrieval;    // most retrieval heads in one KV group (>= 1; 0 with attend)
   int32_t rows_per_cta;
+  // launch_decode_step only: the attention of every head of the group
+  const void* k;            // [Bt][Hkv][L][128] bf16 keys
+  const void* v;
+  void* o;                  // [Bt*Hq][128], bf16 or fp32
+  int32_t out_f32;
+  float* lse;               // [Bt*Hq] or NULL
+  int32_t* dev_status;
+  int32_t window_blocks, L;
+  uint64_t wait_ns;         // limit of each wait for a copy (0: the 4 s default)
 };
 cudaError_t launch_decode_index_select(const IndexSelectArgs& a, cudaStream_t st);
+// The whole decode step of a plan without per-head block sizes in one launch:
+// the Index and Select of launch_decode_index_select, the streaming heads'
+// lists as launch_select writes them, and the attention of every row as
+// launch_decode_attention computes it (block size 32), bit for bit.
+cudaError_t launch_decode_step(const IndexSelectArgs& a, cudaStream_t st);
 
 struct SelectArgs {
   const float* scores;

@@ -15,6 +15,7 @@ from . import (SA_HEAD_RETRIEVAL, SA_HEAD_STREAMING, Shape, sparse_attn_forward,
                sparse_attn_forward_kind, sparse_attn_plan, sparse_attn_pool_kcache,
                sparse_attn_pool_kcache_plan, sparse_attn_score, sparse_attn_score_plan,
                sparse_attn_score_select, sparse_attn_score_workspace_size, sparse_attn_select,
+               sparse_attn_decode_step,
                sparse_attn_select_kind)
 
 
@@ -68,23 +69,30 @@ class DecodeStep:
     attention.  With ``granularity`` (and ``head_budget``) each retrieval head
     selects ``head_budget[h]`` blocks of ``granularity[h]`` tokens.
 
-    By default (``overlap``) the streaming heads, whose block lists do not
-    depend on the scores, are selected and attended on a side stream while
-    the retrieval heads score, select and attend on the caller's stream; the
-    step ends when both are done.  ``overlap=False`` runs the calls for every
-    head in turn on the caller's stream.  With ``fused`` (the default, for
-    plans without per-head block sizes) the retrieval heads' scores and
-    selection are one launch (``sparse_attn_score_select``); ``fused=False``
-    runs the score and select calls apart.  The results are the same; the
-    streaming heads' rows of ``scores`` are written only when not fused."""
+    By default (``one_launch``, for plans without per-head block sizes and
+    with 32-token blocks) the whole step is one launch
+    (``sparse_attn_decode_step``): each head is attended by the warpgroup
+    that selected it, as soon as its list is known.  Otherwise, with
+    ``overlap`` the streaming heads, whose block lists do not depend on the
+    scores, are selected and attended on a side stream while the retrieval
+    heads score, select and attend on the caller's stream; the step ends
+    when both are done.  ``overlap=False`` runs the calls for every head in
+    turn on the caller's stream.  With ``fused`` (plans without per-head
+    block sizes) the retrieval heads' scores and selection are one launch
+    (``sparse_attn_score_select``); ``fused=False`` runs the score and
+    select calls apart.  The results are the same bit for bit; the streaming
+    heads' rows of ``scores`` are written only when neither fused nor one
+    launch."""
 
     def __init__(self, shape: Shape, budget_blocks: int, head_kind, window_blocks: int,
                  device="cuda", with_lse: bool = False, out_dtype=torch.bfloat16,
-                 granularity=None, head_budget=None, overlap: bool = True, fused: bool = True):
+                 granularity=None, head_budget=None, overlap: bool = True, fused: bool = True,
+                 one_launch: bool = True):
         dev = torch.device(device)
         self.shape = shape
         self.overlap = overlap
         self.fused = fused and granularity is None
+        self.one_launch = one_launch and granularity is None and shape.block == 32
         if overlap:
             self.side = torch.cuda.Stream(device=dev)
         self.plan = sparse_attn_plan(shape, budget_blocks, head_kind=head_kind,
@@ -114,6 +122,11 @@ class DecodeStep:
 
     def __call__(self, q, k, v, out=None, stream=None):
         out = self.out if out is None else out
+        if self.one_launch:
+            sparse_attn_decode_step(self.shape, self.plan, q, self.kbar, k, v, self.scores,
+                                    self.idx, self.cnt, self.kmax, out, self.lse,
+                                    self.dev_status, stream=stream)
+            return out
         if self.overlap:
             return self._overlapped(q, k, v, out, stream)
         if self.fused:

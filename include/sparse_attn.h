@@ -351,6 +351,41 @@ sa_status sparse_attn_score_select(const sa_shape* shp, const sa_plan* plan, con
                                    int32_t* cnt, int32_t kmax, sa_stream_t stream);
 
 /*
+ * Decode plans without per-head block sizes, block size 32: the whole decode
+ * step in one launch.  The results are those of sparse_attn_score_select,
+ * sparse_attn_select_kind(SA_HEAD_STREAMING) and sparse_attn_forward, bit for
+ * bit: scores (retrieval rows, when scores is not NULL), idx and cnt (every
+ * row), o and lse (every row).  One thread-block cluster per (sequence, KV
+ * group) scores and selects the group's retrieval heads as
+ * sparse_attn_score_select does; the warpgroup that selected a head then
+ * attends it at once, and the group's streaming heads (block 0 and the last
+ * window_blocks blocks, "Riepilogo Tecnico: Fluxion", "Intuizioni Chiave" 2)
+ * are attended by the cluster's other warpgroups.  No head waits for a
+ * second launch, so attention reads overlap the other heads' selection.
+ *  - q: bf16 [Bt][Hq][128]; kbar: the pooled key cache (fp32
+ *    [Bt][Hkv][nb][128], sparse_attn_pool_kcache); k, v: bf16
+ *    [Bt][Hkv][L][128].
+ *  - scores: fp32 [Bt][Hq][nb] or NULL; idx [Bt*Hq][kmax], cnt [Bt*Hq]: as
+ *    sparse_attn_select writes them.
+ *  - o [Bt*Hq][128] in o_dtype (SA_DTYPE_BF16 or SA_DTYPE_F32); lse
+ *    (nullable) [Bt*Hq]; dev_status: as sparse_attn_forward (an out-of-range
+ *    count or index is flagged, a copy wait that passes the limit of
+ *    sparse_attn_set_wait_limit sets SA_DEV_TIMEOUT).
+ * All pointers are device pointers; q, kbar, k, v, o and scores 16-byte
+ * aligned.  The launch holds up to ~110 KB of shared memory per CTA (two CTAs
+ * per SM at the common shapes).
+ * Errors: INVALID_ARG (NULL pointers, misalignment, o_dtype, prefill plan),
+ * SHAPE (shape differs from the plan's, kmax too small), NOT_UPLOADED,
+ * UNSUPPORTED (per-head block sizes, block size other than 32, d != 128,
+ * Hq/Hkv > 16, nb > 4096), CUDA.
+ */
+sa_status sparse_attn_decode_step(const sa_shape* shp, const sa_plan* plan, const void* q,
+                                  const float* kbar, const void* k, const void* v, float* scores,
+                                  int32_t* idx, int32_t* cnt, int32_t kmax, void* o,
+                                  int32_t o_dtype, float* lse, int32_t* dev_status,
+                                  sa_stream_t stream);
+
+/*
  * Top-p selection, the data-dependent alternative the S-HPLB pages compare
  * against (Italian summary, "Sparsita' Eterogenea": an adaptive top-p budget
  * fixes accuracy but makes every head's work different).  Prefill only.

@@ -239,6 +239,38 @@ def test_device_calls_reject_bad_arguments_before_launch(sa):
     sized = sa.sparse_attn_plan(dshape, 8, head_kind=[1, 0] * 4, window_blocks=4, num_workers=1,
                                 granularity=[32, 16] * 4, head_budget=[8] * 8)
     assert ss(ds, sized.handle, P, P, P, P, P, sized.info()["kmax"], None) == 3
+    # the one-launch decode step: the fused call's checks, plus the attention's
+    # (k, v, o and the status word, the output type, block size 32)
+    st = lib.sparse_attn_decode_step
+    ok = (P, P, P, P, P, P, P, 16, P, 0, None, P, None)
+
+    def step(shape, plan_, *args):
+        return st(shape, plan_, *args)
+
+    assert step(ds, dplan.handle, *ok) == 8                                   # not uploaded
+    assert step(s, plan.handle, *ok) == 1                                     # prefill plan
+    assert step(ds, None, *ok) == 1
+    for i in (0, 1, 2, 3, 5, 6, 8, 11):                                      # q kbar k v idx cnt o st
+        bad = list(ok)
+        bad[i] = None
+        assert step(ds, dplan.handle, *bad) == 1, i
+    for i in (0, 1, 2, 3, 4, 8):                                             # q kbar k v scores o
+        bad = list(ok)
+        bad[i] = P + 4
+        assert step(ds, dplan.handle, *bad) == 1, i
+    bad = list(ok)
+    bad[9] = 3                                                               # output type
+    assert step(ds, dplan.handle, *bad) == 1
+    bad = list(ok)
+    bad[7] = 3                                                               # kmax below the plan's
+    assert step(ds, dplan.handle, *bad) == 2
+    assert step(ctypes.byref(sa.Shape.decode(4096, 32, 8, 2, 128, 2)), dplan.handle, *ok) == 2
+    ok64 = list(ok)
+    assert step(ctypes.byref(d64), p64.handle, *ok64) == 3                   # d = 64
+    assert step(ds, sized.handle, *ok[:7], sized.info()["kmax"], *ok[8:]) == 3
+    b64 = sa.Shape.decode(2048, 64, 8, 2, 128, 2)
+    p_b64 = sa.sparse_attn_plan(b64, 8, head_kind=[1, 0] * 4, window_blocks=4, num_workers=1)
+    assert step(ctypes.byref(b64), p_b64.handle, *ok) == 3                  # block size 64
     n = ctypes.c_size_t()
     assert lib.sparse_attn_score_workspace_size(s, ctypes.byref(n)) == 0
     assert n.value == (8 + 2) * 64 * 64 * 4

@@ -17,13 +17,13 @@ def env():
     return sa, torch
 
 
-def _decode(sa, torch, w, x, kinds, budget, window, out_dtype="float32"):
+def _decode(sa, torch, w, x, kinds, budget, window, out_dtype="float32", one_launch=False):
     from head_heterogeneous_block_gb300.layer import DecodeStep
     from tests._parity import to_dev
     shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
                             w.batch)
     step = DecodeStep(shape, budget, kinds, window, with_lse=True,
-                      out_dtype=getattr(torch, out_dtype))
+                      out_dtype=getattr(torch, out_dtype), one_launch=one_launch)
     t = {n: to_dev(x[n]) for n in "qkv"}
     step.build_cache(t["k"])
     out = step(t["q"], t["k"], t["v"])
@@ -81,8 +81,9 @@ def test_decode_small(env, L, Bt, budget, window):
     x = generate.decode_inputs(w)
     kinds = generate.head_kinds(w)
     for out_dtype in ("float32", "bfloat16"):
-        r = _decode(sa, torch, w, x, kinds, budget, window, out_dtype)
-        _check(w, x, r, kinds, budget, window, bf16_out=out_dtype == "bfloat16")
+        for one_launch in (False, True):
+            r = _decode(sa, torch, w, x, kinds, budget, window, out_dtype, one_launch)
+            _check(w, x, r, kinds, budget, window, bf16_out=out_dtype == "bfloat16")
 
 
 def test_decode_full_size(env):
@@ -93,10 +94,12 @@ def test_decode_full_size(env):
     kinds = generate.head_kinds(w)
     budget = w.budget_tokens // w.block
     window = w.window_tokens // w.block
-    # fp32 output at the plain tolerance, then bf16 output as well
+    # fp32 output at the plain tolerance, then bf16 output as well; the
+    # separate launches, then the one-launch step
     for out_dtype in ("float32", "bfloat16"):
-        r = _decode(sa, torch, w, x, kinds, budget, window, out_dtype)
-        _check(w, x, r, kinds, budget, window, bf16_out=out_dtype == "bfloat16")
+        for one_launch in (False, True):
+            r = _decode(sa, torch, w, x, kinds, budget, window, out_dtype, one_launch)
+            _check(w, x, r, kinds, budget, window, bf16_out=out_dtype == "bfloat16")
 
 
 def _decode_sized(sa, torch, w, x, kinds, gran, budget, window, out_dtype="float32"):
@@ -283,10 +286,11 @@ def test_decode_overlapped_step_equals_the_serial_step(env, case):
         kw = {"granularity": prof["gran"], "head_budget": prof["budget"]}
     t = {n: to_dev(x[n]) for n in "qkv"}
     res = []
-    for overlap, fused in ((False, False), (False, True), (True, False), (True, True)):
+    for overlap, fused, one in ((False, False, False), (False, True, False), (True, False, False),
+                                (True, True, False), (True, True, True)):
         step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
                           with_lse=True, out_dtype=torch.float32, overlap=overlap, fused=fused,
-                          **kw)
+                          one_launch=one, **kw)
         step.build_cache(t["k"])
         for _ in range(2):   # a second call on the same buffers changes nothing
             step.idx.fill_(-5)
@@ -301,10 +305,11 @@ def test_decode_overlapped_step_equals_the_serial_step(env, case):
             assert torch.equal(a, b)
 
 
-def test_decode_overlapped_step_replays_from_a_cuda_graph(env):
-    """The overlapped step (two streams, five launches) captured in a CUDA
-    graph: replays give the eager step's output and lists exactly, and the
-    calls allocate nothing while captured."""
+@pytest.mark.parametrize("one_launch", [False, True])
+def test_decode_overlapped_step_replays_from_a_cuda_graph(env, one_launch):
+    """The overlapped step (two streams, five launches), and the one-launch
+    step, captured in a CUDA graph: replays give the eager step's output and
+    lists exactly, and the calls allocate nothing while captured."""
     sa, torch = env
     from head_heterogeneous_block_gb300.layer import DecodeStep
     from tests._parity import to_dev
@@ -316,7 +321,8 @@ def test_decode_overlapped_step_replays_from_a_cuda_graph(env):
                             w.batch)
     t = {n: to_dev(x[n]) for n in "qkv"}
     step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
-                      with_lse=True, out_dtype=torch.float32, overlap=True)
+                      with_lse=True, out_dtype=torch.float32, overlap=True,
+                      one_launch=one_launch)
     step.build_cache(t["k"])
     want = step(t["q"], t["k"], t["v"]).clone()
     want_idx = step.idx.clone()
@@ -355,7 +361,7 @@ def test_decode_wait_timeout_is_reported_and_the_context_stays_usable(env):
                             w.batch)
     t = {n: to_dev(x[n]) for n in "qkv"}
     step = DecodeStep(shape, w.budget_tokens // w.block, kinds, w.window_tokens // w.block,
-                      out_dtype=torch.float32, overlap=False)
+                      out_dtype=torch.float32, overlap=False, one_launch=False)
     flush = torch.zeros(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     step.build_cache(t["k"])
     want = step(t["q"], t["k"], t["v"]).clone()
@@ -471,3 +477,125 @@ def test_score_select_with_no_retrieval_head_launches_nothing(env):
     sa.sparse_attn_score_select(shape, plan, q, kbar, sc, idx, cnt, kmax)
     torch.cuda.synchronize()
     assert torch.isnan(sc).all() and (idx == -7).all() and (cnt == -7).all()
+
+
+@pytest.mark.parametrize("L,Hq,Hkv,Bt,budget,window,case", [
+    (4096, 4, 4, 2, 9, 4, ""),            # groups of one head
+    (8192, 28, 4, 1, 64, 8, ""),          # one sequence: clusters of eight CTAs
+    (256, 8, 2, 2, 3, 2, ""),             # 8 blocks: most CTAs score nothing but attend
+    (2048, 8, 2, 2, 64, 2, ""),           # the budget keeps every block
+    (2048, 8, 2, 2, 16, 63, ""),          # the window reaches block 1: all blocks
+    (4096, 8, 2, 2, 20, 3, "zero_q"),     # zero queries: every score ties
+    (4096, 8, 2, 3, 16, 4, "group0"),     # KV group 0 all streaming: no scoring, attention only
+    (2048, 8, 2, 2, 16, 4, "all_streaming"),
+    (65536, 32, 4, 4, 64, 32, ""),        # groups of 8 heads
+    (131072, 16, 1, 1, 100, 16, ""),      # 4096 blocks; 16 heads, two per warpgroup
+    (65536, 28, 4, 16, 64, 64, ""),       # the 64K workload: clusters of four CTAs
+])
+def test_decode_step_one_launch_equals_separate_calls(env, L, Hq, Hkv, Bt, budget, window, case):
+    """The one-launch decode step gives the separate calls' (score, select,
+    forward) lists, counts, outputs and log-sum-exps bit for bit on every
+    row, and their scores on the retrieval rows, in fp32 and bf16 output."""
+    sa, torch = env
+    from tests._parity import to_dev
+    from workloads import generate, scaled, workload
+    w = scaled(workload(5), L, num_q_heads=Hq, num_kv_heads=Hkv, batch=Bt)
+    x = generate.decode_inputs(w)
+    kinds = generate.head_kinds(w)
+    G = Hq // Hkv
+    if case == "group0":
+        kinds[:G] = 1
+        kinds[G:] = [0, 1] * ((Hq - G) // 2)
+    elif case == "all_streaming":
+        kinds[:] = 1
+    nb = w.nb
+    shape = sa.Shape.decode(L, w.block, Hq, Hkv, w.head_dim, Bt)
+    plan = sa.sparse_attn_plan(shape, min(budget, nb), head_kind=kinds, window_blocks=window,
+                               num_workers=1)
+    plan.upload()
+    kmax = plan.info()["kmax"]
+    q, k, v = (to_dev(x[n]) for n in "qkv")
+    if case == "zero_q":
+        q.zero_()
+    kbar = torch.empty(Bt * Hkv * nb * w.head_dim, dtype=torch.float32, device="cuda")
+    sa.sparse_attn_pool_kcache(shape, k, kbar)
+    rows = Bt * Hq
+    ret = torch.tensor(np.tile(kinds != 1, Bt), device="cuda")
+    for dt in (torch.float32, torch.bfloat16):
+        def buffers():
+            return (torch.full((rows, nb), float("nan"), device="cuda"),
+                    torch.full((rows, kmax), -7, dtype=torch.int32, device="cuda"),
+                    torch.full((rows,), -7, dtype=torch.int32, device="cuda"),
+                    torch.full((rows, w.head_dim), float("nan"), dtype=dt, device="cuda"),
+                    torch.full((rows,), float("nan"), device="cuda"),
+                    torch.zeros(1, dtype=torch.int32, device="cuda"))
+        sc_a, idx_a, cnt_a, o_a, lse_a, st_a = buffers()
+        sa.sparse_attn_score(shape, q, kbar, sc_a, None, 0)
+        sa.sparse_attn_select(shape, plan, sc_a, idx_a, cnt_a, kmax)
+        sa.sparse_attn_forward(shape, plan, q, k, v, idx_a, cnt_a, kmax, o_a, lse_a, st_a)
+        sc_b, idx_b, cnt_b, o_b, lse_b, st_b = buffers()
+        sa.sparse_attn_decode_step(shape, plan, q, kbar, k, v, sc_b, idx_b, cnt_b, kmax, o_b,
+                                   lse_b, st_b)
+        _, idx_c, cnt_c, o_c, _, st_c = buffers()
+        sa.sparse_attn_decode_step(shape, plan, q, kbar, k, v, None, idx_c, cnt_c, kmax, o_c,
+                                   None, st_c)
+        torch.cuda.synchronize()
+        assert int(st_a.item()) == 0 and int(st_b.item()) == 0 and int(st_c.item()) == 0
+        assert torch.equal(sc_b[ret], sc_a[ret])
+        assert torch.isnan(sc_b[~ret]).all()
+        for idx, cnt, o in ((idx_b, cnt_b, o_b), (idx_c, cnt_c, o_c)):
+            assert torch.equal(idx, idx_a)
+            assert torch.equal(cnt, cnt_a)
+            assert torch.equal(o, o_a)
+        assert torch.equal(lse_b, lse_a)
+
+
+def test_decode_step_one_launch_wait_timeout_is_reported(env):
+    """The one-launch step's waits for its attention copies, limited to 1 ns,
+    run out: the launch reports SA_DEV_TIMEOUT and returns (each warp waits
+    with the full limit for the copies it issued, and the cluster barriers
+    are still met), and normal launches right after give the step's output
+    exactly."""
+    sa, torch = env
+    from tests._parity import to_dev
+    from workloads import generate, workload
+    w = workload(5)
+    x = generate.decode_inputs(w)
+    kinds = generate.head_kinds(w)
+    shape = sa.Shape.decode(w.seq_len, w.block, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                            w.batch)
+    plan = sa.sparse_attn_plan(shape, w.budget_tokens // w.block, head_kind=kinds,
+                               window_blocks=w.window_tokens // w.block, num_workers=1)
+    plan.upload()
+    kmax = plan.info()["kmax"]
+    q, k, v = (to_dev(x[n]) for n in "qkv")
+    rows, nb = w.batch * w.num_q_heads, w.nb
+    kbar = torch.empty(w.batch * w.num_kv_heads * nb * w.head_dim, dtype=torch.float32,
+                       device="cuda")
+    sa.sparse_attn_pool_kcache(shape, k, kbar)
+    idx = torch.empty(rows, kmax, dtype=torch.int32, device="cuda")
+    cnt = torch.empty(rows, dtype=torch.int32, device="cuda")
+    out = torch.empty(rows, w.head_dim, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.zeros(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def step():
+        st.zero_()
+        out.fill_(float("nan"))
+        sa.sparse_attn_decode_step(shape, plan, q, kbar, k, v, None, idx, cnt, kmax, out, None, st)
+        torch.cuda.synchronize()
+        return int(st.item())
+
+    assert step() == 0
+    want = out.clone()
+    try:
+        sa.sparse_attn_set_wait_limit(1)
+        flush.max()                    # the copies come from memory, not L2
+        got = step()
+    finally:
+        sa.sparse_attn_set_wait_limit(0)
+    assert got & sa.SA_DEV_TIMEOUT, got
+    assert not got & (sa.SA_DEV_BAD_INDEX | sa.SA_DEV_BAD_COUNT)
+    for _ in range(2):
+        assert step() == 0
+        assert torch.equal(out, want)
