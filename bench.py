@@ -425,6 +425,38 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
         return (time.perf_counter() - t0) / reps
 
+    # where a pipelined step's time goes: six more steps with timing events
+    # on the three streams (not timed above); per step the spans of copy-in,
+    # compute and copy-out, and the share of copy time that ran while the
+    # compute stream was busy
+    tl = []
+    pipe.run(steps_in[:6], stream=stream, timeline=tl)
+    torch.cuda.synchronize(dev)
+    t0 = tl[0]["in"][0]
+
+    def span(ev):
+        return t0.elapsed_time(ev[0]), t0.elapsed_time(ev[1])
+
+    comp_spans = [span(x["compute"]) for x in tl]
+
+    def hidden(a, b):
+        # ms of [a, b) that fall inside some compute span
+        return sum(max(0.0, min(b, ce) - max(a, cs)) for cs, ce in comp_spans)
+
+    copy_ms = hid_ms = 0.0
+    for x in tl:
+        for k in ("in", "out"):
+            a, b = span(x[k])
+            copy_ms += b - a
+            hid_ms += hidden(a, b)
+    last = max(span(x["out"])[1] for x in tl)
+    pipeline = {"steps": len(tl), "ms_per_step": round(last / len(tl), 3),
+                "copy_in_ms": round(statistics.mean(b - a for a, b in (span(x["in"]) for x in tl)), 3),
+                "compute_ms": round(statistics.mean(b - a for a, b in comp_spans), 3),
+                "copy_out_ms": round(statistics.mean(b - a for a, b in (span(x["out"]) for x in tl)), 3),
+                "copy_time_under_compute": round(hid_ms / copy_ms, 3) if copy_ms else None}
+    del tl
+
     link("both", 1)
     t_in, t_out, t_both = link("in"), link("out"), link("both")
     host_link = {"h2d_gbs": round(h2d / t_in / 1e9, 1), "d2h_gbs": round(d2h / t_out / 1e9, 1),
@@ -470,7 +502,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": round(e2e_s * 1e3, 3),
                 "overlap": "double-buffered: copies of one step overlap another's compute",
-                "host_link": host_link},
+                "host_link": host_link, "pipeline": pipeline},
         "gpu_launches": 5 * args.steps,
         "clocks": clk,
         "device_status": status,

@@ -200,11 +200,24 @@ class HostPipeline:
         self.copy_out = torch.cuda.Stream(dev)
         self.dev = dev
 
-    def run(self, steps, stream=None, before_step=None):
+    def run(self, steps, stream=None, before_step=None, timeline=None):
         """steps: iterable of (q, k, v, o) pinned host tensors; o receives the
         step's output.  before_step(s), if given, runs on the host before
-        step s is issued.  Returns once every output is on the host."""
+        step s is issued.  Returns once every output is on the host.
+        timeline: if a list, each step appends its copy-in, compute and
+        copy-out spans as (start, end) pairs of timing events recorded on the
+        three streams (events between operations; for diagnosis, not for the
+        timed steps)."""
         comp = torch.cuda.current_stream(self.dev) if stream is None else stream
+        timed = timeline is not None
+
+        def mark(st):
+            if not timed:
+                return None
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(st)
+            return e
+
         done = [None, None]       # compute of the last step that used each set
         read = [None, None]       # read-back of the last output of each set
         for s, (qh, kh, vh, oh) in enumerate(steps):
@@ -215,22 +228,28 @@ class HostPipeline:
             with torch.cuda.stream(self.copy_in):
                 if done[b] is not None:
                     self.copy_in.wait_event(done[b])
+                in0 = mark(self.copy_in)
                 buf["q"].copy_(qh, non_blocking=True)
                 buf["k"].copy_(kh, non_blocking=True)
                 buf["v"].copy_(vh, non_blocking=True)
-                copied = torch.cuda.Event()
+                copied = torch.cuda.Event(enable_timing=timed)
                 copied.record(self.copy_in)
             comp.wait_event(copied)
             if read[b] is not None:
                 comp.wait_event(read[b])
+            c0 = mark(comp)
             self.layer(buf["q"], buf["k"], buf["v"], out=buf["o"], stream=comp)
-            done[b] = torch.cuda.Event()
+            done[b] = torch.cuda.Event(enable_timing=timed)
             done[b].record(comp)
             with torch.cuda.stream(self.copy_out):
                 self.copy_out.wait_event(done[b])
+                out0 = mark(self.copy_out)
                 oh.copy_(buf["o"], non_blocking=True)
-                read[b] = torch.cuda.Event()
+                read[b] = torch.cuda.Event(enable_timing=timed)
                 read[b].record(self.copy_out)
+            if timed:
+                timeline.append({"in": (in0, copied), "compute": (c0, done[b]),
+                                 "out": (out0, read[b])})
         self.copy_out.synchronize()
         self.copy_in.synchronize()
         comp.synchronize()
