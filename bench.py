@@ -411,7 +411,7 @@ def run_ours(args):
     # the host link alone: one step's copies with no compute, each direction
     # by itself and both at once on the pipeline's two copy streams; the
     # larger of the both-at-once time and the device step bounds e2e
-    def link(direction, reps=3):
+    def link(direction, reps=3, out_buf=0):
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for _ in range(reps):
@@ -421,7 +421,7 @@ def run_ours(args):
                         pipe.bufs[0][n].copy_(host[n], non_blocking=True)
             if direction in ("out", "both"):
                 with torch.cuda.stream(pipe.copy_out):
-                    out_host[0].copy_(pipe.bufs[0]["o"], non_blocking=True)
+                    out_host[out_buf].copy_(pipe.bufs[0]["o"], non_blocking=True)
         torch.cuda.synchronize(dev)
         return (time.perf_counter() - t0) / reps
 
@@ -454,12 +454,17 @@ def run_ours(args):
                 "copy_in_ms": round(statistics.mean(b - a for a, b in (span(x["in"]) for x in tl)), 3),
                 "compute_ms": round(statistics.mean(b - a for a, b in comp_spans), 3),
                 "copy_out_ms": round(statistics.mean(b - a for a, b in (span(x["out"]) for x in tl)), 3),
+                # the two output buffers alternate: their copies apart
+                "copy_out_ms_by_buffer": [round(statistics.mean(
+                    b - a for a, b in (span(x["out"]) for x in tl[i::2])), 3) for i in (0, 1)],
                 "copy_time_under_compute": round(hid_ms / copy_ms, 3) if copy_ms else None}
     del tl
 
     link("both", 1)
     t_in, t_out, t_both = link("in"), link("out"), link("both")
+    t_out1 = link("out", out_buf=1)
     host_link = {"h2d_gbs": round(h2d / t_in / 1e9, 1), "d2h_gbs": round(d2h / t_out / 1e9, 1),
+                 "d2h_gbs_second_buffer": round(d2h / t_out1 / 1e9, 1),
                  "copies_ms_per_step": round(t_both * 1e3, 3),
                  "floor_ms_per_step": round(max(t_both * 1e3, ms_step), 3),
                  "bound": "host link" if t_both * 1e3 > ms_step else "device"}
